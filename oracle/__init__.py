@@ -1,0 +1,177 @@
+"""fp64 CPU oracle for the weight-only quantized matmul + AddRmsNorm and the INT4 pack.
+
+TEST INFRASTRUCTURE ONLY. The arithmetic lives in ``wq_oracle.c`` (plain C,
+fp64, OpenMP over n-chunks); this module builds it with gcc, loads it with
+ctypes and converts torch/numpy inputs to fp64 (an exact upcast for fp16/bf16).
+It shares nothing with the CUDA library and the CUDA library never imports it.
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference leg may use it.
+
+Pages followed (Ascend CANN operator docs): ``aclnnConvertWeightToINT4Pack``
+(function description: sparse INT32 -> dense INT4), ``aclnnDynamicQuant``
+(constraints: INT4 packs along the last dimension), and
+``aclnnWeightQuantMatmulAllReduceAddRmsNorm`` (function description: formula;
+constraints: scale/offset shapes, group size). Every function is pinned by
+``tests/test_oracle.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "wq_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``wq_oracle.c`` into ``liboracle.so`` (gcc, -O2, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-shared", "-fPIC", "-std=c11",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load(path=None):
+    global _lib
+    if _lib is None or path is not None:
+        if path is None:
+            build()
+        lib = ctypes.CDLL(path or _LIB)
+        P = ctypes.c_void_p
+        I = ctypes.c_int64
+        lib.wqo_pack_int4.argtypes = [P, I, I, P]
+        lib.wqo_unpack_int4.argtypes = [P, I, I, P]
+        lib.wqo_dequant.argtypes = [P, I, I, P, P, I, I, I, P]
+        lib.wqo_matmul_add_rmsnorm.argtypes = [P, I, I, P, I, P, P, I, I, I, P, P, P,
+                                               ctypes.c_double, P, P, P]
+        for f in (lib.wqo_pack_int4, lib.wqo_unpack_int4, lib.wqo_dequant,
+                  lib.wqo_matmul_add_rmsnorm):
+            f.restype = ctypes.c_int
+        if path is not None:
+            return lib
+        _lib = lib
+    return _lib
+
+
+class use_library:
+    """Context manager that points this module at another build of the oracle
+    source (used by the mutation tests, which plant mistakes in a copy of
+    ``wq_oracle.c`` and check that the pins catch them)."""
+
+    def __init__(self, path):
+        self.path = path
+
+    def __enter__(self):
+        global _lib
+        self._saved = _lib
+        _lib = _load(self.path)
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self._saved
+        return False
+
+
+def _f64(a):
+    """Exact upcast of a torch tensor / numpy array / scalar list to contiguous fp64."""
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor: fp16/bf16 -> fp64 is exact
+        a = a.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _i32(a):
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu").numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def pack_int4(v) -> np.ndarray:
+    """(K, N) int32 -> (K, N/2) uint8; column 2j -> bits 3:0, column 2j+1 -> bits 7:4."""
+    v = _i32(v)
+    K, N = v.shape
+    out = np.empty((K, N // 2), dtype=np.uint8)
+    rc = _load().wqo_pack_int4(_p(v), K, N, _p(out))
+    if rc:
+        raise ValueError(f"wqo_pack_int4 rejected shape {v.shape}")
+    return out
+
+
+def unpack_int4(b, N: int) -> np.ndarray:
+    """(K, N/2) uint8 -> (K, N) int32 in [-8, 7]."""
+    if hasattr(b, "detach"):
+        b = b.detach().to("cpu").numpy()
+    b = np.ascontiguousarray(np.asarray(b, dtype=np.uint8))
+    K = b.shape[0]
+    out = np.empty((K, N), dtype=np.int32)
+    rc = _load().wqo_unpack_int4(_p(b), K, N, _p(out))
+    if rc:
+        raise ValueError("wqo_unpack_int4 rejected its shape")
+    return out
+
+
+def _so_shape(S, N):
+    """(Gs, Ns) view of a scale/offset array: (1) -> (1,1); (N) -> (1,N); (G,N) stays."""
+    if S.ndim == 1:
+        return S.reshape(1, -1)
+    return S
+
+
+def dequant(q, scale, offset=None, group: int = 0) -> np.ndarray:
+    """W = q * S[r(k), c(n)] + O[r(k), c(n)] in fp64 (q is (K, N) int32)."""
+    q = _i32(q)
+    K, N = q.shape
+    S = _so_shape(_f64(scale), N)
+    O = None if offset is None else _so_shape(_f64(offset), N)
+    W = np.empty((K, N), dtype=np.float64)
+    rc = _load().wqo_dequant(_p(q), K, N, _p(np.ascontiguousarray(S)),
+                             _p(None if O is None else np.ascontiguousarray(O)),
+                             S.shape[0], S.shape[1], int(group), _p(W))
+    if rc:
+        raise ValueError("wqo_dequant rejected its arguments")
+    return W
+
+
+def matmul_add_rmsnorm(x1, q, scale, offset, bias, residual, gamma, eps: float,
+                       group: int = 0, rows=None):
+    """The fused operator in fp64. Returns (mm, y, normOut), each (R, N).
+
+    x1 is (M, K) (or (b, s, K)), q the (K, N) integer weights, residual (M, N)
+    (or (b, s, N)). ``rows`` selects a subset of the M rows (rows are
+    independent); the outputs then hold those rows in that order.
+    """
+    x = _f64(x1)
+    K = x.shape[-1]
+    x = x.reshape(-1, K)
+    q = _i32(q)
+    N = q.shape[1]
+    r = _f64(residual).reshape(-1, N)
+    if rows is not None:
+        rows = np.asarray(rows, dtype=np.int64)
+        x = np.ascontiguousarray(x[rows])
+        r = np.ascontiguousarray(r[rows])
+    M = x.shape[0]
+    S = np.ascontiguousarray(_so_shape(_f64(scale), N))
+    O = None if offset is None else np.ascontiguousarray(_so_shape(_f64(offset), N))
+    b = _f64(bias)
+    gm = _f64(gamma)
+    mm = np.empty((M, N)); y = np.empty((M, N)); no = np.empty((M, N))
+    rc = _load().wqo_matmul_add_rmsnorm(_p(x), M, K, _p(q), N, _p(S), _p(O),
+                                        S.shape[0], S.shape[1], int(group), _p(b), _p(r),
+                                        _p(gm), float(eps), _p(mm), _p(y), _p(no))
+    if rc:
+        raise ValueError(f"wqo_matmul_add_rmsnorm rejected its arguments (rc={rc})")
+    return mm, y, no

@@ -1,0 +1,177 @@
+/*
+ * Plain fp64 CPU oracle for the weight-only quantized matmul with fused
+ * residual-add + RMSNorm, and for the INT32 -> dense INT4 weight pack.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the independent checker for the CUDA
+ * library in weight_only_bit_pack_b300/. It shares no code, header, table or
+ * helper with it and must never be linked into, or called from, the product
+ * path. Only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline /
+ * --impl reference leg may load it.
+ *
+ * What it follows (page titles and sections of the Ascend CANN operator docs):
+ *   - aclnnConvertWeightToINT4Pack, "Function description": INT32 values that
+ *     hold 4-bit integers are re-laid out from sparse storage (one per int32)
+ *     to dense storage (two per byte).
+ *   - aclnnDynamicQuant, "Constraints": an INT4 output needs its last
+ *     dimension divisible by 2 and an INT32-packed output needs it divisible by
+ *     8, i.e. packing runs along the LAST dimension.
+ *   - aclnnWeightQuantMatmulAllReduceAddRmsNorm, "Function description",
+ *     formula: mm_out = allReduce(x1 @ (x2*antiquantScale + antiquantOffset)
+ *     + bias); y = mm_out + residual; normOut = y / RMS(y) * gamma with
+ *     RMS(y) = sqrt((1/d) * sum_i y_i^2 + epsilon).
+ *   - same page, "Constraints": antiquantScale is (1) per-tensor, (n)/(1,n)
+ *     per-channel, (ceil(k/groupSize), n) per-group; antiquantOffset has the
+ *     scale's shape.
+ *
+ * Readings where the pages are silent (each one is listed with its reason in
+ * the repository's design notes):
+ *   - nibble order: the element in even column 2j goes to bits 3:0 of byte j,
+ *     the element in column 2j+1 to bits 7:4.
+ *   - an INT32 outside [-8, 7] keeps its low four bits (two's complement
+ *     truncation), so the pack is defined for every input.
+ *   - the offset is added after scaling: W = q*S + O.
+ *   - per-group row r(k) = floor(k / g); the last group may be short.
+ *   - d in RMS is n, the last dimension of y; epsilon sits inside the sqrt.
+ *   - allReduce over one rank is the identity, so bias is added once.
+ *
+ * Everything is fp64 with no intermediate rounding. Each output element of the
+ * matmul is summed over k in ascending order. Rows are independent, so the
+ * caller may pass any subset of rows of x1/residual (row sampling).
+ *
+ * Parity status: every function here is pinned by tests/test_oracle.py
+ * (closed forms, library matmul, exhaustive nibble round trip, hand-worked
+ * cases). Nothing is "parity unpinned".
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <math.h>
+
+#define WQO_OK 0
+#define WQO_EINVAL 1
+#define WQO_ENOMEM 2
+
+/* Pack: v is (K, N) int32, row-major; out is (K, N/2) bytes. N must be even. */
+int wqo_pack_int4(const int32_t *v, int64_t K, int64_t N, uint8_t *out)
+{
+    if (K < 0 || N < 0 || (N % 2) != 0) return WQO_EINVAL;
+    for (int64_t k = 0; k < K; ++k) {
+        for (int64_t j = 0; j < N / 2; ++j) {
+            uint32_t lo = (uint32_t)v[k * N + 2 * j] & 0xFu;      /* even column */
+            uint32_t hi = (uint32_t)v[k * N + 2 * j + 1] & 0xFu;  /* odd column  */
+            out[k * (N / 2) + j] = (uint8_t)(lo | (hi << 4));
+        }
+    }
+    return WQO_OK;
+}
+
+/* Unpack: inverse of the pack for values in [-8, 7]. A nibble is read as a
+ * 4-bit two's complement integer. */
+int wqo_unpack_int4(const uint8_t *b, int64_t K, int64_t N, int32_t *out)
+{
+    if (K < 0 || N < 0 || (N % 2) != 0) return WQO_EINVAL;
+    for (int64_t k = 0; k < K; ++k) {
+        for (int64_t n = 0; n < N; ++n) {
+            uint8_t byte = b[k * (N / 2) + n / 2];
+            int32_t nib = (n % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+            out[k * N + n] = nib >= 8 ? nib - 16 : nib;
+        }
+    }
+    return WQO_OK;
+}
+
+/* Scale/offset element for weight (k, n).
+ * S and O are (Gs, Ns) row-major: Gs = 1 unless per-group; Ns = 1 for
+ * per-tensor, N otherwise. g = 0 means no grouping. */
+static double so_at(const double *T, int64_t Gs, int64_t Ns, int64_t g,
+                    int64_t k, int64_t n)
+{
+    int64_t r = (g > 0) ? k / g : 0;
+    int64_t c = (Ns == 1) ? 0 : n;
+    (void)Gs;
+    return T[r * Ns + c];
+}
+
+/* Antiquant: W = q * S + O (O absent -> 0). q and W are (K, N). */
+int wqo_dequant(const int32_t *q, int64_t K, int64_t N,
+                const double *S, const double *O, int64_t Gs, int64_t Ns,
+                int64_t g, double *W)
+{
+    if (K < 0 || N < 0 || Gs < 1 || Ns < 1) return WQO_EINVAL;
+    if (g > 0 && Gs != (K + g - 1) / g) return WQO_EINVAL;
+    if (g == 0 && Gs != 1) return WQO_EINVAL;
+    if (Ns != 1 && Ns != N) return WQO_EINVAL;
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t n = 0; n < N; ++n) {
+            double w = (double)q[k * N + n] * so_at(S, Gs, Ns, g, k, n);
+            if (O) w += so_at(O, Gs, Ns, g, k, n);
+            W[k * N + n] = w;
+        }
+    return WQO_OK;
+}
+
+/* The fused operator on M rows.
+ *   x1 (M, K), q (K, N) integer weights (unpacked values), S/O (Gs, Ns),
+ *   bias (N) or NULL, residual (M, N), gamma (N).
+ * Outputs (any may be NULL): mm (M, N) = x1 @ W + bias, y (M, N), normOut (M, N).
+ *
+ * The k-sum of every (m, n) runs in ascending k. W[k, :] is formed once per k
+ * and applied to every row (a loop order that leaves each sum's order as is).
+ * OpenMP threads split the n range; every element is still summed by one
+ * thread in ascending k. */
+int wqo_matmul_add_rmsnorm(const double *x1, int64_t M, int64_t K,
+                           const int32_t *q, int64_t N,
+                           const double *S, const double *O, int64_t Gs,
+                           int64_t Ns, int64_t g,
+                           const double *bias, const double *residual,
+                           const double *gamma, double eps,
+                           double *mm, double *y, double *normOut)
+{
+    if (M < 0 || K < 1 || N < 0 || Gs < 1 || Ns < 1 || g < 0) return WQO_EINVAL;
+    if (g > 0 && Gs != (K + g - 1) / g) return WQO_EINVAL;
+    if (g == 0 && Gs != 1) return WQO_EINVAL;
+    if (Ns != 1 && Ns != N) return WQO_EINVAL;
+    if (M == 0 || N == 0) return WQO_OK;
+
+    double *acc = (double *)calloc((size_t)(M * N), sizeof(double));
+    if (!acc) return WQO_ENOMEM;
+
+    const int64_t NB = 256; /* n-chunk handled by one thread at a time */
+    int64_t nchunks = (N + NB - 1) / NB;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t c = 0; c < nchunks; ++c) {
+        int64_t n0 = c * NB, n1 = n0 + NB < N ? n0 + NB : N;
+        double w[256];
+        for (int64_t k = 0; k < K; ++k) {
+            for (int64_t n = n0; n < n1; ++n) {
+                double wk = (double)q[k * N + n] * so_at(S, Gs, Ns, g, k, n);
+                if (O) wk += so_at(O, Gs, Ns, g, k, n);
+                w[n - n0] = wk;
+            }
+            for (int64_t m = 0; m < M; ++m) {
+                double xk = x1[m * K + k];
+                double *a = acc + m * N;
+                for (int64_t n = n0; n < n1; ++n) a[n] += xk * w[n - n0];
+            }
+        }
+    }
+
+    for (int64_t m = 0; m < M; ++m) {
+        double ss = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            double v = acc[m * N + n] + (bias ? bias[n] : 0.0);
+            if (mm) mm[m * N + n] = v;
+            double yv = v + residual[m * N + n];
+            acc[m * N + n] = yv;
+            ss += yv * yv;
+        }
+        double rms = sqrt(ss / (double)N + eps);
+        for (int64_t n = 0; n < N; ++n) {
+            double yv = acc[m * N + n];
+            if (y) y[m * N + n] = yv;
+            if (normOut) normOut[m * N + n] = yv / rms * gamma[n];
+        }
+    }
+    free(acc);
+    return WQO_OK;
+}

@@ -1,0 +1,70 @@
+"""Mutation check for the oracle's pins (CPU only).
+
+Each case plants one plausible mistake in a temporary copy of the oracle's C
+source, builds it, and re-runs the pins of tests/test_oracle.py against it. At
+least one pin must fail for every mistake; otherwise the pins would not pin.
+"""
+import inspect
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "wq_oracle.c")
+
+MUTATIONS = {
+    "nibble_order_swapped": ("(uint8_t)(lo | (hi << 4))", "(uint8_t)(hi | (lo << 4))"),
+    "unpack_unsigned": ("nib >= 8 ? nib - 16 : nib", "nib"),
+    "group_index_off_by_one": ("(g > 0) ? k / g : 0", "(g > 0) ? (k + 1) / g : 0"),
+    "channel_index_dropped": ("(Ns == 1) ? 0 : n", "0"),
+    "offset_scaled": ("if (O) wk += so_at(O, Gs, Ns, g, k, n);",
+                      "if (O) wk += so_at(O, Gs, Ns, g, k, n) * so_at(S, Gs, Ns, g, k, n);"),
+    "bias_dropped": ("(bias ? bias[n] : 0.0)", "0.0"),
+    "residual_dropped": ("double yv = v + residual[m * N + n];", "double yv = v;"),
+    "mean_over_wrong_dim": ("ss / (double)N + eps", "ss / (double)(N + 1) + eps"),
+    "eps_outside_sqrt": ("sqrt(ss / (double)N + eps)", "(sqrt(ss / (double)N) + eps)"),
+    "gamma_reversed": ("yv / rms * gamma[n]", "yv / rms * gamma[N - 1 - n]"),
+    "x_reversed_k": ("double xk = x1[m * K + k];", "double xk = x1[m * K + (K - 1 - k)];"),
+    "weight_row_shifted": ("double wk = (double)q[k * N + n]", "double wk = (double)q[((k + 1) % K) * N + n]"),
+}
+
+
+def _pin_functions():
+    out = []
+    for name, fn in inspect.getmembers(pins, inspect.isfunction):
+        if not name.startswith("test_"):
+            continue
+        marks = getattr(fn, "pytestmark", [])
+        params = [m for m in marks if m.name == "parametrize"]
+        if params:
+            argnames, values = params[0].args[0], params[0].args[1]
+            argnames = [a.strip() for a in argnames.split(",")]
+            for v in values:
+                v = v if isinstance(v, (tuple, list)) else (v,)
+                out.append((f"{name}{v}", fn, dict(zip(argnames, v))))
+        else:
+            out.append((name, fn, {}))
+    return out
+
+
+@pytest.mark.parametrize("mut", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(mut, tmp_path):
+    old, new = MUTATIONS[mut]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {mut} not found exactly once"
+    csrc = tmp_path / "mut.c"
+    csrc.write_text(src.replace(old, new))
+    so = tmp_path / "libmut.so"
+    subprocess.check_call(["gcc", "-O1", "-shared", "-fPIC", "-std=c11", "-o", str(so),
+                           str(csrc), "-lm"])
+    failed = []
+    with oracle.use_library(str(so)):
+        for name, fn, kw in _pin_functions():
+            try:
+                fn(**kw)
+            except Exception:  # noqa: BLE001 - any failure counts as caught
+                failed.append(name)
+    assert failed, f"no pin failed for planted mistake '{mut}'"
