@@ -1,0 +1,473 @@
+#!/usr/bin/env python
+"""Benchmark of the weight-only quantized matmul + AddRmsNorm on one B300.
+
+A step is one call of the fused operator (dequant-matmul + bias + residual +
+RMSNorm, through the C ABI) on one batch of seeded synthetic inputs whose packed
+INT4/INT8 weights are already resident, as a deployed layer's weights are. The
+INT32 -> INT4 pack runs once per weight; it is timed in the same run and
+reported under "pack".
+
+Default workload: the bf16 decode step, M = 8 (1 x 8) x K 4096 x N 4096, INT4
+per-group g = 128. ``--config`` picks another: tiny, w8a16, prefill,
+sweep:<M>, sweep_pt:<M>.
+
+L2: every step uses the next of R distinct input sets (weights included) whose
+total size exceeds twice the L2 size, so no step finds its weights in L2; a
+set larger than that is used alone.
+
+Timing: W eager warm-up steps, then the K timed steps are replayed from a CUDA
+graph (capture of the same C-ABI calls), bracketed by a barrier and a device
+synchronize, timed with CUDA events on the launching stream; max over ranks.
+``e2e`` repeats the K steps eagerly with the step's inputs copied from pinned
+host memory and both outputs copied back inside the timed region.
+
+Multi-GPU (torchrun): "replicas only" -- each rank runs its own copy of the
+workload, with no collective on the data path; value = all ranks' FLOPs / the
+slowest rank's time.
+
+``--impl reference`` times the fp64 CPU oracle (the plain restatement of the
+operator used by the tests) on a bounded row sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "dequant-GEMM+AddRmsNorm TFLOP/s, weight GB/s, % of B300 roofline"
+PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="decode")
+    ap.add_argument("--kernel", choices=["auto", "generic", "decode", "prefill"], default="auto")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pack", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ workload
+
+def make_problem(config: str, device):
+    from weight_only_bit_pack_b300 import inputs
+    if config in inputs.CONFIGS:
+        return inputs.CONFIGS[config](device)
+    if config.startswith("sweep_pt:"):
+        return inputs.sweep(int(config.split(":")[1]), per_tensor=True, device=device)
+    if config.startswith("sweep:"):
+        return inputs.sweep(int(config.split(":")[1]), device=device)
+    raise SystemExit(f"unknown config {config}")
+
+
+def default_steps(config: str) -> int:
+    return {"tiny": 2000, "decode": 20000, "w8a16": 200, "prefill": 40}.get(
+        config, 20000 if config.endswith(":1") or config.endswith(":16") else 100)
+
+
+def alg_bytes(p) -> dict:
+    """Algorithmic bytes of one call: every input read once, every output written once."""
+    dt = 2
+    w = p.K * p.N * p.wbits // 8
+    so = p.scale.numel() * dt * (2 if p.offset is not None else 1)
+    vec = p.N * dt * (2 if p.bias is not None else 1)
+    act = p.M * p.K * dt + p.M * p.N * dt * 3  # x1, residual, y, normOut
+    return {"weight": w, "scale_offset": so, "vectors": vec, "activations": act,
+            "total": w + so + vec + act}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except OSError:
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML while running."""
+
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown", 0x1: "gpu_idle"}
+
+    def __init__(self, device, period_s: float = 0.005):
+        self.samples = []
+        self.reasons = set()
+        self.period = period_s
+        self.stop_ev = threading.Event()
+        self.max_mhz = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            if not uuid.startswith("GPU-"):
+                uuid = "GPU-" + uuid
+            self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+        except Exception as e:  # noqa: BLE001
+            self.nv = None
+            self.err = str(e)
+        self.th = threading.Thread(target=self._run, daemon=True)
+
+    def _sample(self):
+        mhz = self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
+        r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+        self.samples.append(mhz)
+        for bit, name in self.REASONS.items():
+            if r & bit and name != "gpu_idle":
+                self.reasons.add(name)
+
+    def _run(self):
+        while not self.stop_ev.is_set():
+            try:
+                self._sample()
+            except Exception:  # noqa: BLE001
+                break
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.nv:
+            self.th.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.nv:
+            self.stop_ev.set()
+            self.th.join()
+            if not self.samples:
+                try:
+                    self._sample()
+                except Exception:  # noqa: BLE001
+                    pass
+
+    def summary(self):
+        if not self.nv:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.err}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return world, rank, local  # rank 0 alone runs the CPU oracle; no process group
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value: float) -> float:
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(p, target_flops: float):
+    """Row sample of the workload whose fp64 oracle cost is about target_flops."""
+    per_row = 2.0 * p.K * p.N
+    rows = max(1, min(p.M, int(target_flops // per_row)))
+    return list(range(rows))
+
+
+def run_oracle_rows(p, rows, cpu_cache):
+    import oracle
+    if "x2" not in cpu_cache:
+        cpu_cache["x2"] = p.x2.to("cpu").to(torch.int32)
+        for f in ("scale", "offset", "bias", "gamma"):
+            v = getattr(p, f)
+            cpu_cache[f] = None if v is None else v.to("cpu")
+        cpu_cache["x1"] = p.x1.reshape(-1, p.K)[: max(rows) + 1].to("cpu")
+        cpu_cache["res"] = p.residual.reshape(-1, p.N)[: max(rows) + 1].to("cpu")
+    c = cpu_cache
+    return oracle.matmul_add_rmsnorm(c["x1"][rows], c["x2"], c["scale"], c["offset"], c["bias"],
+                                     c["res"][rows], c["gamma"], p.eps, p.group)
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_baseline(p, seconds=10.0, max_reps=200):
+    rows = oracle_sample(p, 2e9)
+    cache = {}
+    run_oracle_rows(p, rows, cache)  # load + first call (untimed)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        run_oracle_rows(p, rows, cache)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or reps >= max_reps:
+            break
+    flops = 2.0 * len(rows) * p.K * p.N * reps
+    return {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+            "sample": f"{len(rows)} of {p.M} rows x {reps} repetitions ({el:.1f} s, fp64 C oracle)"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, world, rank, local):
+    import weight_only_bit_pack_b300 as wq
+    from weight_only_bit_pack_b300 import build as wqbuild
+    wqbuild.build()
+    dev = torch.device("cuda", local)
+    kernel = {"auto": 0, "generic": 1, "decode": 2, "prefill": 3}[args.kernel]
+    p = make_problem(args.config, dev)
+    K = args.steps if args.steps is not None else default_steps(args.config)
+    W = max(3, args.warmup)
+
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
+    # one packed weight, then R distinct copies of every input
+    w_src = p.x2
+    if p.wbits == 4:
+        w0 = wq.pack_int4(w_src)
+    else:
+        w0 = w_src.contiguous()
+    ab = alg_bytes(p)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = ab["total"]
+    R = 1 if set_bytes > 2 * l2 else int(math.ceil(2 * l2 / set_bytes)) + 1
+    R = max(1, min(R, 64))
+    sets = []
+    for i in range(R):
+        s = {"x1": p.x1.clone(), "w": w0.clone(), "scale": p.scale.clone(),
+             "offset": None if p.offset is None else p.offset.clone(),
+             "bias": None if p.bias is None else p.bias.clone(), "residual": p.residual.clone(),
+             "gamma": p.gamma.clone(), "y": torch.empty_like(p.residual),
+             "normOut": torch.empty_like(p.residual)}
+        sets.append(s)
+    ws_bytes = wq.matmul_add_rmsnorm_get_workspace(p.x1, w0, p.scale, p.offset, p.bias,
+                                                   p.residual, p.gamma, p.eps, p.group,
+                                                   kernel=kernel)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    chosen = int(wq.select_kernel(p.x1, w0, p.scale, p.offset, p.bias, p.residual, p.gamma, p.eps,
+                                  p.group)) if kernel == 0 else kernel
+
+    def step(i):
+        s = sets[i % R]
+        wq.matmul_add_rmsnorm(s["x1"], s["w"], s["scale"], s["offset"], s["bias"], s["residual"],
+                              s["gamma"], p.eps, p.group, y=s["y"], normOut=s["normOut"],
+                              workspace=ws, kernel=kernel, stream=stream)
+
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    # capture the K timed steps (in chunks so a graph stays small), replay once untimed
+    chunk = min(K, 1000)
+    graphs = []
+    done = 0
+    while done < K:
+        n = min(chunk, K - done)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(done, done + n):
+                step(i)
+        graphs.append(g)
+        done += n
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize(dev)
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev) as clk:
+        ev0.record(stream)
+        for g in graphs:
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    t_ms = ev0.elapsed_time(ev1)
+    t_ms = max_over_ranks(world, t_ms)
+    ms_step = t_ms / K
+    flops = 2.0 * p.M * p.K * p.N
+    tflops = flops / (ms_step * 1e-3) / 1e12 * world
+    w_gbs = ab["weight"] / (ms_step * 1e-3) / 1e9
+
+    # end-to-end: pinned host inputs -> device, call, outputs -> pinned host
+    e2e = None
+    if not args.no_e2e:
+        hx = [p.x1.cpu().pin_memory() for _ in range(2)]
+        hr = [p.residual.cpu().pin_memory() for _ in range(2)]
+        hy = torch.empty(p.residual.shape, dtype=p.residual.dtype).pin_memory()
+        hn = torch.empty(p.residual.shape, dtype=p.residual.dtype).pin_memory()
+        Ke = min(K, 2000 if ms_step < 0.1 else 50)
+        for i in range(W + Ke):
+            if i == W:
+                barrier(world)
+                torch.cuda.synchronize(dev)
+                ev0.record(stream)
+            s = sets[i % R]
+            s["x1"].copy_(hx[i % 2], non_blocking=True)
+            s["residual"].copy_(hr[i % 2], non_blocking=True)
+            step(i)
+            hy.copy_(s["y"], non_blocking=True)
+            hn.copy_(s["normOut"], non_blocking=True)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        te = max_over_ranks(world, ev0.elapsed_time(ev1)) / Ke
+        h2d = hx[0].numel() * hx[0].element_size() + hr[0].numel() * hr[0].element_size()
+        d2h = 2 * hy.numel() * hy.element_size()
+        e2e = {"value": flops / (te * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
+               "ms_per_step": te, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": Ke}
+
+    # INT32 -> INT4 pack of this workload's weight (once per weight in deployment)
+    pack = None
+    if not args.no_pack and p.wbits == 4:
+        out = torch.empty_like(w0)
+        for _ in range(3):
+            wq.pack_int4(w_src, out=out, stream=stream)
+        torch.cuda.synchronize(dev)
+        reps = 20
+        ev0.record(stream)
+        for _ in range(reps):
+            wq.pack_int4(w_src, out=out, stream=stream)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        tp = ev0.elapsed_time(ev1) / reps
+        pbytes = w_src.numel() * 4 + out.numel()
+        peaks, _src = load_peaks()
+        pack = {"ms": tp, "GB/s": pbytes / (tp * 1e-3) / 1e9, "bytes": pbytes,
+                "frac_of_measured_hbm": pbytes / (tp * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                "bit_exact": bool(torch.equal(out, w0))}
+
+    peaks, peak_src = load_peaks()
+    t_s = ms_step * 1e-3
+    bound_time_hbm = ab["total"] / (peaks["hbm_gbs"] * 1e9)
+    bound_time_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    if bound_time_hbm >= bound_time_tc:
+        roof = {"bound": "hbm", "achieved": ab["total"] / t_s / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / t_s / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else \
+        "fallback 6.4 TB/s / 1.8 PFLOP/s"
+    roof["kernel"] = ("the operator's launches of one step (matmul + epilogue), "
+                      f"kernel choice {['auto', 'generic', 'decode', 'prefill'][chosen]}")
+    roof["alg_bytes_per_launch"] = ab["total"]
+    roof["flops_per_launch"] = flops
+
+    kernels_per_call = {1: 2, 2: 2, 3: 1}.get(chosen, 2)
+    line = {
+        "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": {torch.bfloat16: "bf16", torch.float16: "f16"}[p.dtype],
+        "data": "synthetic (seeded; weights random INT4/INT8, activations N(0,1))",
+        "config": {"workload": p.name, "M": p.M, "K": p.K, "N": p.N, "wbits": p.wbits,
+                   "group": p.group, "offset": p.offset is not None, "bias": p.bias is not None,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": (f"rotating {R} distinct input sets, {R * set_bytes / 1e6:.0f} MB > 2x L2"
+                          if R > 1 else f"one input set of {set_bytes / 1e6:.0f} MB > 2x L2"),
+                   "timing": "CUDA graph replay of the K steps, CUDA events on the launch stream",
+                   "kernel": ["auto", "generic", "decode", "prefill"][chosen]},
+        "weight_GBps": w_gbs,
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": K * kernels_per_call,
+        "pack": pack,
+    }
+    if rank == 0:
+        line["clocks"] = clk.summary()
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(p)
+        elif not args.no_cpu_baseline:
+            line["cpu_baseline"] = None
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ reference arm (CPU oracle)
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    p = make_problem(args.config, "cpu")
+    K = args.steps if args.steps is not None else 10
+    W = max(3, args.warmup)
+    rows = oracle_sample(p, 1e9)
+    cache = {}
+    for _ in range(W):
+        run_oracle_rows(p, rows, cache)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        run_oracle_rows(p, rows, cache)
+    el = time.perf_counter() - t0
+    flops = 2.0 * len(rows) * p.K * p.N
+    val = flops * K / el / 1e12
+    sample = f"{len(rows)} of {p.M} rows per step (fp64 C oracle, OpenMP)"
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": el / K * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": p.name, "M": p.M, "K": p.K, "N": p.N, "rows_per_step": len(rows)},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores_used(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

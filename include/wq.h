@@ -1,0 +1,210 @@
+/*
+ * wq.h -- C ABI of the B300 (sm_103a) weight-only quantized matmul with a fused
+ * residual-add + RMSNorm epilogue, and of the INT32 -> dense INT4 weight pack.
+ *
+ * Operations (Ascend CANN operator pages they restate):
+ *   pack      aclnnConvertWeightToINT4Pack, "Function description": INT32 values
+ *             that hold 4-bit integers are re-laid out from sparse storage (one
+ *             per int32) to dense storage (two per byte), along the last
+ *             dimension (aclnnDynamicQuant, "Constraints": INT4 needs the last
+ *             dimension even, an INT32 view needs it divisible by 8).
+ *   matmul    aclnnWeightQuantMatmulAllReduceAddRmsNorm, "Function description",
+ *             formula:  mm_out  = x1 @ (x2 * antiquantScale + antiquantOffset) + bias
+ *                       y       = mm_out + residual
+ *                       normOut = y / sqrt(mean_n(y^2) + epsilon) * gamma
+ *             The page's allReduce runs over one rank here, i.e. it is the
+ *             identity. Shapes, dtypes and ranges follow that page's
+ *             "Constraints" section.
+ *
+ * Call shape: both operations are two-phase like the pages' aclnn APIs
+ * ("each operator has two calls"): *_get_workspace validates every argument and
+ * returns the workspace size; the second call re-validates (cheaply), then
+ * enqueues the work on `stream` and returns without waiting for it.
+ *
+ * Conventions for every function below:
+ *   - Tensors are dense, row-major, on the current CUDA device. `data` is a
+ *     device pointer; it may be NULL only when the tensor has zero elements.
+ *     Strided or transposed tensors are not accepted.
+ *   - The caller owns every buffer, the workspace and the stream. The library
+ *     allocates no device memory and keeps no state between calls (apart from a
+ *     thread-local error string for wq_last_error()).
+ *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream. Work is asynchronous on it; errors found by the GPU while it runs
+ *     are reported through the workspace status word (wq_read_device_status).
+ *   - A function returns WQ_OK or a wq_status code and, on error, enqueues
+ *     nothing. wq_last_error() then holds a one-line explanation.
+ *   - Calls on the same stream are ordered; calls that share a workspace must
+ *     not run concurrently on different streams.
+ */
+#ifndef WQ_H_
+#define WQ_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. WQ_INT4 is a logical type: a tensor of logical shape
+ * (..., N) stores its elements two per byte along the last dimension, N/2 bytes
+ * per row; the element in even column 2j sits in bits 3:0 of byte j and the
+ * element in column 2j+1 in bits 7:4 (the pages do not fix this order; this is
+ * the library's reading). Read as little-endian int32 words, element 8i+t of a
+ * row sits in bits 4t+3:4t of word i. */
+typedef enum wq_dtype {
+    WQ_F16 = 1,
+    WQ_BF16 = 2,
+    WQ_INT8 = 3,
+    WQ_INT4 = 4,
+    WQ_INT32 = 5
+} wq_dtype;
+
+/* Tensor descriptor (the analogue of aclTensor): pointer, element type, rank
+ * (1..3) and logical shape. Unused trailing shape entries are ignored. */
+typedef struct wq_tensor {
+    void *data;
+    int32_t dtype;      /* a wq_dtype value */
+    int32_t ndim;       /* 1, 2 or 3 */
+    int64_t shape[3];
+} wq_tensor;
+
+typedef enum wq_status {
+    WQ_OK = 0,
+    WQ_ERR_NULL = 1,           /* a required pointer is NULL */
+    WQ_ERR_DTYPE = 2,          /* an element type is not allowed */
+    WQ_ERR_SHAPE = 3,          /* ranks, dimensions or ranges disagree */
+    WQ_ERR_GROUP = 4,          /* group size not allowed for the scale shape */
+    WQ_ERR_WORKSPACE = 5,      /* workspace NULL or smaller than required */
+    WQ_ERR_UNSUPPORTED = 6,    /* a forced kernel cannot run this problem */
+    WQ_ERR_CUDA = 7,           /* a CUDA runtime call or kernel launch failed */
+    WQ_ERR_DEVICE_TIMEOUT = 8, /* a bounded device-side wait gave up (see below) */
+    WQ_ERR_ALIAS = 9           /* an output overlaps an input it must not overlap */
+} wq_status;
+
+/* Kernel selection for the *_ex entry points. WQ_KERNEL_AUTO is what the plain
+ * entry points use: DECODE for small M, PREFILL for large M when the shapes
+ * meet its alignment rules, GENERIC otherwise. */
+typedef enum wq_kernel {
+    WQ_KERNEL_AUTO = 0,
+    WQ_KERNEL_GENERIC = 1,     /* predicated CUDA-core kernel, any shape */
+    WQ_KERNEL_DECODE = 2,      /* weight-streaming mma.sync kernel, small M */
+    WQ_KERNEL_PREFILL = 3      /* TMA + tcgen05/TMEM kernel, large M */
+} wq_kernel;
+
+/* ------------------------------------------------------------------ pack */
+
+/* First phase of the pack (aclnnConvertWeightToINT4Pack).
+ *   weight       WQ_INT32, 2-D (K, N), N even, K >= 0, N >= 0. Values should lie
+ *                in [-8, 7]; any other value keeps its low four bits (two's
+ *                complement truncation).
+ *   weight_int4  WQ_INT4, 2-D, logical shape (K, N), i.e. K*N/2 bytes.
+ *   ws_bytes     out: workspace bytes the second phase needs (always 0).
+ * Errors: WQ_ERR_NULL, WQ_ERR_DTYPE, WQ_ERR_SHAPE. Touches no device memory. */
+int32_t wq_pack_int4_get_workspace(const wq_tensor *weight, const wq_tensor *weight_int4,
+                                   uint64_t *ws_bytes);
+
+/* Second phase: enqueue the pack on `stream`. The output must not overlap the
+ * input (WQ_ERR_ALIAS). K*N == 0 enqueues nothing. The result is bit-exact and
+ * deterministic. `ws` may be NULL when ws_bytes is 0. */
+int32_t wq_pack_int4(const wq_tensor *weight, const wq_tensor *weight_int4,
+                     void *ws, uint64_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------ matmul */
+
+/* First phase of the fused operator (aclnnWeightQuantMatmulAllReduceAddRmsNorm).
+ *   x1        WQ_F16 or WQ_BF16, (M, K) or (b, s, K) with M = b*s; 0 <= M < 2^31,
+ *             1 <= K <= 65535. Not transposed.
+ *   x2        WQ_INT8 (K, N) or WQ_INT4 (K, N) packed as described above (N even);
+ *             0 <= N <= 65535. Not transposed.
+ *   scale     antiquantScale, x1's dtype: (1) per-tensor, (N) or (1, N)
+ *             per-channel, (ceil(K/group), N) per-group.
+ *   offset    antiquantOffset or NULL; if given, the scale's shape and dtype.
+ *             The dequantized weight is W[k][n] = x2[k][n] * S + O, where S and O
+ *             are taken at row floor(k/group) (per-group) or 0, column n or 0.
+ *   bias      NULL or (N), x1's dtype.
+ *   residual  (M, N) or (b, s, N) with b*s = M, x1's dtype.
+ *   gamma     (N), x1's dtype.
+ *   eps       epsilon inside the square root, >= 0.
+ *   group     0 for per-tensor / per-channel scales; otherwise the group size:
+ *             a multiple of 32 with 32 <= group <= K - 1, and then the scale
+ *             must be (ceil(K/group), N).
+ *   y         out, residual's shape and dtype. It MAY be the residual buffer
+ *             itself (the page's in-place variant writes y into residual); any
+ *             other overlap with an input is rejected.
+ *   normOut   out, residual's shape and dtype; must not overlap any input or y.
+ *   ws_bytes  out: bytes of device workspace the second phase needs.
+ * Errors: WQ_ERR_NULL, WQ_ERR_DTYPE, WQ_ERR_SHAPE (K = 0 included), WQ_ERR_GROUP,
+ * WQ_ERR_ALIAS. M = 0 or N = 0 is valid and the second phase enqueues nothing.
+ * Touches no device memory. */
+int32_t wq_matmul_add_rmsnorm_get_workspace(
+    const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scale,
+    const wq_tensor *offset, const wq_tensor *bias, const wq_tensor *residual,
+    const wq_tensor *gamma, double eps, int64_t group,
+    const wq_tensor *y, const wq_tensor *normOut, uint64_t *ws_bytes);
+
+/* Second phase: enqueue the fused operator on `stream`.
+ *   ws / ws_bytes  device workspace of at least the size the first phase
+ *                  returned for the same arguments (WQ_ERR_WORKSPACE otherwise).
+ *                  Its contents on entry do not matter; it holds partial sums,
+ *                  counters and the device status word, and is overwritten.
+ * Accumulation is fp32; y feeds the norm unrounded and y/normOut are rounded
+ * once to x1's dtype. Results are bitwise identical from run to run for the
+ * same arguments (no floating-point atomics; fixed reduction order). */
+int32_t wq_matmul_add_rmsnorm(
+    const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scale,
+    const wq_tensor *offset, const wq_tensor *bias, const wq_tensor *residual,
+    const wq_tensor *gamma, double eps, int64_t group,
+    const wq_tensor *y, const wq_tensor *normOut,
+    void *ws, uint64_t ws_bytes, void *stream);
+
+/* Same two phases with an explicit kernel choice (a wq_kernel value). A forced
+ * kernel that cannot run the given shapes returns WQ_ERR_UNSUPPORTED. The
+ * workspace size depends on the kernel, so pass the same `kernel` to both. */
+int32_t wq_matmul_add_rmsnorm_get_workspace_ex(
+    const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scale,
+    const wq_tensor *offset, const wq_tensor *bias, const wq_tensor *residual,
+    const wq_tensor *gamma, double eps, int64_t group,
+    const wq_tensor *y, const wq_tensor *normOut, int32_t kernel, uint64_t *ws_bytes);
+
+int32_t wq_matmul_add_rmsnorm_ex(
+    const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scale,
+    const wq_tensor *offset, const wq_tensor *bias, const wq_tensor *residual,
+    const wq_tensor *gamma, double eps, int64_t group,
+    const wq_tensor *y, const wq_tensor *normOut, int32_t kernel,
+    void *ws, uint64_t ws_bytes, void *stream);
+
+/* Which kernel WQ_KERNEL_AUTO picks for these arguments (a wq_kernel value),
+ * or a negative wq_status if the arguments are invalid. Host only. */
+int32_t wq_matmul_add_rmsnorm_select_kernel(
+    const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scale,
+    const wq_tensor *offset, const wq_tensor *bias, const wq_tensor *residual,
+    const wq_tensor *gamma, double eps, int64_t group,
+    const wq_tensor *y, const wq_tensor *normOut);
+
+/* ------------------------------------------------------------------ status */
+
+/* Device status word of a workspace after the work enqueued on `stream` has
+ * finished: synchronizes `stream`, copies the word to the host and stores it in
+ * *device_status (0 = no device-side error; otherwise WQ_ERR_DEVICE_TIMEOUT in
+ * the low 8 bits and the place that gave up in the upper bits). A kernel whose
+ * bounded wait for other thread blocks runs out stops waiting, sets this word,
+ * skips the dependent writes and exits, so the CUDA context stays usable.
+ * Returns WQ_ERR_NULL, WQ_ERR_WORKSPACE (ws_bytes < 16) or WQ_ERR_CUDA on
+ * failure. */
+int32_t wq_read_device_status(const void *ws, uint64_t ws_bytes, void *stream,
+                              int32_t *device_status);
+
+/* Static description of a status code ("WQ_OK", "WQ_ERR_SHAPE", ...). */
+const char *wq_status_string(int32_t status);
+
+/* Thread-local detail of the last error returned on this thread ("" if none). */
+const char *wq_last_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t wq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WQ_H_ */

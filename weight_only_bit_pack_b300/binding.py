@@ -1,0 +1,215 @@
+"""ctypes binding of ``libwq.so`` (the C ABI declared in ``include/wq.h``).
+
+Argument marshalling only: torch tensors become ``wq_tensor`` descriptors, the
+current CUDA stream is passed as ``cudaStream_t``, and every status code other
+than ``WQ_OK`` raises :class:`WQError`. No computation happens here and there
+is no fallback: if the library cannot be loaded, importing this module raises.
+
+Tensor conventions: fp16/bf16 tensors map to WQ_F16/WQ_BF16, ``torch.int8`` to
+WQ_INT8, ``torch.int32`` to WQ_INT32, and a ``torch.uint8`` tensor of shape
+(K, N/2) is read as packed WQ_INT4 of logical shape (K, N).
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libwq.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"libwq.so is missing at {_LIB_PATH}; build it with "
+                      "`python -m weight_only_bit_pack_b300.build` (there is no CPU fallback)")
+lib = ctypes.CDLL(_LIB_PATH)
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    ERR_NULL = 1
+    ERR_DTYPE = 2
+    ERR_SHAPE = 3
+    ERR_GROUP = 4
+    ERR_WORKSPACE = 5
+    ERR_UNSUPPORTED = 6
+    ERR_CUDA = 7
+    ERR_DEVICE_TIMEOUT = 8
+    ERR_ALIAS = 9
+
+
+class Kernel(enum.IntEnum):
+    AUTO = 0
+    GENERIC = 1
+    DECODE = 2
+    PREFILL = 3
+
+
+class DType(enum.IntEnum):
+    F16 = 1
+    BF16 = 2
+    INT8 = 3
+    INT4 = 4
+    INT32 = 5
+
+
+class WQError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = Status(status) if status in Status._value2member_map_ else status
+        super().__init__(f"{lib.wq_status_string(status).decode()}: {detail}")
+
+
+class WqTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 3)]
+
+
+_P = ctypes.POINTER(WqTensor)
+_T = [_P] * 7 + [ctypes.c_double, ctypes.c_int64, _P, _P]
+lib.wq_pack_int4_get_workspace.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint64)]
+lib.wq_pack_int4.argtypes = [_P, _P, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
+lib.wq_matmul_add_rmsnorm_get_workspace.argtypes = _T + [ctypes.POINTER(ctypes.c_uint64)]
+lib.wq_matmul_add_rmsnorm.argtypes = _T + [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
+lib.wq_matmul_add_rmsnorm_get_workspace_ex.argtypes = _T + [ctypes.c_int32,
+                                                            ctypes.POINTER(ctypes.c_uint64)]
+lib.wq_matmul_add_rmsnorm_ex.argtypes = _T + [ctypes.c_int32, ctypes.c_void_p, ctypes.c_uint64,
+                                              ctypes.c_void_p]
+lib.wq_matmul_add_rmsnorm_select_kernel.argtypes = _T
+lib.wq_read_device_status.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p,
+                                      ctypes.POINTER(ctypes.c_int32)]
+lib.wq_status_string.argtypes = [ctypes.c_int32]
+lib.wq_status_string.restype = ctypes.c_char_p
+lib.wq_last_error.argtypes = []
+lib.wq_last_error.restype = ctypes.c_char_p
+for _f in ("wq_pack_int4_get_workspace", "wq_pack_int4", "wq_matmul_add_rmsnorm_get_workspace",
+           "wq_matmul_add_rmsnorm", "wq_matmul_add_rmsnorm_get_workspace_ex",
+           "wq_matmul_add_rmsnorm_ex", "wq_matmul_add_rmsnorm_select_kernel",
+           "wq_read_device_status", "wq_version"):
+    getattr(lib, _f).restype = ctypes.c_int32
+
+_TORCH2WQ = {torch.float16: DType.F16, torch.bfloat16: DType.BF16, torch.int8: DType.INT8,
+             torch.uint8: DType.INT4, torch.int32: DType.INT32}
+
+
+def _check(status: int):
+    if status != 0:
+        raise WQError(status, lib.wq_last_error().decode())
+
+
+def describe(t: Optional[torch.Tensor], dtype: Optional[int] = None, shape=None):
+    """wq_tensor for a contiguous torch tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("wq tensors must be contiguous")
+    d = WqTensor()
+    d.data = t.data_ptr() if t.numel() > 0 else (t.data_ptr() or None)
+    d.dtype = int(dtype if dtype is not None else _TORCH2WQ[t.dtype])
+    shp = list(shape if shape is not None else t.shape)
+    if d.dtype == DType.INT4 and shape is None:
+        shp[-1] = shp[-1] * 2  # logical N of a (K, N/2) byte tensor
+    d.ndim = len(shp)
+    for i, v in enumerate(shp):
+        d.shape[i] = int(v)
+    return d
+
+
+def _ref(d):
+    return None if d is None else ctypes.byref(d)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def pack_int4_get_workspace(weight: torch.Tensor, out: torch.Tensor) -> int:
+    ws = ctypes.c_uint64(0)
+    _check(lib.wq_pack_int4_get_workspace(_ref(describe(weight)), _ref(describe(out)),
+                                          ctypes.byref(ws)))
+    return ws.value
+
+
+def pack_int4(weight: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """(K, N) int32 -> (K, N/2) uint8 packed INT4, on the GPU (``wq_pack_int4``)."""
+    if out is None:
+        out = torch.empty((weight.shape[0], weight.shape[1] // 2), dtype=torch.uint8,
+                          device=weight.device)
+    wd, od = describe(weight), describe(out)
+    ws = ctypes.c_uint64(0)
+    _check(lib.wq_pack_int4_get_workspace(_ref(wd), _ref(od), ctypes.byref(ws)))
+    _check(lib.wq_pack_int4(_ref(wd), _ref(od), None, 0, _stream(stream)))
+    return out
+
+
+def pack_int4_bytes(n_logical: int, data: torch.Tensor) -> WqTensor:
+    """Descriptor of packed INT4 bytes with an explicit logical last dimension."""
+    shp = list(data.shape)
+    shp[-1] = n_logical
+    return describe(data, DType.INT4, shp)
+
+
+def _descs(x1, x2, scale, offset, bias, residual, gamma, y, normOut):
+    return [describe(x1), describe(x2), describe(scale), describe(offset), describe(bias),
+            describe(residual), describe(gamma), describe(y), describe(normOut)]
+
+
+def matmul_add_rmsnorm_get_workspace(x1, x2, scale, offset, bias, residual, gamma, eps, group=0,
+                                     y=None, normOut=None, kernel: int = Kernel.AUTO) -> int:
+    y = residual if y is None else y
+    normOut = torch.empty_like(residual) if normOut is None else normOut
+    d = _descs(x1, x2, scale, offset, bias, residual, gamma, y, normOut)
+    ws = ctypes.c_uint64(0)
+    _check(lib.wq_matmul_add_rmsnorm_get_workspace_ex(*[_ref(v) for v in d[:7]], float(eps),
+                                                      int(group), _ref(d[7]), _ref(d[8]),
+                                                      int(kernel), ctypes.byref(ws)))
+    return ws.value
+
+
+def select_kernel(x1, x2, scale, offset, bias, residual, gamma, eps, group=0) -> Kernel:
+    y = torch.empty_like(residual)
+    no = torch.empty_like(residual)
+    d = _descs(x1, x2, scale, offset, bias, residual, gamma, y, no)
+    r = lib.wq_matmul_add_rmsnorm_select_kernel(*[_ref(v) for v in d[:7]], float(eps), int(group),
+                                                _ref(d[7]), _ref(d[8]))
+    if r < 0:
+        _check(-r)
+    return Kernel(r)
+
+
+def matmul_add_rmsnorm(x1, x2, scale, offset, bias, residual, gamma, eps: float, group: int = 0,
+                       y: Optional[torch.Tensor] = None, normOut: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None, kernel: int = Kernel.AUTO,
+                       stream=None):
+    """Fused ``y = x1 @ (x2*scale + offset) + bias + residual``,
+    ``normOut = y / sqrt(mean(y^2) + eps) * gamma`` (``wq_matmul_add_rmsnorm``).
+
+    Outputs and workspace are allocated with torch when not given. Pass
+    ``y=residual`` for the in-place variant. Returns ``(y, normOut)``.
+    """
+    if y is None:
+        y = torch.empty_like(residual)
+    if normOut is None:
+        normOut = torch.empty_like(residual)
+    d = _descs(x1, x2, scale, offset, bias, residual, gamma, y, normOut)
+    refs = [_ref(v) for v in d]
+    ws = ctypes.c_uint64(0)
+    _check(lib.wq_matmul_add_rmsnorm_get_workspace_ex(*refs[:7], float(eps), int(group), refs[7],
+                                                      refs[8], int(kernel), ctypes.byref(ws)))
+    if workspace is None:
+        workspace = torch.empty(max(ws.value, 1), dtype=torch.uint8, device=residual.device)
+    elif workspace.numel() < ws.value:
+        raise WQError(Status.ERR_WORKSPACE, f"need {ws.value} bytes")
+    _check(lib.wq_matmul_add_rmsnorm_ex(*refs[:7], float(eps), int(group), refs[7], refs[8],
+                                        int(kernel), workspace.data_ptr(), workspace.numel(),
+                                        _stream(stream)))
+    return y, normOut
+
+
+def read_device_status(workspace: torch.Tensor, stream=None) -> int:
+    st = ctypes.c_int32(0)
+    _check(lib.wq_read_device_status(workspace.data_ptr(), workspace.numel(), _stream(stream),
+                                     ctypes.byref(st)))
+    return st.value

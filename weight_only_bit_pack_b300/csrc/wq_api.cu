@@ -1,0 +1,439 @@
+// Host side of the C ABI: argument validation (the "first phase" of each
+// operator), workspace sizing, kernel selection and launch.
+//
+// Validation follows aclnnWeightQuantMatmulAllReduceAddRmsNorm, "Constraints":
+// x1 2-D (s, k) or 3-D (b, s, k) with b*s and s in [1, 2^31-1] (0 allowed as an
+// empty tensor), k and n in [1, 65535] (k = 0 rejected, n = 0 empty), x2 2-D
+// (k, n) INT8/INT4, bias (n), residual (b, s, n) with b*s = s of a 2-D x1,
+// gamma (n), y/normOut shaped like residual, one floating dtype for x1, scale,
+// offset, bias, residual and gamma, scale (1) / (n) / (1, n) /
+// (ceil(k/group), n), offset shaped like scale, group in [32, k-1] and a
+// multiple of 32. The INT4 storage rule (last dimension even) is the one of
+// aclnnDynamicQuant, "Constraints".
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "wq_internal.h"
+
+namespace wq {
+namespace {
+
+thread_local std::string g_last_error;
+
+int32_t fail(int32_t code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int32_t ok() {
+  g_last_error.clear();
+  return WQ_OK;
+}
+
+int64_t numel(const wq_tensor *t) {
+  int64_t n = 1;
+  for (int i = 0; i < t->ndim; ++i) n *= t->shape[i];
+  return n;
+}
+
+int64_t elem_bits(int dt) {
+  switch (dt) {
+    case WQ_F16: case WQ_BF16: return 16;
+    case WQ_INT8: return 8;
+    case WQ_INT4: return 4;
+    case WQ_INT32: return 32;
+    default: return 0;
+  }
+}
+
+uint64_t nbytes(const wq_tensor *t) { return (uint64_t)((numel(t) * elem_bits(t->dtype) + 7) / 8); }
+
+bool valid_rank(const wq_tensor *t) {
+  if (t->ndim < 1 || t->ndim > 3) return false;
+  for (int i = 0; i < t->ndim; ++i)
+    if (t->shape[i] < 0) return false;
+  return true;
+}
+
+bool overlap(const wq_tensor *a, const wq_tensor *b) {
+  if (!a || !b || !a->data || !b->data) return false;
+  uint64_t a0 = (uint64_t)(uintptr_t)a->data, a1 = a0 + nbytes(a);
+  uint64_t b0 = (uint64_t)(uintptr_t)b->data, b1 = b0 + nbytes(b);
+  if (a1 == a0 || b1 == b0) return false;
+  return a0 < b1 && b0 < a1;
+}
+
+bool same_shape(const wq_tensor *a, const wq_tensor *b) {
+  if (a->ndim != b->ndim) return false;
+  for (int i = 0; i < a->ndim; ++i)
+    if (a->shape[i] != b->shape[i]) return false;
+  return true;
+}
+
+const char *dtname(int dt) {
+  switch (dt) {
+    case WQ_F16: return "F16"; case WQ_BF16: return "BF16"; case WQ_INT8: return "INT8";
+    case WQ_INT4: return "INT4"; case WQ_INT32: return "INT32"; default: return "?";
+  }
+}
+
+constexpr int64_t kMaxRows = 2147483647LL;  // b*s upper bound
+constexpr int64_t kMaxKN = 65535;           // k, n upper bound
+
+// Full validation of the fused operator; fills `p` on success.
+int32_t validate(const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scale,
+                 const wq_tensor *offset, const wq_tensor *bias, const wq_tensor *residual,
+                 const wq_tensor *gamma, double eps, int64_t group, const wq_tensor *y,
+                 const wq_tensor *normOut, Problem &p) {
+  if (!x1 || !x2 || !scale || !residual || !gamma || !y || !normOut)
+    return fail(WQ_ERR_NULL, "x1, x2, scale, residual, gamma, y and normOut are required");
+  const wq_tensor *all[] = {x1, x2, scale, offset, bias, residual, gamma, y, normOut};
+  const char *names[] = {"x1", "x2", "scale", "offset", "bias", "residual", "gamma", "y", "normOut"};
+  for (int i = 0; i < 9; ++i)
+    if (all[i] && !valid_rank(all[i]))
+      return fail(WQ_ERR_SHAPE, "%s: rank must be 1..3 with non-negative dims", names[i]);
+
+  // dtypes
+  const int dt = x1->dtype;
+  if (dt != WQ_F16 && dt != WQ_BF16)
+    return fail(WQ_ERR_DTYPE, "x1 must be F16 or BF16, got %s", dtname(dt));
+  if (x2->dtype != WQ_INT8 && x2->dtype != WQ_INT4)
+    return fail(WQ_ERR_DTYPE, "x2 must be INT8 or INT4, got %s", dtname(x2->dtype));
+  const wq_tensor *same[] = {scale, offset, bias, residual, gamma, y, normOut};
+  const char *snames[] = {"scale", "offset", "bias", "residual", "gamma", "y", "normOut"};
+  for (int i = 0; i < 7; ++i)
+    if (same[i] && same[i]->dtype != dt)
+      return fail(WQ_ERR_DTYPE, "%s must have x1's dtype %s, got %s", snames[i], dtname(dt),
+                  dtname(same[i]->dtype));
+
+  // x1: (s, k) or (b, s, k)
+  if (x1->ndim != 2 && x1->ndim != 3) return fail(WQ_ERR_SHAPE, "x1 must be 2-D or 3-D");
+  const int64_t K = x1->shape[x1->ndim - 1];
+  int64_t M = 1;
+  for (int i = 0; i < x1->ndim - 1; ++i) {
+    if (x1->shape[i] > kMaxRows) return fail(WQ_ERR_SHAPE, "x1 dim %d exceeds 2^31-1", i);
+    M *= x1->shape[i];
+  }
+  if (M > kMaxRows) return fail(WQ_ERR_SHAPE, "b*s = %lld exceeds 2^31-1", (long long)M);
+  if (K < 1) return fail(WQ_ERR_SHAPE, "k must be >= 1 (empty k is not supported)");
+  if (K > kMaxKN) return fail(WQ_ERR_SHAPE, "k = %lld exceeds 65535", (long long)K);
+
+  // x2: (k, n)
+  if (x2->ndim != 2) return fail(WQ_ERR_SHAPE, "x2 must be 2-D (k, n)");
+  if (x2->shape[0] != K)
+    return fail(WQ_ERR_SHAPE, "x2 has k = %lld, x1 has k = %lld", (long long)x2->shape[0],
+                (long long)K);
+  const int64_t N = x2->shape[1];
+  if (N > kMaxKN) return fail(WQ_ERR_SHAPE, "n = %lld exceeds 65535", (long long)N);
+  if (x2->dtype == WQ_INT4 && (N % 2) != 0)
+    return fail(WQ_ERR_SHAPE, "INT4 x2 needs an even last dimension, got n = %lld", (long long)N);
+
+  // scale / group
+  int smode;
+  int64_t G = 1, Ns = 1;
+  if (group != 0) {
+    if (group < 32 || group > K - 1 || group % 32 != 0)
+      return fail(WQ_ERR_GROUP, "group = %lld must be a multiple of 32 in [32, k-1 = %lld]",
+                  (long long)group, (long long)(K - 1));
+    const int64_t want = (K + group - 1) / group;
+    if (scale->ndim != 2 || scale->shape[0] != want || scale->shape[1] != N)
+      return fail(WQ_ERR_GROUP, "per-group scale must be (ceil(k/group) = %lld, n = %lld)",
+                  (long long)want, (long long)N);
+    smode = kPerGroup;
+    G = want;
+    Ns = N;
+  } else {
+    if (scale->ndim == 1 && scale->shape[0] == 1) {
+      smode = kPerTensor;
+    } else if (scale->ndim == 1 && scale->shape[0] == N) {
+      smode = kPerChannel;
+      Ns = N;
+    } else if (scale->ndim == 2 && scale->shape[0] == 1 && scale->shape[1] == N) {
+      smode = kPerChannel;
+      Ns = N;
+    } else if (scale->ndim == 2 && scale->shape[1] == N && scale->shape[0] > 1) {
+      return fail(WQ_ERR_GROUP, "a (%lld, n) scale is per-group and needs group != 0",
+                  (long long)scale->shape[0]);
+    } else {
+      return fail(WQ_ERR_SHAPE, "scale must be (1), (n), (1, n) or (ceil(k/group), n)");
+    }
+    if (smode == kPerTensor && N == 1) { smode = kPerChannel; Ns = 1; }
+  }
+  if (offset && !same_shape(offset, scale))
+    return fail(WQ_ERR_SHAPE, "offset must have the scale's shape");
+
+  // bias (n), gamma (n)
+  if (bias && (bias->ndim != 1 || bias->shape[0] != N))
+    return fail(WQ_ERR_SHAPE, "bias must be 1-D (n = %lld)", (long long)N);
+  if (gamma->ndim != 1 || gamma->shape[0] != N)
+    return fail(WQ_ERR_SHAPE, "gamma must be 1-D (n = %lld)", (long long)N);
+
+  // residual: (b, s, n) with b*s = M, or (M, n)
+  if (residual->ndim != 2 && residual->ndim != 3)
+    return fail(WQ_ERR_SHAPE, "residual must be 3-D (b, s, n) or 2-D (b*s, n)");
+  {
+    int64_t rm = 1;
+    for (int i = 0; i < residual->ndim - 1; ++i) rm *= residual->shape[i];
+    if (rm != M || residual->shape[residual->ndim - 1] != N)
+      return fail(WQ_ERR_SHAPE, "residual must hold b*s = %lld rows of n = %lld", (long long)M,
+                  (long long)N);
+  }
+  if (!same_shape(y, residual)) return fail(WQ_ERR_SHAPE, "y must have residual's shape");
+  if (!same_shape(normOut, residual)) return fail(WQ_ERR_SHAPE, "normOut must have residual's shape");
+
+  if (!(eps >= 0.0) || !std::isfinite(eps))
+    return fail(WQ_ERR_SHAPE, "eps must be finite and >= 0");
+
+  // data pointers of non-empty tensors
+  for (int i = 0; i < 9; ++i)
+    if (all[i] && numel(all[i]) > 0 && !all[i]->data)
+      return fail(WQ_ERR_NULL, "%s has elements but a NULL data pointer", names[i]);
+
+  // aliasing: y may be exactly residual (in-place variant), nothing else overlaps
+  const wq_tensor *ins[] = {x1, x2, scale, offset, bias, residual, gamma};
+  const char *inames[] = {"x1", "x2", "scale", "offset", "bias", "residual", "gamma"};
+  for (int i = 0; i < 7; ++i) {
+    if (overlap(normOut, ins[i]))
+      return fail(WQ_ERR_ALIAS, "normOut overlaps %s", inames[i]);
+    if (i == 5) {
+      if (overlap(y, residual) && y->data != residual->data)
+        return fail(WQ_ERR_ALIAS, "y partially overlaps residual (only y == residual is allowed)");
+      continue;
+    }
+    if (overlap(y, ins[i])) return fail(WQ_ERR_ALIAS, "y overlaps %s", inames[i]);
+  }
+  if (overlap(normOut, y)) return fail(WQ_ERR_ALIAS, "normOut overlaps y");
+
+  p = Problem();
+  p.M = M; p.K = K; p.N = N;
+  p.dtype = dt;
+  p.wbits = x2->dtype == WQ_INT4 ? 4 : 8;
+  p.smode = smode; p.group = smode == kPerGroup ? group : 0; p.G = G; p.Ns = Ns;
+  p.eps = (float)eps;
+  p.x1 = x1->data; p.x2 = x2->data; p.scale = scale->data;
+  p.offset = offset ? offset->data : nullptr;
+  p.bias = bias ? bias->data : nullptr;
+  p.residual = residual->data; p.gamma = gamma->data;
+  p.y = y->data; p.normOut = normOut->data;
+  return WQ_OK;
+}
+
+// Picks the kernel and sizes the workspace. Returns WQ_ERR_UNSUPPORTED for a
+// forced kernel that cannot run the problem.
+int32_t make_plan(const Problem &p, int32_t kernel, Plan &plan) {
+  plan = Plan();
+  if (kernel < WQ_KERNEL_AUTO || kernel > WQ_KERNEL_PREFILL)
+    return fail(WQ_ERR_UNSUPPORTED, "unknown kernel selector %d", kernel);
+  if (p.M == 0 || p.N == 0) {  // empty output: nothing to launch
+    plan.kernel = kernel == WQ_KERNEL_AUTO ? WQ_KERNEL_GENERIC : kernel;
+    plan.ws_bytes = 0;
+    return WQ_OK;
+  }
+  int chosen = kernel;
+  if (chosen == WQ_KERNEL_AUTO) chosen = WQ_KERNEL_GENERIC;
+  if (chosen == WQ_KERNEL_DECODE || chosen == WQ_KERNEL_PREFILL)
+    return fail(WQ_ERR_UNSUPPORTED, "kernel %d is not available for this problem", chosen);
+  if (!plan_generic(p, plan)) return fail(WQ_ERR_UNSUPPORTED, "generic plan failed");
+  plan_epilogue(p, plan);
+  plan.kernel = chosen;
+  return WQ_OK;
+}
+
+int32_t cuda_fail(cudaError_t e, const char *what) {
+  return fail(WQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+const DeviceInfo &device_info() {
+  // One entry per device id; filled on first use with that device current.
+  static std::mutex mu;
+  static std::vector<DeviceInfo> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (auto &d : cache)
+    if (d.device == dev) return d;
+  DeviceInfo d;
+  d.device = dev;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) == cudaSuccess) {
+    d.sms = prop.multiProcessorCount;
+    d.cc_major = prop.major;
+    d.cc_minor = prop.minor;
+    d.smem_optin = prop.sharedMemPerBlockOptin;
+  } else {
+    cudaGetLastError();
+  }
+  cache.push_back(d);
+  return cache.back();
+}
+
+}  // namespace wq
+
+using namespace wq;
+
+extern "C" {
+
+int32_t wq_version(void) { return 100; }
+
+const char *wq_status_string(int32_t s) {
+  switch (s) {
+    case WQ_OK: return "WQ_OK";
+    case WQ_ERR_NULL: return "WQ_ERR_NULL";
+    case WQ_ERR_DTYPE: return "WQ_ERR_DTYPE";
+    case WQ_ERR_SHAPE: return "WQ_ERR_SHAPE";
+    case WQ_ERR_GROUP: return "WQ_ERR_GROUP";
+    case WQ_ERR_WORKSPACE: return "WQ_ERR_WORKSPACE";
+    case WQ_ERR_UNSUPPORTED: return "WQ_ERR_UNSUPPORTED";
+    case WQ_ERR_CUDA: return "WQ_ERR_CUDA";
+    case WQ_ERR_DEVICE_TIMEOUT: return "WQ_ERR_DEVICE_TIMEOUT";
+    case WQ_ERR_ALIAS: return "WQ_ERR_ALIAS";
+    default: return "WQ_ERR_UNKNOWN";
+  }
+}
+
+const char *wq_last_error(void) { return g_last_error.c_str(); }
+
+// ------------------------------------------------------------------ pack
+
+static int32_t validate_pack(const wq_tensor *w, const wq_tensor *o) {
+  if (!w || !o) return fail(WQ_ERR_NULL, "weight and weight_int4 are required");
+  if (w->dtype != WQ_INT32) return fail(WQ_ERR_DTYPE, "weight must be INT32, got %s", dtname(w->dtype));
+  if (o->dtype != WQ_INT4) return fail(WQ_ERR_DTYPE, "weight_int4 must be INT4, got %s", dtname(o->dtype));
+  if (!valid_rank(w) || !valid_rank(o) || w->ndim != 2 || o->ndim != 2)
+    return fail(WQ_ERR_SHAPE, "weight and weight_int4 must be 2-D");
+  if (!same_shape(w, o)) return fail(WQ_ERR_SHAPE, "weight_int4 must have weight's logical shape");
+  if (w->shape[1] % 2 != 0) return fail(WQ_ERR_SHAPE, "the last dimension must be even for INT4");
+  if (numel(w) > 0 && (!w->data || !o->data))
+    return fail(WQ_ERR_NULL, "non-empty tensors need data pointers");
+  if (overlap(w, o)) return fail(WQ_ERR_ALIAS, "weight_int4 overlaps weight");
+  return WQ_OK;
+}
+
+int32_t wq_pack_int4_get_workspace(const wq_tensor *w, const wq_tensor *o, uint64_t *ws_bytes) {
+  if (!ws_bytes) return fail(WQ_ERR_NULL, "ws_bytes is required");
+  int32_t st = validate_pack(w, o);
+  if (st) return st;
+  *ws_bytes = 0;
+  return ok();
+}
+
+int32_t wq_pack_int4(const wq_tensor *w, const wq_tensor *o, void *ws, uint64_t ws_bytes,
+                     void *stream) {
+  (void)ws; (void)ws_bytes;
+  int32_t st = validate_pack(w, o);
+  if (st) return st;
+  if (numel(w) == 0) return ok();
+  cudaError_t e = launch_pack_int4((const int32_t *)w->data, (uint8_t *)o->data, w->shape[0],
+                                   w->shape[1], (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "pack kernel launch");
+  return ok();
+}
+
+// ------------------------------------------------------------------ matmul
+
+int32_t wq_matmul_add_rmsnorm_get_workspace_ex(
+    const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scale, const wq_tensor *offset,
+    const wq_tensor *bias, const wq_tensor *residual, const wq_tensor *gamma, double eps,
+    int64_t group, const wq_tensor *y, const wq_tensor *normOut, int32_t kernel,
+    uint64_t *ws_bytes) {
+  if (!ws_bytes) return fail(WQ_ERR_NULL, "ws_bytes is required");
+  Problem p;
+  int32_t st = validate(x1, x2, scale, offset, bias, residual, gamma, eps, group, y, normOut, p);
+  if (st) return st;
+  Plan plan;
+  st = make_plan(p, kernel, plan);
+  if (st) return st;
+  *ws_bytes = plan.ws_bytes;
+  return ok();
+}
+
+int32_t wq_matmul_add_rmsnorm_get_workspace(
+    const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scale, const wq_tensor *offset,
+    const wq_tensor *bias, const wq_tensor *residual, const wq_tensor *gamma, double eps,
+    int64_t group, const wq_tensor *y, const wq_tensor *normOut, uint64_t *ws_bytes) {
+  return wq_matmul_add_rmsnorm_get_workspace_ex(x1, x2, scale, offset, bias, residual, gamma, eps,
+                                                group, y, normOut, WQ_KERNEL_AUTO, ws_bytes);
+}
+
+int32_t wq_matmul_add_rmsnorm_select_kernel(
+    const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scale, const wq_tensor *offset,
+    const wq_tensor *bias, const wq_tensor *residual, const wq_tensor *gamma, double eps,
+    int64_t group, const wq_tensor *y, const wq_tensor *normOut) {
+  Problem p;
+  int32_t st = validate(x1, x2, scale, offset, bias, residual, gamma, eps, group, y, normOut, p);
+  if (st) return -st;
+  Plan plan;
+  st = make_plan(p, WQ_KERNEL_AUTO, plan);
+  if (st) return -st;
+  ok();
+  return plan.kernel;
+}
+
+int32_t wq_matmul_add_rmsnorm_ex(
+    const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scale, const wq_tensor *offset,
+    const wq_tensor *bias, const wq_tensor *residual, const wq_tensor *gamma, double eps,
+    int64_t group, const wq_tensor *y, const wq_tensor *normOut, int32_t kernel, void *ws,
+    uint64_t ws_bytes, void *stream) {
+  Problem p;
+  int32_t st = validate(x1, x2, scale, offset, bias, residual, gamma, eps, group, y, normOut, p);
+  if (st) return st;
+  Plan plan;
+  st = make_plan(p, kernel, plan);
+  if (st) return st;
+  if (p.M == 0 || p.N == 0) return ok();
+  if (ws_bytes < plan.ws_bytes || (plan.ws_bytes > 0 && !ws))
+    return fail(WQ_ERR_WORKSPACE, "workspace of %llu bytes given, %llu needed",
+                (unsigned long long)ws_bytes, (unsigned long long)plan.ws_bytes);
+  if (((uintptr_t)ws) % 256 != 0)
+    return fail(WQ_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e;
+  switch (plan.kernel) {
+    case WQ_KERNEL_GENERIC:
+      e = launch_generic(p, plan, ws, s);
+      if (e != cudaSuccess) return cuda_fail(e, "generic kernel launch");
+      e = launch_epilogue(p, plan, ws, false, s);
+      if (e != cudaSuccess) return cuda_fail(e, "epilogue kernel launch");
+      break;
+    default:
+      return fail(WQ_ERR_UNSUPPORTED, "kernel %d is not available", plan.kernel);
+  }
+  return ok();
+}
+
+int32_t wq_matmul_add_rmsnorm(
+    const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scale, const wq_tensor *offset,
+    const wq_tensor *bias, const wq_tensor *residual, const wq_tensor *gamma, double eps,
+    int64_t group, const wq_tensor *y, const wq_tensor *normOut, void *ws, uint64_t ws_bytes,
+    void *stream) {
+  return wq_matmul_add_rmsnorm_ex(x1, x2, scale, offset, bias, residual, gamma, eps, group, y,
+                                  normOut, WQ_KERNEL_AUTO, ws, ws_bytes, stream);
+}
+
+int32_t wq_read_device_status(const void *ws, uint64_t ws_bytes, void *stream,
+                              int32_t *device_status) {
+  if (!ws || !device_status) return fail(WQ_ERR_NULL, "ws and device_status are required");
+  if (ws_bytes < 16) return fail(WQ_ERR_WORKSPACE, "workspace smaller than its status word");
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  uint32_t word = 0;
+  e = cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "status word copy");
+  *device_status = (int32_t)word;
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,67 @@
+// Small device helpers shared by the kernels of libwq.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace wq {
+
+// Element type of the floating tensors, selected by the wq_dtype value.
+template <int DT> struct Elem;
+template <> struct Elem<WQ_F16> {
+  using T = __half;
+  __device__ static __forceinline__ float to_f(T v) { return __half2float(v); }
+  __device__ static __forceinline__ T from_f(float v) { return __float2half_rn(v); }
+};
+template <> struct Elem<WQ_BF16> {
+  using T = __nv_bfloat16;
+  __device__ static __forceinline__ float to_f(T v) { return __bfloat162float(v); }
+  __device__ static __forceinline__ T from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+// Two 16-bit floats of a 32-bit word -> two fp32 values (low half first).
+template <int DT> __device__ __forceinline__ float2 unpack2(uint32_t w);
+template <> __device__ __forceinline__ float2 unpack2<WQ_BF16>(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+template <> __device__ __forceinline__ float2 unpack2<WQ_F16>(uint32_t w) {
+  __half2 h = *reinterpret_cast<__half2 *>(&w);
+  return __half22float2(h);
+}
+
+// Two fp32 values -> one word of two 16-bit floats, each rounded to nearest even.
+template <int DT> __device__ __forceinline__ uint32_t pack2(float lo, float hi);
+template <> __device__ __forceinline__ uint32_t pack2<WQ_BF16>(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+template <> __device__ __forceinline__ uint32_t pack2<WQ_F16>(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Read-only streaming 128-bit load (not kept in L1).
+__device__ __forceinline__ uint4 ld_stream_u4(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint2 ld_stream_u2(const void *p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+               : "=r"(v.x), "=r"(v.y)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_stream_u4(void *p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+}  // namespace wq

@@ -1,0 +1,71 @@
+// Internal declarations shared by the .cu files of libwq (not part of the ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/wq.h"
+
+namespace wq {
+
+// Scale layout after validation.
+enum ScaleMode : int { kPerTensor = 0, kPerChannel = 1, kPerGroup = 2 };
+
+// A validated problem: everything a launcher needs, in plain integers/pointers.
+struct Problem {
+  int64_t M = 0, K = 0, N = 0;
+  int dtype = WQ_BF16;     // WQ_F16 or WQ_BF16 (x1, scale, offset, bias, residual, gamma, y, normOut)
+  int wbits = 4;           // 4 (packed, two per byte along N) or 8
+  int smode = kPerTensor;  // ScaleMode
+  int64_t group = 0;       // > 0 only for kPerGroup
+  int64_t G = 1;           // scale rows: ceil(K/group) for kPerGroup, else 1
+  int64_t Ns = 1;          // scale columns: 1 (per-tensor) or N
+  float eps = 0.f;
+  const void *x1 = nullptr, *x2 = nullptr, *scale = nullptr, *offset = nullptr,
+             *bias = nullptr, *residual = nullptr, *gamma = nullptr;
+  void *y = nullptr, *normOut = nullptr;
+};
+
+// Workspace header: the first kWsHeader bytes of every matmul workspace.
+//   word 0: device status (0 = ok, else WQ_ERR_DEVICE_TIMEOUT | where << 8)
+constexpr uint64_t kWsHeader = 256;
+
+// Device properties cached per device (SM count, cluster support ...).
+struct DeviceInfo {
+  int device = -1;
+  int sms = 148;
+  int cc_major = 10, cc_minor = 3;
+  size_t smem_optin = 227 * 1024;
+};
+const DeviceInfo &device_info();
+
+// Launch plan of one call; computed on the host from the Problem alone, so the
+// first and second phases agree on the workspace size.
+struct Plan {
+  int kernel = WQ_KERNEL_GENERIC;
+  uint64_t ws_bytes = 0;
+  // split-K partial sums: parts x M x N fp32, at ws + part_off
+  int parts = 1;
+  uint64_t part_off = kWsHeader;
+  // generic kernel: k rows per split
+  int64_t ksplit = 0;
+  // epilogue: CTAs per row (a thread-block cluster), vectorised or not
+  int epi_cluster = 1;
+  bool epi_vec = false;
+  // prefill: counters and row partials
+  uint64_t cnt_off = 0, rowpart_off = 0;
+  int64_t n_tiles = 0, m_tiles = 0;
+  int grid = 0;
+};
+
+// Launchers (return cudaError_t of the launch).
+cudaError_t launch_pack_int4(const int32_t *in, uint8_t *out, int64_t K, int64_t N, cudaStream_t s);
+cudaError_t launch_generic(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
+cudaError_t launch_epilogue(const Problem &p, const Plan &plan, const void *ws, bool pdl,
+                            cudaStream_t s);
+
+// Plan builders.
+bool plan_generic(const Problem &p, Plan &plan);
+void plan_epilogue(const Problem &p, Plan &plan);
+
+}  // namespace wq
