@@ -116,18 +116,19 @@ class ClockSampler:
         self.period = period_s
         self.stop_ev = threading.Event()
         self.max_mhz = None
+        self.err = None
+        self.proc = None
+        uuid = str(torch.cuda.get_device_properties(device).uuid)
+        self.uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
         try:
             import pynvml
             pynvml.nvmlInit()
             self.nv = pynvml
-            uuid = str(torch.cuda.get_device_properties(device).uuid)
-            if not uuid.startswith("GPU-"):
-                uuid = "GPU-" + uuid
-            self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+            self.h = pynvml.nvmlDeviceGetHandleByUUID(self.uuid)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception as e:  # noqa: BLE001
+        except Exception as e:  # noqa: BLE001 - no NVML binding: sample nvidia-smi instead
             self.nv = None
-            self.err = str(e)
+            self.err = f"pynvml unavailable ({e}); sampled nvidia-smi"
         self.th = threading.Thread(target=self._run, daemon=True)
 
     def _sample(self):
@@ -146,9 +147,40 @@ class ClockSampler:
                 break
             time.sleep(self.period)
 
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
+
+    def _smi_cmd(self, loop):
+        cmd = ["nvidia-smi", "-i", self.uuid, f"--query-gpu={self.SMI_FIELDS}",
+               "--format=csv,noheader,nounits"]
+        return cmd + (["-lms", "20"] if loop else [])
+
+    def _parse_smi(self, text):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in text.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 6:
+                continue
+            try:
+                self.samples.append(float(f[0]))
+                self.max_mhz = float(f[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[2:6]):
+                if v.lower() == "active":
+                    self.reasons.add(name)
+
     def __enter__(self):
         if self.nv:
             self.th.start()
+        else:
+            import subprocess
+            try:
+                self.proc = subprocess.Popen(self._smi_cmd(True), stdout=subprocess.PIPE,
+                                             stderr=subprocess.DEVNULL, text=True)
+            except OSError as e:
+                self.err = f"no NVML and no nvidia-smi: {e}"
         return self
 
     def __exit__(self, *a):
@@ -160,13 +192,22 @@ class ClockSampler:
                     self._sample()
                 except Exception:  # noqa: BLE001
                     pass
+        elif self.proc is not None:
+            import subprocess
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self._parse_smi(out)
+            if not self.samples:  # region shorter than one sampling period
+                r = subprocess.run(self._smi_cmd(False), capture_output=True, text=True)
+                self._parse_smi(r.stdout)
 
     def summary(self):
-        if not self.nv:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.err}
-        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-                "samples": len(self.samples)}
+        d = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+             "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+             "samples": len(self.samples)}
+        if self.err:
+            d["note"] = self.err
+        return d
 
 
 # ------------------------------------------------------------------ distributed
