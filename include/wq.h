@@ -181,6 +181,38 @@ int32_t wq_matmul_add_rmsnorm_select_kernel(
     const wq_tensor *gamma, double eps, int64_t group,
     const wq_tensor *y, const wq_tensor *normOut);
 
+/* ------------------------------------------------------------------ no-alloc variant */
+
+/* The operator pages have no counterpart to this entry point.
+ *
+ * For callers that cannot allocate device memory or hand over a workspace --
+ * a host framework whose custom-operator interface passes only inputs and
+ * outputs, or a runtime that fixes its device memory at start-up and forbids
+ * later allocations (cudaMalloc may synchronize the device, fail under memory
+ * pressure or fragment a planned heap mid-run). It computes exactly what
+ * wq_matmul_add_rmsnorm computes, with the same kernels, but takes no workspace:
+ * its scratch memory is a fixed array of WQ_NOALLOC_SCRATCH_BYTES inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits. It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Arguments, validation and errors are those of wq_matmul_add_rmsnorm.
+ *   - A problem whose workspace (as wq_matmul_add_rmsnorm_get_workspace
+ *     reports it) exceeds WQ_NOALLOC_SCRATCH_BYTES is rejected with
+ *     WQ_ERR_WORKSPACE before anything is enqueued.
+ *   - The first call on each device looks up that device's address of the
+ *     array (cudaGetSymbolAddress with the device current); make that first
+ *     call before any stream capture.
+ *   - All calls share the one array per device and it keeps the last call's
+ *     contents (each call clears the part that must start at zero). Calls whose
+ *     work overlaps on the GPU -- on different streams or from different host
+ *     threads without ordering -- race on it and give wrong results. */
+#define WQ_NOALLOC_SCRATCH_BYTES (8ull << 20)
+
+int32_t wq_matmul_add_rmsnorm_noalloc(
+    const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scale,
+    const wq_tensor *offset, const wq_tensor *bias, const wq_tensor *residual,
+    const wq_tensor *gamma, double eps, int64_t group,
+    const wq_tensor *y, const wq_tensor *normOut, void *stream);
+
 /* ------------------------------------------------------------------ status */
 
 /* Device status word of a workspace after the work enqueued on `stream` has

@@ -76,6 +76,7 @@ lib.wq_matmul_add_rmsnorm_get_workspace_ex.argtypes = _T + [ctypes.c_int32,
 lib.wq_matmul_add_rmsnorm_ex.argtypes = _T + [ctypes.c_int32, ctypes.c_void_p, ctypes.c_uint64,
                                               ctypes.c_void_p]
 lib.wq_matmul_add_rmsnorm_select_kernel.argtypes = _T
+lib.wq_matmul_add_rmsnorm_noalloc.argtypes = _T + [ctypes.c_void_p]
 lib.wq_read_device_status.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p,
                                       ctypes.POINTER(ctypes.c_int32)]
 lib.wq_status_string.argtypes = [ctypes.c_int32]
@@ -85,7 +86,7 @@ lib.wq_last_error.restype = ctypes.c_char_p
 for _f in ("wq_pack_int4_get_workspace", "wq_pack_int4", "wq_matmul_add_rmsnorm_get_workspace",
            "wq_matmul_add_rmsnorm", "wq_matmul_add_rmsnorm_get_workspace_ex",
            "wq_matmul_add_rmsnorm_ex", "wq_matmul_add_rmsnorm_select_kernel",
-           "wq_read_device_status", "wq_version"):
+           "wq_read_device_status", "wq_version", "wq_matmul_add_rmsnorm_noalloc"):
     getattr(lib, _f).restype = ctypes.c_int32
 
 _TORCH2WQ = {torch.float16: DType.F16, torch.bfloat16: DType.BF16, torch.int8: DType.INT8,
@@ -213,3 +214,26 @@ def read_device_status(workspace: torch.Tensor, stream=None) -> int:
     _check(lib.wq_read_device_status(workspace.data_ptr(), workspace.numel(), _stream(stream),
                                      ctypes.byref(st)))
     return st.value
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20  # WQ_NOALLOC_SCRATCH_BYTES in include/wq.h
+
+
+def matmul_add_rmsnorm_noalloc(x1, x2, scale, offset, bias, residual, gamma, eps: float,
+                               group: int = 0, y: Optional[torch.Tensor] = None,
+                               normOut: Optional[torch.Tensor] = None, stream=None):
+    """``wq_matmul_add_rmsnorm_noalloc``: the fused operator without a workspace.
+
+    The library keeps its scratch in a fixed per-device array, for callers that
+    cannot allocate device memory. Outputs are allocated here only when not
+    given. Calls sharing a device must not overlap on the GPU.
+    """
+    if y is None:
+        y = torch.empty_like(residual)
+    if normOut is None:
+        normOut = torch.empty_like(residual)
+    d = _descs(x1, x2, scale, offset, bias, residual, gamma, y, normOut)
+    refs = [_ref(v) for v in d]
+    _check(lib.wq_matmul_add_rmsnorm_noalloc(*refs[:7], float(eps), int(group), refs[7], refs[8],
+                                             _stream(stream)))
+    return y, normOut

@@ -255,6 +255,13 @@ int32_t cuda_fail(cudaError_t e, const char *what) {
 
 }  // namespace
 
+void set_last_error(int32_t code, const char *msg) {
+  if (code == WQ_OK)
+    g_last_error.clear();
+  else
+    g_last_error = msg;
+}
+
 const DeviceInfo &device_info() {
   // One entry per device id; filled on first use with that device current.
   static std::mutex mu;

@@ -64,6 +64,9 @@ cudaError_t launch_generic(const Problem &p, const Plan &plan, void *ws, cudaStr
 cudaError_t launch_epilogue(const Problem &p, const Plan &plan, const void *ws, bool pdl,
                             cudaStream_t s);
 
+// Sets the thread-local message that wq_last_error() returns.
+void set_last_error(int32_t code, const char *msg);
+
 // Plan builders.
 bool plan_generic(const Problem &p, Plan &plan);
 void plan_epilogue(const Problem &p, Plan &plan);
