@@ -39,13 +39,66 @@ def test_tiny_forced(wq, kernel):
     _check(wq, to_device(inputs.tiny()), kernel)
 
 
-@pytest.mark.parametrize("kernel", [0, GENERIC])
+def test_prefill_rejects_fp16_per_group(wq):
+    """fp16 activations with per-group scales have no exact single-operand tensor-core
+    form; the prefill kernel refuses them instead of rounding W."""
+    from weight_only_bit_pack_b300.binding import WQError, Status
+    with pytest.raises(WQError) as ei:
+        run_gpu(wq, to_device(inputs.tiny()), PREFILL)
+    assert ei.value.status == Status.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kernel", [0, GENERIC, PREFILL])
 def test_decode(wq, kernel):
     _check(wq, inputs.decode("cuda"), kernel)
 
 
-def test_w8a16_generic(wq):
-    _check(wq, inputs.w8a16("cuda"), GENERIC, n_sample=48)
+@pytest.mark.parametrize("kernel", [0, GENERIC, PREFILL])
+def test_w8a16(wq, kernel):
+    _check(wq, inputs.w8a16("cuda"), kernel, n_sample=48)
+
+
+@pytest.mark.parametrize("kernel", [0, PREFILL])
+def test_prefill_workload(wq, kernel):
+    _check(wq, inputs.prefill("cuda"), kernel, n_sample=48)
+
+
+@pytest.mark.parametrize("M", inputs.SWEEP_M)
+def test_sweep(wq, M):
+    _check(wq, inputs.sweep(M, device="cuda"), 0, n_sample=24)
+
+
+def test_sweep_per_tensor(wq):
+    _check(wq, inputs.sweep(4096, per_tensor=True, device="cuda"), 0, n_sample=24)
+
+
+PREFILL_EDGE = [
+    ("m_tail_k_tail", dict(M_shape=(300,), K=200, N=608, dtype=torch.bfloat16, wbits=4,
+                           mode="group", group=64)),
+    ("many_waves_bf16_g32", dict(M_shape=(1000,), K=512, N=2048, dtype=torch.bfloat16, wbits=4,
+                                 mode="group", group=32)),
+    ("many_waves_fp16_channel", dict(M_shape=(1000,), K=512, N=2048, dtype=torch.float16, wbits=4,
+                                     mode="channel")),
+    ("int8_bf16_group", dict(M_shape=(160,), K=256, N=272, dtype=torch.bfloat16, wbits=8,
+                             mode="group", group=64)),
+    ("int8_bf16_offset", dict(M_shape=(3, 70), K=136, N=208, dtype=torch.bfloat16, wbits=8,
+                              mode="channel")),
+    ("int8_fp16_tensor", dict(M_shape=(129,), K=64, N=272, dtype=torch.float16, wbits=8,
+                              mode="tensor", bias=False)),
+    ("int4_per_tensor_nobias", dict(M_shape=(256,), K=1024, N=512, dtype=torch.bfloat16, wbits=4,
+                                    mode="tensor", bias=False, offset=False)),
+    ("single_k_tile", dict(M_shape=(130,), K=64, N=256, dtype=torch.float16, wbits=4,
+                           mode="channel")),
+    ("wide_rows_79_ntiles", dict(M_shape=(200,), K=128, N=20000 + 224, dtype=torch.bfloat16,
+                                 wbits=4, mode="group", group=32)),
+]
+
+
+@pytest.mark.parametrize("name,kw", PREFILL_EDGE, ids=[e[0] for e in PREFILL_EDGE])
+def test_prefill_edge_shapes(wq, name, kw):
+    prob = inputs.make_problem(**kw, seed=zlib.crc32(name.encode()) % 1000, device="cuda",
+                               name=name)
+    _check(wq, prob, PREFILL)
 
 
 # ------------------------------------------------------------------ edge shapes
@@ -108,7 +161,7 @@ def test_integer_inputs_bit_exact_y(wq):
     to_device(prob)
     mm = (x1.double() @ q.double())
     assert mm.abs().max() <= 2048
-    for kernel in (0, GENERIC):
+    for kernel in (0, GENERIC, PREFILL):
         y, _ = run_gpu(wq, prob, kernel)
         assert torch.equal(y.cpu(), mm.to(torch.float16)), kernel
 
@@ -116,7 +169,7 @@ def test_integer_inputs_bit_exact_y(wq):
 def test_deterministic_across_runs(wq):
     prob = inputs.decode("cuda")
     w = gpu_weight(wq, prob)
-    for kernel in (0, GENERIC):
+    for kernel in (0, GENERIC, PREFILL):
         a = run_gpu(wq, prob, kernel, w=w)
         b = run_gpu(wq, prob, kernel, w=w)
         assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])

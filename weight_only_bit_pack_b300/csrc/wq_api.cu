@@ -240,9 +240,16 @@ int32_t make_plan(const Problem &p, int32_t kernel, Plan &plan) {
     return WQ_OK;
   }
   int chosen = kernel;
-  if (chosen == WQ_KERNEL_AUTO) chosen = WQ_KERNEL_GENERIC;
-  if (chosen == WQ_KERNEL_DECODE || chosen == WQ_KERNEL_PREFILL)
+  if (chosen == WQ_KERNEL_AUTO) chosen = prefill_applicable(p) ? WQ_KERNEL_PREFILL : WQ_KERNEL_GENERIC;
+  if (chosen == WQ_KERNEL_DECODE)
     return fail(WQ_ERR_UNSUPPORTED, "kernel %d is not available for this problem", chosen);
+  if (chosen == WQ_KERNEL_PREFILL) {
+    if (!plan_prefill(p, plan))
+      return fail(WQ_ERR_UNSUPPORTED,
+                  "the prefill kernel needs k %% 8 == 0, n %% 32 == 0 (INT4) or n %% 16 == 0 "
+                  "(INT8), 16-byte aligned tensors and ceil(n/256) <= SM count");
+    return WQ_OK;
+  }
   if (!plan_generic(p, plan)) return fail(WQ_ERR_UNSUPPORTED, "generic plan failed");
   plan_epilogue(p, plan);
   plan.kernel = chosen;
@@ -413,6 +420,10 @@ int32_t wq_matmul_add_rmsnorm_ex(
       if (e != cudaSuccess) return cuda_fail(e, "generic kernel launch");
       e = launch_epilogue(p, plan, ws, false, s);
       if (e != cudaSuccess) return cuda_fail(e, "epilogue kernel launch");
+      break;
+    case WQ_KERNEL_PREFILL:
+      e = launch_prefill(p, plan, ws, s);
+      if (e != cudaSuccess) return cuda_fail(e, "prefill kernel launch");
       break;
     default:
       return fail(WQ_ERR_UNSUPPORTED, "kernel %d is not available", plan.kernel);

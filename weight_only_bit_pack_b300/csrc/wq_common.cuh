@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "../../include/wq.h"
+
 namespace wq {
 
 // Element type of the floating tensors, selected by the wq_dtype value.

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/wq.h"
@@ -52,8 +53,10 @@ struct Plan {
   // epilogue: CTAs per row (a thread-block cluster), vectorised or not
   int epi_cluster = 1;
   bool epi_vec = false;
-  // prefill: counters and row partials
-  uint64_t cnt_off = 0, rowpart_off = 0;
+  // prefill: operand mode, counters, row partials and preparation buffers
+  int mode = 0;
+  uint64_t cnt_off = 0, rowpart_off = 0, rowsum_off = 0, erow_off = 0, ecol_off = 0, s16_off = 0,
+           o16_off = 0, x16_off = 0;
   int64_t n_tiles = 0, m_tiles = 0;
   int grid = 0;
 };
@@ -61,6 +64,11 @@ struct Plan {
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_pack_int4(const int32_t *in, uint8_t *out, int64_t K, int64_t N, cudaStream_t s);
 cudaError_t launch_generic(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
+cudaError_t launch_prefill(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
+cudaError_t launch_row_prep(const Problem &p, float *rowsum, int8_t *e_row, __half *x16,
+                            cudaStream_t s);
+cudaError_t launch_so_prep(const Problem &p, int8_t *e_col, __half *S16, __half *O16,
+                           cudaStream_t s);
 cudaError_t launch_epilogue(const Problem &p, const Plan &plan, const void *ws, bool pdl,
                             cudaStream_t s);
 
@@ -69,6 +77,8 @@ void set_last_error(int32_t code, const char *msg);
 
 // Plan builders.
 bool plan_generic(const Problem &p, Plan &plan);
+bool prefill_applicable(const Problem &p);
+bool plan_prefill(const Problem &p, Plan &plan);
 void plan_epilogue(const Problem &p, Plan &plan);
 
 }  // namespace wq

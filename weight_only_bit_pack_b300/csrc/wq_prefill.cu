@@ -1,0 +1,850 @@
+// Prefill (large-M) kernel of the weight-only quantized matmul with the fused
+// residual-add + RMSNorm epilogue (aclnnWeightQuantMatmulAllReduceAddRmsNorm,
+// "Function description": mm_out = x1 @ (x2*antiquantScale + antiquantOffset)
+// + bias; y = mm_out + residual; normOut = y / RMS(y) * gamma).
+//
+// One persistent CTA per SM walks output tiles of BM x BN = 128 x 256 in
+// row-block-major order. Warp roles (16 warps):
+//   warp 0       TMA producer: x1 tile (128 x 64, 128-byte swizzle) and the
+//                packed weight tile (64 k-rows x 256 n, INT4 or INT8) per k-step.
+//   warp 1       TMEM owner (512 columns = two 128 x 256 fp32 accumulators) and
+//                tcgen05.mma issuer (M=128, N=256, K=16, kind::f16).
+//   warps 4-11   dequant: packed weight -> B operand (W^T, 256 x 64, K-major,
+//                128-byte swizzle), in one of two exact forms (below).
+//   warps 12-15  epilogue (one per TMEM lane quarter): y = acc + bias +
+//                residual, written to HBM and kept (fp32) in TMEM; per-row
+//                partial sum(y^2) published to the workspace; then, for the
+//                previous tile, wait until every n-tile of its row block has
+//                published, sum the partials in a fixed order, and write
+//                normOut = y * rstd * gamma from TMEM. y is never read back
+//                from memory.
+// Operand modes (both keep the dequantized weight exact or within 2^-12):
+//   RAWQ   per-tensor / per-channel scales: B holds the integer q itself (exact
+//          in fp16 and bf16), the MMA accumulates x1*q in fp32, and the epilogue
+//          applies mm = S[n]*acc + O[n]*rowsum(x1[m,:]) + bias.
+//   F16EMU bf16 per-group scales: A is an fp16 copy of x1 (exact; a per-row
+//          power of two e_m keeps it in range) and B = q*S16 + O16 in fp16,
+//          where S16/O16 are the scales times a per-column power of two e_n so
+//          that q*S16 is exact (8-bit significand x 3-bit q <= 11 bits); only
+//          the offset add rounds, at 2^-12. The epilogue multiplies by
+//          2^(e_m + e_n). Rounding W to bf16 instead (2^-9) would put the
+//          result outside the operator's stated tolerance at these K.
+// Pipelines: NR raw stages (x1 + packed weight) and NB dequantized-weight
+// stages, each guarded by full/empty mbarriers; two accumulator buffers, so
+// the epilogue of tile j overlaps the main loop of tile j+1.
+//
+// Cross-CTA row reduction: all CTAs are co-resident (grid <= SMs, 1 CTA/SM)
+// and a CTA publishes tile j before it waits for the row block of tile j-1;
+// with n-tiles per row <= grid size every wait depends only on tiles with a
+// smaller index, so the waits always end. Every wait is bounded anyway: on
+// timeout the kernel sets the workspace status word, stops waiting and exits
+// after draining its own copies and MMAs, leaving the context usable.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "wq_common.cuh"
+#include "wq_internal.h"
+#include "wq_sm100.cuh"
+
+namespace wq {
+namespace {
+
+using namespace sm100;
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int NR = 4;  // raw stages: x1 tile + packed weight tile
+constexpr int NB = 2;  // dequantized weight stages
+constexpr int kThreads = 512;
+constexpr int kDqWarp0 = 4, kDqWarps = 8;
+constexpr int kEpiWarp0 = 12, kEpiWarps = 4;
+constexpr uint32_t kTmemCols = 512;
+constexpr long long kWaitBudget = 4000000000LL;  // clock64 cycles, about 2 s
+
+// Where a bounded wait gave up (upper bits of the status word).
+enum Where : uint32_t {
+  kWhereProducer = 1, kWhereMma = 2, kWhereDequant = 3, kWhereEpiAcc = 4, kWhereRowBlock = 5
+};
+
+enum Mode : int { kRawQ = 0, kF16Emu = 1 };
+
+struct PrefillArgs {
+  const void *scale, *offset, *bias, *residual, *gamma;
+  void *y, *normOut;
+  uint32_t *status;
+  uint32_t *counters;
+  float *rowpart;
+  const float *rowsum;       // RAWQ with offset: sum_k x1[m, k]
+  const int8_t *e_row;       // F16EMU: row exponents
+  const int8_t *e_col;       // F16EMU: column exponents
+  const __half *S16, *O16;   // F16EMU: scaled fp16 scale / offset (G x N)
+  long long M;
+  int K, N, group, Ns, nTilesN, kTiles;
+  long long nTiles;
+  float eps;
+};
+
+template <int WBITS>
+struct Layout {
+  static constexpr uint32_t A_BYTES = BM * BK * 2;            // 16 KB
+  static constexpr uint32_t BQ_BYTES = BK * BN * WBITS / 8;   // 8 or 16 KB
+  static constexpr uint32_t B_BYTES = BN * BK * 2;            // 32 KB
+  static constexpr uint32_t A_OFF = 0;
+  static constexpr uint32_t BQ_OFF = A_OFF + NR * A_BYTES;
+  static constexpr uint32_t B_OFF = BQ_OFF + NR * BQ_BYTES;
+  static constexpr uint32_t BAR_OFF = B_OFF + NB * B_BYTES;
+  static constexpr int NBARS = 2 * NR + 2 * NB + 4 + 1;
+  static constexpr uint32_t SMEM = BAR_OFF + 8 * NBARS + 16 + 1024;
+};
+
+// barrier indices
+__device__ __forceinline__ int FULL(int s) { return s; }
+__device__ __forceinline__ int RAWEMPTY(int s) { return NR + s; }
+__device__ __forceinline__ int BFULL(int s) { return 2 * NR + s; }
+__device__ __forceinline__ int BEMPTY(int s) { return 2 * NR + NB + s; }
+__device__ __forceinline__ int ACCFULL(int b) { return 2 * NR + 2 * NB + b; }
+__device__ __forceinline__ int ACCEMPTY(int b) { return 2 * NR + 2 * NB + 2 + b; }
+__device__ __forceinline__ int DRAIN() { return 2 * NR + 2 * NB + 4; }
+
+__device__ __forceinline__ void record_timeout(uint32_t *status, uint32_t where) {
+  atomicOr(status, (uint32_t)WQ_ERR_DEVICE_TIMEOUT | (where << 8));
+}
+
+// Bounded wait on an mbarrier phase; gives up when another role aborted or the
+// budget ran out (then it aborts the CTA and records where).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         uint32_t *status, uint32_t where) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitBudget) {
+      *abort_flag = 1;
+      record_timeout(status, where);
+      return false;
+    }
+  }
+}
+
+// Warp-collective form: every lane polls (each gets the barrier's acquire) and
+// the warp takes one decision, so no lane leaves a loop its warp-mates stay in.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                              uint32_t *status, uint32_t where) {
+  const bool ok = wait_bar(bar, parity, abort_flag, status, where);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Wait used only while draining: ignores the abort flag, bounded budget.
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitBudget) return;
+  }
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// (lo, hi) 16-bit halves of a packed pair, both set to the half `h` of w.
+__device__ __forceinline__ uint32_t dup_half(uint32_t w, int h) {
+  return __byte_perm(w, w, h ? 0x3232 : 0x1010);
+}
+
+// Packed pair arithmetic in the activation dtype: (v - c) * s + o, one rounding
+// for the subtraction (exact here: small integers) and one for the fma.
+template <int DT>
+__device__ __forceinline__ uint32_t sub_fma2(uint32_t v, uint32_t c, uint32_t s, uint32_t o) {
+  uint32_t r;
+  if (DT == WQ_BF16) {
+    asm("{\n\t.reg .b32 t;\n\t"
+        "sub.rn.bf16x2 t, %1, %2;\n\t"
+        "fma.rn.bf16x2 %0, t, %3, %4;\n\t}"
+        : "=r"(r)
+        : "r"(v), "r"(c), "r"(s), "r"(o));
+  } else {
+    asm("{\n\t.reg .b32 t;\n\t"
+        "sub.rn.f16x2 t, %1, %2;\n\t"
+        "fma.rn.f16x2 %0, t, %3, %4;\n\t}"
+        : "=r"(r)
+        : "r"(v), "r"(c), "r"(s), "r"(o));
+  }
+  return r;
+}
+
+// Loads per-group S and O (element type SDT, G x N) for CNT consecutive
+// columns starting at n, duplicated into packed pairs; zero when the k-octet
+// or the columns are out of range (such weights meet zero-filled x1 or are
+// never stored).
+template <int SDT, int CNT>
+__device__ __forceinline__ void load_so(const void *Sv, const void *Ov, const PrefillArgs &a, int k,
+                                        int n, uint32_t (&s2)[CNT], uint32_t (&o2)[CNT]) {
+  using T = typename Elem<SDT>::T;
+  if (k >= a.K || n >= a.N) {
+#pragma unroll
+    for (int j = 0; j < CNT; ++j) s2[j] = o2[j] = 0u;
+    return;
+  }
+  const long long r = k / a.group;
+  const T *sp = static_cast<const T *>(Sv) + r * a.N + n;
+  const T *op = Ov ? static_cast<const T *>(Ov) + r * a.N + n : nullptr;
+  uint32_t sw[CNT / 2], ow[CNT / 2];
+  if constexpr (CNT == 8) {
+    const uint4 v = *reinterpret_cast<const uint4 *>(sp);
+    sw[0] = v.x; sw[1] = v.y; sw[2] = v.z; sw[3] = v.w;
+    if (op) {
+      const uint4 u = *reinterpret_cast<const uint4 *>(op);
+      ow[0] = u.x; ow[1] = u.y; ow[2] = u.z; ow[3] = u.w;
+    } else {
+      ow[0] = ow[1] = ow[2] = ow[3] = 0u;
+    }
+  } else {
+    const uint2 v = *reinterpret_cast<const uint2 *>(sp);
+    sw[0] = v.x; sw[1] = v.y;
+    if (op) {
+      const uint2 u = *reinterpret_cast<const uint2 *>(op);
+      ow[0] = u.x; ow[1] = u.y;
+    } else {
+      ow[0] = ow[1] = 0u;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < CNT; ++j) {
+    s2[j] = dup_half(sw[j >> 1], j & 1);
+    o2[j] = dup_half(ow[j >> 1], j & 1);
+  }
+}
+
+// Packed pair subtraction in the operand dtype (exact here: small integers).
+template <int DT>
+__device__ __forceinline__ uint32_t sub2(uint32_t v, uint32_t c) {
+  uint32_t r;
+  if (DT == WQ_BF16)
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(c));
+  else
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(c));
+  return r;
+}
+
+// Byte offset of the 16-byte chunk (row r, k-octet c) in a K-major 128-byte
+// swizzled tile with 64 elements per row.
+__device__ __forceinline__ uint32_t sw128_chunk(int r, int c) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+template <int DT, int WBITS, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                   const PrefillArgs a) {
+  using L = Layout<WBITS>;
+  using E = Elem<DT>;
+  using T = typename E::T;
+  constexpr int MDT = MODE == kF16Emu ? WQ_F16 : DT;  // operand dtype of the MMA
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  auto BAR = [&](int i) -> uint32_t { return sbase + L::BAR_OFF + 8u * i; };
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::BAR_OFF + 8 * L::NBARS);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NR; ++s) {
+      mbar_init(BAR(FULL(s)), 1);
+      mbar_init(BAR(RAWEMPTY(s)), kDqWarps + 1);
+    }
+    for (int s = 0; s < NB; ++s) {
+      mbar_init(BAR(BFULL(s)), kDqWarps);
+      mbar_init(BAR(BEMPTY(s)), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(BAR(ACCFULL(b)), 1);
+      mbar_init(BAR(ACCEMPTY(b)), kEpiWarps);
+    }
+    mbar_init(BAR(DRAIN()), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_x);
+    prefetch_tmap(&tm_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    long long it = 0;
+    for (long long t = blockIdx.x; t < a.nTiles; t += gridDim.x) {
+      const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
+      for (int ks = 0; ks < a.kTiles; ++ks, ++it) {
+        const int s = (int)(it % NR);
+        const uint32_t ph = (uint32_t)((it / NR) & 1);
+        if (!wait_bar_warp(BAR(RAWEMPTY(s)), ph ^ 1u, abort_flag, a.status, kWhereProducer)) goto pdone;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(BAR(FULL(s)), L::A_BYTES + L::BQ_BYTES);
+          tma_load_2d(sbase + L::A_OFF + s * L::A_BYTES, &tm_x, ks * BK, rb * BM, BAR(FULL(s)));
+          tma_load_2d(sbase + L::BQ_OFF + s * L::BQ_BYTES, &tm_w, nt * (BN * WBITS / 8), ks * BK,
+                      BAR(FULL(s)));
+        }
+        __syncwarp();
+      }
+    }
+  pdone:
+    // every copy this warp issued has landed before the CTA may exit
+    for (long long j = (it > NR ? it - NR : 0); j < it; ++j)
+      drain_bar(BAR(FULL((int)(j % NR))), (uint32_t)((j / NR) & 1));
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    {
+      const uint32_t idesc = idesc_f16(MDT == WQ_BF16 ? 1u : 0u, BM, BN);
+      long long it = 0;
+      int lt = 0;
+      for (long long t = blockIdx.x; t < a.nTiles; t += gridDim.x, ++lt) {
+        const int buf = lt & 1;
+        if (!wait_bar_warp(BAR(ACCEMPTY(buf)), (uint32_t)(((lt >> 1) & 1) ^ 1), abort_flag, a.status,
+                           kWhereMma))
+          goto mdone;
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+        for (int ks = 0; ks < a.kTiles; ++ks, ++it) {
+          const int s = (int)(it % NR), sb = (int)(it % NB);
+          if (!wait_bar_warp(BAR(FULL(s)), (uint32_t)((it / NR) & 1), abort_flag, a.status, kWhereMma))
+            goto mdone;
+          if (!wait_bar_warp(BAR(BFULL(sb)), (uint32_t)((it / NB) & 1), abort_flag, a.status,
+                             kWhereMma))
+            goto mdone;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t aaddr = sbase + L::A_OFF + s * L::A_BYTES;
+            const uint32_t baddr = sbase + L::B_OFF + sb * L::B_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              mma_f16(d, desc_kmajor_sw128(aaddr + kk * 32), desc_kmajor_sw128(baddr + kk * 32),
+                      idesc, (ks | kk) != 0 ? 1u : 0u);
+            mma_commit(BAR(BEMPTY(sb)));
+            mma_commit(BAR(RAWEMPTY(s)));
+          }
+          __syncwarp();
+        }
+        if (lane == 0) mma_commit(BAR(ACCFULL(buf)));
+        __syncwarp();
+      }
+    mdone:
+      if (lane == 0) mma_commit(BAR(DRAIN()));
+      __syncwarp();
+      drain_bar(BAR(DRAIN()), 0);
+      __syncwarp();
+    }
+  } else if (warp >= kDqWarp0 && warp < kDqWarp0 + kDqWarps) {
+    // ---------------------------------------------------------------- dequant
+    // Each thread owns one k-octet (8 k-rows) of 8 (INT4) or 2 x 4 (INT8)
+    // consecutive columns per stage. The k-octet is rotated by lane so that
+    // both the packed-word loads and the 16-byte swizzled stores are free of
+    // shared-memory bank conflicts.
+    const int dw = warp - kDqWarp0;
+    const int ko = (dw + lane) & 7;
+    // INT4: nibble r, u = r ^ 8 = q + 8, and (magic | u) is the 16-bit float
+    // 128 + u (bf16) or 1024 + u (fp16); subtracting `magic` gives q exactly.
+    const uint32_t magic4 = MDT == WQ_BF16 ? 0x43084308u : 0x64086408u;
+    long long it = 0;
+    for (long long t = blockIdx.x; t < a.nTiles; t += gridDim.x) {
+      const int nt = (int)(t % a.nTilesN);
+      const int n0 = nt * BN;
+      for (int ks = 0; ks < a.kTiles; ++ks, ++it) {
+        const int s = (int)(it % NR), sb = (int)(it % NB);
+        const int k = ks * BK + 8 * ko;
+        const uint32_t bq = sbase + L::BQ_OFF + s * L::BQ_BYTES;
+        const uint32_t bst = sbase + L::B_OFF + sb * L::B_BYTES;
+        if constexpr (WBITS == 4) {
+          uint32_t s2[8], o2[8];
+          if constexpr (MODE == kF16Emu) load_so<WQ_F16, 8>(a.S16, a.O16, a, k, n0 + 8 * lane, s2, o2);
+          if (!wait_bar_warp(BAR(FULL(s)), (uint32_t)((it / NR) & 1), abort_flag, a.status,
+                             kWhereDequant))
+            goto ddone;
+          if (!wait_bar_warp(BAR(BEMPTY(sb)), (uint32_t)(((it / NB) & 1) ^ 1), abort_flag, a.status,
+                             kWhereDequant))
+            goto ddone;
+          uint32_t wr[8], wsh[8];
+#pragma unroll
+          for (int tt = 0; tt < 8; ++tt) wr[tt] = ld_shared_u32(bq + (8 * ko + tt) * 128 + 4 * lane);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(RAWEMPTY(s)));
+#pragma unroll
+          for (int tt = 0; tt < 8; ++tt) wsh[tt] = wr[tt] >> 4;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t b = (uint32_t)(j >> 1);
+            const uint32_t sel = b | ((b + 4u) << 8);
+            uint32_t c[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+              const uint32_t x = (j & 1) ? __byte_perm(wsh[2 * p], wsh[2 * p + 1], sel)
+                                         : __byte_perm(wr[2 * p], wr[2 * p + 1], sel);
+              const uint32_t v = (x & 0x000F000Fu) ^ magic4;
+              if constexpr (MODE == kF16Emu)
+                c[p] = sub_fma2<WQ_F16>(v, magic4, s2[j], o2[j]);
+              else
+                c[p] = sub2<MDT>(v, magic4);
+            }
+            st_shared_v4(bst + sw128_chunk(8 * lane + j, ko), c[0], c[1], c[2], c[3]);
+          }
+        } else {
+          uint32_t s2a[4], o2a[4], s2b[4], o2b[4];
+          if constexpr (MODE == kF16Emu) {
+            load_so<WQ_F16, 4>(a.S16, a.O16, a, k, n0 + 4 * lane, s2a, o2a);
+            load_so<WQ_F16, 4>(a.S16, a.O16, a, k, n0 + 4 * (lane + 32), s2b, o2b);
+          }
+          if (!wait_bar_warp(BAR(FULL(s)), (uint32_t)((it / NR) & 1), abort_flag, a.status,
+                             kWhereDequant))
+            goto ddone;
+          if (!wait_bar_warp(BAR(BEMPTY(sb)), (uint32_t)(((it / NB) & 1) ^ 1), abort_flag, a.status,
+                             kWhereDequant))
+            goto ddone;
+          uint32_t wa[8], wb[8];
+#pragma unroll
+          for (int tt = 0; tt < 8; ++tt) {
+            wa[tt] = ld_shared_u32(bq + (8 * ko + tt) * 256 + 4 * lane);
+            wb[tt] = ld_shared_u32(bq + (8 * ko + tt) * 256 + 4 * (lane + 32));
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(RAWEMPTY(s)));
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t *w = half ? wb : wa;
+            const int nq = lane + 32 * half;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t sel = (uint32_t)j | ((uint32_t)(j + 4) << 8);
+              uint32_t c[4];
+#pragma unroll
+              for (int p = 0; p < 4; ++p) {
+                const uint32_t x = __byte_perm(w[2 * p], w[2 * p + 1], sel);
+                if constexpr (MDT == WQ_F16) {
+                  // byte b, (b ^ 0x80) | 0x6400 is the fp16 value 1152 + q
+                  const uint32_t v = (x & 0x00FF00FFu) ^ 0x64806480u;
+                  if constexpr (MODE == kF16Emu)
+                    c[p] = sub_fma2<WQ_F16>(v, 0x64806480u, half ? s2b[j] : s2a[j],
+                                            half ? o2b[j] : o2a[j]);
+                  else
+                    c[p] = sub2<WQ_F16>(v, 0x64806480u);
+                } else {
+                  // bf16 operand, raw q: |q| <= 128 is exact in bf16
+                  c[p] = pack2<WQ_BF16>((float)(int8_t)(x & 0xFFu), (float)(int8_t)((x >> 16) & 0xFFu));
+                }
+              }
+              st_shared_v4(bst + sw128_chunk(4 * nq + j, ko), c[0], c[1], c[2], c[3]);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(BFULL(sb)));
+      }
+    }
+  ddone:;
+  } else if (warp >= kEpiWarp0) {
+    // ---------------------------------------------------------------- epilogue
+    const int qd = warp & 3;  // TMEM lane quarter
+    const int rit = 32 * qd + lane;
+    const T *bias = static_cast<const T *>(a.bias);
+    const T *res = static_cast<const T *>(a.residual);
+    const T *gam = static_cast<const T *>(a.gamma);
+    T *yout = static_cast<T *>(a.y);
+    T *nout = static_cast<T *>(a.normOut);
+    const uint32_t lane_addr = tmem_base + ((uint32_t)(32 * qd) << 16);
+    int lt = 0;
+    long long prev_t = -1;
+    bool ok = true;
+
+    auto normalize = [&](long long t, int buf) -> bool {
+      const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
+      const long long m = (long long)rb * BM + rit;
+      const bool row_ok = m < a.M;
+      // wait until every n-tile of this row block published its partial sums
+      {
+        const uint32_t target = (uint32_t)(kEpiWarps * a.nTilesN);
+        const long long t0 = clock64();
+        bool done = false;
+        while (true) {
+          done = ld_acquire_u32(a.counters + rb) >= target;
+          if (done || *abort_flag) break;
+          if (clock64() - t0 > kWaitBudget) {
+            *abort_flag = 1;
+            record_timeout(a.status, kWhereRowBlock);
+            break;
+          }
+          __nanosleep(64);
+        }
+        if (!__all_sync(0xffffffffu, done)) return false;
+      }
+      float tot = 0.f;
+      if (row_ok) {
+        const float *rp = a.rowpart + m * a.nTilesN;
+        for (int j = 0; j < a.nTilesN; ++j) tot += __ldcg(rp + j);
+      }
+      const float rstd = rsqrtf(tot / (float)a.N + a.eps);
+      const uint32_t taddr = lane_addr + (uint32_t)(buf * BN);
+      const int n0 = nt * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(taddr + 32 * c, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int n = n0 + 32 * c + 8 * v;
+          if (n < a.N && row_ok) {
+            const uint4 g = *reinterpret_cast<const uint4 *>(gam + n);
+            const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 g2 = unpack2<DT>(gw[i]);
+              o[i] = pack2<DT>(__uint_as_float(r[8 * v + 2 * i]) * rstd * g2.x,
+                               __uint_as_float(r[8 * v + 2 * i + 1]) * rstd * g2.y);
+            }
+            *reinterpret_cast<uint4 *>(nout + m * a.N + n) = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(ACCEMPTY(buf)));
+      return true;
+    };
+
+    for (long long t = blockIdx.x; t < a.nTiles && ok; t += gridDim.x, ++lt) {
+      const int buf = lt & 1;
+      if (!wait_bar_warp(BAR(ACCFULL(buf)), (uint32_t)((lt >> 1) & 1), abort_flag, a.status,
+                         kWhereEpiAcc)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
+      const long long m = (long long)rb * BM + rit;
+      const bool row_ok = m < a.M;
+      const int n0 = nt * BN;
+      const uint32_t taddr = lane_addr + (uint32_t)(buf * BN);
+      float ss = 0.f;
+      // per-row factor of this thread's row
+      float rs = 0.f;   // RAWQ + offset: sum_k x1[m, k]
+      int em = 0;       // F16EMU: row exponent
+      if (row_ok) {
+        if constexpr (MODE == kRawQ) {
+          if (a.offset) rs = a.rowsum[m];
+        } else {
+          em = a.e_row[m];
+        }
+      }
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(taddr + 32 * c, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int n = n0 + 32 * c + 8 * v;
+          float yv[8];
+          if (n < a.N) {
+            // mm = the operator's x1 @ W for these 8 columns
+            float mmv[8];
+            if constexpr (MODE == kRawQ) {
+              uint32_t sw[4], ow[4] = {0u, 0u, 0u, 0u};
+              if (a.Ns == 1) {
+                const uint32_t sb = *reinterpret_cast<const uint16_t *>(a.scale);
+                sw[0] = sw[1] = sw[2] = sw[3] = sb | (sb << 16);
+                if (a.offset) {
+                  const uint32_t ob = *reinterpret_cast<const uint16_t *>(a.offset);
+                  ow[0] = ow[1] = ow[2] = ow[3] = ob | (ob << 16);
+                }
+              } else {
+                const uint4 sv = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.scale) + n);
+                sw[0] = sv.x; sw[1] = sv.y; sw[2] = sv.z; sw[3] = sv.w;
+                if (a.offset) {
+                  const uint4 ov = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.offset) + n);
+                  ow[0] = ov.x; ow[1] = ov.y; ow[2] = ov.z; ow[3] = ov.w;
+                }
+              }
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 s2 = unpack2<DT>(sw[i]);
+                const float2 o2 = unpack2<DT>(ow[i]);
+                mmv[2 * i] = fmaf(s2.x, __uint_as_float(r[8 * v + 2 * i]), o2.x * rs);
+                mmv[2 * i + 1] = fmaf(s2.y, __uint_as_float(r[8 * v + 2 * i + 1]), o2.y * rs);
+              }
+            } else {
+              const uint2 ev = *reinterpret_cast<const uint2 *>(a.e_col + n);
+              const uint32_t ew[2] = {ev.x, ev.y};
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int en = (int)(int8_t)((ew[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+                mmv[i] = __uint_as_float(r[8 * v + i]) * __int_as_float((em + en + 127) << 23);
+              }
+            }
+            uint32_t bw[4] = {0u, 0u, 0u, 0u}, rw[4] = {0u, 0u, 0u, 0u};
+            if (bias) {
+              const uint4 bb = *reinterpret_cast<const uint4 *>(bias + n);
+              bw[0] = bb.x; bw[1] = bb.y; bw[2] = bb.z; bw[3] = bb.w;
+            }
+            if (row_ok) {
+              const uint4 rr = *reinterpret_cast<const uint4 *>(res + m * a.N + n);
+              rw[0] = rr.x; rw[1] = rr.y; rw[2] = rr.z; rw[3] = rr.w;
+            }
+            uint32_t yo[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 b2 = unpack2<DT>(bw[i]);
+              const float2 r2 = unpack2<DT>(rw[i]);
+              yv[2 * i] = mmv[2 * i] + b2.x + r2.x;
+              yv[2 * i + 1] = mmv[2 * i + 1] + b2.y + r2.y;
+              yo[i] = pack2<DT>(yv[2 * i], yv[2 * i + 1]);
+            }
+            if (row_ok) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) ss = fmaf(yv[i], yv[i], ss);
+              *reinterpret_cast<uint4 *>(yout + m * a.N + n) = make_uint4(yo[0], yo[1], yo[2], yo[3]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) yv[i] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) r[8 * v + i] = __float_as_uint(yv[i]);
+        }
+        tmem_st32(taddr + 32 * c, r);
+      }
+      tmem_wait_st();
+      if (row_ok) a.rowpart[m * a.nTilesN + nt] = ss;
+      // each epilogue warp publishes its 32 rows; the row block is complete
+      // when all kEpiWarps warps of all n-tiles have published
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        red_release_add(a.counters + rb, 1u);
+      }
+      __syncwarp();
+      if (prev_t >= 0) {
+        if (!normalize(prev_t, buf ^ 1)) {
+          ok = false;
+          break;
+        }
+      }
+      prev_t = t;
+    }
+    if (ok && prev_t >= 0) normalize(prev_t, (lt - 1) & 1);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+using EncodeTiledFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+bool aligned16(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) % 16) == 0; }
+
+}  // namespace
+
+static uint64_t align256(uint64_t v) { return (v + 255) / 256 * 256; }
+
+bool prefill_applicable(const Problem &p) {
+  if (p.M < 1 || p.N < 1) return false;
+  if (p.K % 8 != 0) return false;                       // x1 row stride: 16-byte multiple for TMA
+  if (p.wbits == 4 ? (p.N % 32 != 0) : (p.N % 16 != 0)) return false;  // packed row stride
+  // fp16 activations with per-group scales have no exact single-operand form
+  // (an 11-bit fp16 scale times q needs more than 11 bits): other kernels.
+  if (p.smode == kPerGroup && p.dtype == WQ_F16) return false;
+  const void *ptrs[] = {p.x1, p.x2, p.scale, p.offset, p.bias, p.residual, p.gamma, p.y, p.normOut};
+  for (const void *q : ptrs)
+    if (!aligned16(q)) return false;
+  const int64_t nTilesN = (p.N + BN - 1) / BN;
+  if (nTilesN > device_info().sms) return false;        // row-block waits need n-tiles <= CTAs
+  return true;
+}
+
+bool plan_prefill(const Problem &p, Plan &plan) {
+  if (!prefill_applicable(p)) return false;
+  plan.kernel = WQ_KERNEL_PREFILL;
+  plan.mode = p.smode == kPerGroup ? kF16Emu : kRawQ;
+  plan.n_tiles = (p.N + BN - 1) / BN;
+  plan.m_tiles = (p.M + BM - 1) / BM;
+  const int64_t tiles = plan.n_tiles * plan.m_tiles;
+  plan.grid = (int)(tiles < device_info().sms ? tiles : device_info().sms);
+  uint64_t off = kWsHeader;
+  plan.cnt_off = off;
+  off += align256((uint64_t)plan.m_tiles * 4);
+  plan.rowpart_off = off;
+  off += align256((uint64_t)p.M * (uint64_t)plan.n_tiles * sizeof(float));
+  if (plan.mode == kRawQ) {
+    if (p.offset) {
+      plan.rowsum_off = off;
+      off += align256((uint64_t)p.M * sizeof(float));
+    }
+  } else {
+    plan.erow_off = off;
+    off += align256((uint64_t)p.M);
+    plan.ecol_off = off;
+    off += align256((uint64_t)p.N);
+    plan.s16_off = off;
+    off += align256((uint64_t)p.G * p.N * 2);
+    if (p.offset) {
+      plan.o16_off = off;
+      off += align256((uint64_t)p.G * p.N * 2);
+    }
+    plan.x16_off = off;
+    off += align256((uint64_t)p.M * p.K * 2);
+  }
+  plan.ws_bytes = off;
+  return true;
+}
+
+template <int DT, int WBITS, int MODE>
+static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws, cudaStream_t s) {
+  using L = Layout<WBITS>;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(prefill_kernel<DT, WBITS, MODE>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  char *wsb = static_cast<char *>(ws);
+
+  PrefillArgs args = {};
+  args.scale = p.scale; args.offset = p.offset; args.bias = p.bias; args.residual = p.residual;
+  args.gamma = p.gamma; args.y = p.y; args.normOut = p.normOut;
+  args.status = reinterpret_cast<uint32_t *>(ws);
+  args.counters = reinterpret_cast<uint32_t *>(wsb + plan.cnt_off);
+  args.rowpart = reinterpret_cast<float *>(wsb + plan.rowpart_off);
+  args.M = p.M; args.K = (int)p.K; args.N = (int)p.N; args.group = (int)p.group; args.Ns = (int)p.Ns;
+  args.nTilesN = (int)plan.n_tiles;
+  args.kTiles = (int)((p.K + BK - 1) / BK);
+  args.nTiles = plan.n_tiles * plan.m_tiles;
+  args.eps = p.eps;
+
+  // status word and row-block counters start at zero on every call
+  cudaError_t e = cudaMemsetAsync(ws, 0, plan.rowpart_off, s);
+  if (e != cudaSuccess) return e;
+
+  const void *a_src = p.x1;
+  CUtensorMapDataType a_type =
+      DT == WQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if constexpr (MODE == kRawQ) {
+    if (p.offset) {
+      float *rowsum = reinterpret_cast<float *>(wsb + plan.rowsum_off);
+      e = launch_row_prep(p, rowsum, nullptr, nullptr, s);
+      if (e != cudaSuccess) return e;
+      args.rowsum = rowsum;
+    }
+  } else {
+    int8_t *e_row = reinterpret_cast<int8_t *>(wsb + plan.erow_off);
+    int8_t *e_col = reinterpret_cast<int8_t *>(wsb + plan.ecol_off);
+    __half *S16 = reinterpret_cast<__half *>(wsb + plan.s16_off);
+    __half *O16 = p.offset ? reinterpret_cast<__half *>(wsb + plan.o16_off) : nullptr;
+    __half *x16 = reinterpret_cast<__half *>(wsb + plan.x16_off);
+    e = launch_row_prep(p, nullptr, e_row, x16, s);
+    if (e != cudaSuccess) return e;
+    e = launch_so_prep(p, e_col, S16, O16, s);
+    if (e != cudaSuccess) return e;
+    args.e_row = e_row; args.e_col = e_col; args.S16 = S16; args.O16 = O16;
+    a_src = x16;
+    a_type = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  }
+
+  CUtensorMap tm_x, tm_w;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.K * 2};
+    const cuuint32_t box[2] = {BK, BM};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&tm_x, a_type, 2, const_cast<void *>(a_src), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t row_bytes = (cuuint64_t)p.N * WBITS / 8;
+    const cuuint64_t dims[2] = {row_bytes, (cuuint64_t)p.K};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)(BN * WBITS / 8), BK};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(p.x2), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  prefill_kernel<DT, WBITS, MODE><<<plan.grid, kThreads, L::SMEM, s>>>(tm_x, tm_w, args);
+  return cudaGetLastError();
+}
+
+template <int DT, int WBITS>
+static cudaError_t launch_prefill_m(const Problem &p, const Plan &plan, void *ws, cudaStream_t s) {
+  if (plan.mode == kF16Emu) {
+    if constexpr (DT == WQ_BF16) return launch_prefill_t<DT, WBITS, kF16Emu>(p, plan, ws, s);
+    return cudaErrorNotSupported;
+  }
+  return launch_prefill_t<DT, WBITS, kRawQ>(p, plan, ws, s);
+}
+
+cudaError_t launch_prefill(const Problem &p, const Plan &plan, void *ws, cudaStream_t s) {
+  if (p.dtype == WQ_BF16)
+    return p.wbits == 4 ? launch_prefill_m<WQ_BF16, 4>(p, plan, ws, s)
+                        : launch_prefill_m<WQ_BF16, 8>(p, plan, ws, s);
+  return p.wbits == 4 ? launch_prefill_m<WQ_F16, 4>(p, plan, ws, s)
+                      : launch_prefill_m<WQ_F16, 8>(p, plan, ws, s);
+}
+
+}  // namespace wq
