@@ -54,8 +54,11 @@ namespace {
 using namespace sm100;
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int NR = 4;  // raw stages: x1 tile + packed weight tile
-constexpr int NB = 2;  // dequantized weight stages
+// Stage counts: NR raw stages (x1 tile + packed weight tile + scale/offset
+// rows) and NB dequantized-weight stages; INT8 tiles are twice as large, so
+// they get one raw stage less to stay inside 227 KB of shared memory.
+template <int WBITS> struct Stages { static constexpr int NR = WBITS == 4 ? 4 : 3, NB = 3; };
+constexpr int SO_ROWS = 3;  // group rows a 64-deep k-stage can touch (group >= 32)
 constexpr int kThreads = 512;
 constexpr int kDqWarp0 = 4, kDqWarps = 8;
 constexpr int kEpiWarp0 = 12, kEpiWarps = 4;
@@ -83,29 +86,34 @@ struct PrefillArgs {
   int K, N, group, Ns, nTilesN, kTiles;
   long long nTiles;
   float eps;
+  uint32_t so_bytes;         // F16EMU: bytes of one scale/offset row box (rows x 256 x 2)
 };
 
 template <int WBITS>
 struct Layout {
+  static constexpr int NR = Stages<WBITS>::NR, NB = Stages<WBITS>::NB;
   static constexpr uint32_t A_BYTES = BM * BK * 2;            // 16 KB
   static constexpr uint32_t BQ_BYTES = BK * BN * WBITS / 8;   // 8 or 16 KB
   static constexpr uint32_t B_BYTES = BN * BK * 2;            // 32 KB
+  static constexpr uint32_t SO_BYTES = SO_ROWS * BN * 2;      // 1.5 KB: fp16 rows of S16 / O16
   static constexpr uint32_t A_OFF = 0;
   static constexpr uint32_t BQ_OFF = A_OFF + NR * A_BYTES;
   static constexpr uint32_t B_OFF = BQ_OFF + NR * BQ_BYTES;
-  static constexpr uint32_t BAR_OFF = B_OFF + NB * B_BYTES;
+  static constexpr uint32_t S_OFF = B_OFF + NB * B_BYTES;
+  static constexpr uint32_t O_OFF = S_OFF + NR * SO_BYTES;
+  static constexpr uint32_t BAR_OFF = O_OFF + NR * SO_BYTES;
   static constexpr int NBARS = 2 * NR + 2 * NB + 4 + 1;
   static constexpr uint32_t SMEM = BAR_OFF + 8 * NBARS + 16 + 1024;
 };
 
-// barrier indices
-__device__ __forceinline__ int FULL(int s) { return s; }
-__device__ __forceinline__ int RAWEMPTY(int s) { return NR + s; }
-__device__ __forceinline__ int BFULL(int s) { return 2 * NR + s; }
-__device__ __forceinline__ int BEMPTY(int s) { return 2 * NR + NB + s; }
-__device__ __forceinline__ int ACCFULL(int b) { return 2 * NR + 2 * NB + b; }
-__device__ __forceinline__ int ACCEMPTY(int b) { return 2 * NR + 2 * NB + 2 + b; }
-__device__ __forceinline__ int DRAIN() { return 2 * NR + 2 * NB + 4; }
+// barrier indices (NR, NB are the kernel's stage counts)
+#define FULL(s) (s)
+#define RAWEMPTY(s) (NR + (s))
+#define BFULL(s) (2 * NR + (s))
+#define BEMPTY(s) (2 * NR + NB + (s))
+#define ACCFULL(b) (2 * NR + 2 * NB + (b))
+#define ACCEMPTY(b) (2 * NR + 2 * NB + 2 + (b))
+#define DRAIN() (2 * NR + 2 * NB + 4)
 
 __device__ __forceinline__ void record_timeout(uint32_t *status, uint32_t where) {
   atomicOr(status, (uint32_t)WQ_ERR_DEVICE_TIMEOUT | (where << 8));
@@ -192,41 +200,29 @@ __device__ __forceinline__ uint32_t sub_fma2(uint32_t v, uint32_t c, uint32_t s,
   return r;
 }
 
-// Loads per-group S and O (element type SDT, G x N) for CNT consecutive
-// columns starting at n, duplicated into packed pairs; zero when the k-octet
-// or the columns are out of range (such weights meet zero-filled x1 or are
-// never stored).
-template <int SDT, int CNT>
-__device__ __forceinline__ void load_so(const void *Sv, const void *Ov, const PrefillArgs &a, int k,
-                                        int n, uint32_t (&s2)[CNT], uint32_t (&o2)[CNT]) {
-  using T = typename Elem<SDT>::T;
-  if (k >= a.K || n >= a.N) {
-#pragma unroll
-    for (int j = 0; j < CNT; ++j) s2[j] = o2[j] = 0u;
-    return;
-  }
-  const long long r = k / a.group;
-  const T *sp = static_cast<const T *>(Sv) + r * a.N + n;
-  const T *op = Ov ? static_cast<const T *>(Ov) + r * a.N + n : nullptr;
+// Reads the fp16 S16/O16 values of CNT consecutive columns (starting at
+// column c of the tile) in group row `row` of the stage's scale/offset rows,
+// duplicated into packed pairs. Rows past the last group were zero-filled by
+// the copy (callers skip k-rows past K, whose rows may be stale).
+template <int CNT>
+__device__ __forceinline__ void smem_so(uint32_t s_base, uint32_t o_base, bool has_o, int row, int c,
+                                        uint32_t (&s2)[CNT], uint32_t (&o2)[CNT]) {
+  const uint32_t off = (uint32_t)(row * BN + c) * 2u;
   uint32_t sw[CNT / 2], ow[CNT / 2];
   if constexpr (CNT == 8) {
-    const uint4 v = *reinterpret_cast<const uint4 *>(sp);
-    sw[0] = v.x; sw[1] = v.y; sw[2] = v.z; sw[3] = v.w;
-    if (op) {
-      const uint4 u = *reinterpret_cast<const uint4 *>(op);
-      ow[0] = u.x; ow[1] = u.y; ow[2] = u.z; ow[3] = u.w;
-    } else {
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(sw[0]), "=r"(sw[1]), "=r"(sw[2]), "=r"(sw[3]) : "r"(s_base + off));
+    if (has_o)
+      asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(ow[0]), "=r"(ow[1]), "=r"(ow[2]), "=r"(ow[3]) : "r"(o_base + off));
+    else
       ow[0] = ow[1] = ow[2] = ow[3] = 0u;
-    }
   } else {
-    const uint2 v = *reinterpret_cast<const uint2 *>(sp);
-    sw[0] = v.x; sw[1] = v.y;
-    if (op) {
-      const uint2 u = *reinterpret_cast<const uint2 *>(op);
-      ow[0] = u.x; ow[1] = u.y;
-    } else {
+    asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(sw[0]), "=r"(sw[1]) : "r"(s_base + off));
+    if (has_o)
+      asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(ow[0]), "=r"(ow[1]) : "r"(o_base + off));
+    else
       ow[0] = ow[1] = 0u;
-    }
   }
 #pragma unroll
   for (int j = 0; j < CNT; ++j) {
@@ -255,11 +251,13 @@ __device__ __forceinline__ uint32_t sw128_chunk(int r, int c) {
 template <int DT, int WBITS, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                   const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_o,
                    const PrefillArgs a) {
   using L = Layout<WBITS>;
   using E = Elem<DT>;
   using T = typename E::T;
   constexpr int MDT = MODE == kF16Emu ? WQ_F16 : DT;  // operand dtype of the MMA
+  constexpr int NR = L::NR, NB = L::NB;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -289,6 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
     prefetch_tmap(&tm_x);
     prefetch_tmap(&tm_w);
+    if (MODE == kF16Emu) {
+      prefetch_tmap(&tm_s);
+      if (a.offset) prefetch_tmap(&tm_o);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
@@ -301,6 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
+    // packed weights are re-read by every row block: keep them in L2
+    const uint64_t pol_w = policy_evict_last();
     long long it = 0;
     for (long long t = blockIdx.x; t < a.nTiles; t += gridDim.x) {
       const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
@@ -309,10 +313,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ph = (uint32_t)((it / NR) & 1);
         if (!wait_bar_warp(BAR(RAWEMPTY(s)), ph ^ 1u, abort_flag, a.status, kWhereProducer)) goto pdone;
         if (lane == 0) {
-          mbar_arrive_expect_tx(BAR(FULL(s)), L::A_BYTES + L::BQ_BYTES);
+          uint32_t bytes = L::A_BYTES + L::BQ_BYTES;
+          if (MODE == kF16Emu) bytes += (a.offset ? 2u : 1u) * a.so_bytes;
+          mbar_arrive_expect_tx(BAR(FULL(s)), bytes);
           tma_load_2d(sbase + L::A_OFF + s * L::A_BYTES, &tm_x, ks * BK, rb * BM, BAR(FULL(s)));
-          tma_load_2d(sbase + L::BQ_OFF + s * L::BQ_BYTES, &tm_w, nt * (BN * WBITS / 8), ks * BK,
-                      BAR(FULL(s)));
+          tma_load_2d_hint(sbase + L::BQ_OFF + s * L::BQ_BYTES, &tm_w, nt * (BN * WBITS / 8),
+                           ks * BK, BAR(FULL(s)), pol_w);
+          if (MODE == kF16Emu) {
+            // the group rows this k-stage touches: (ks*BK)/group .. +SO_ROWS-1
+            const int r0 = (ks * BK) / a.group;
+            tma_load_2d(sbase + L::S_OFF + s * L::SO_BYTES, &tm_s, nt * BN, r0, BAR(FULL(s)));
+            if (a.offset)
+              tma_load_2d(sbase + L::O_OFF + s * L::SO_BYTES, &tm_o, nt * BN, r0, BAR(FULL(s)));
+          }
         }
         __syncwarp();
       }
@@ -377,8 +390,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t magic4 = MDT == WQ_BF16 ? 0x43084308u : 0x64086408u;
     long long it = 0;
     for (long long t = blockIdx.x; t < a.nTiles; t += gridDim.x) {
-      const int nt = (int)(t % a.nTilesN);
-      const int n0 = nt * BN;
       for (int ks = 0; ks < a.kTiles; ++ks, ++it) {
         const int s = (int)(it % NR), sb = (int)(it % NB);
         const int k = ks * BK + 8 * ko;
@@ -386,13 +397,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t bst = sbase + L::B_OFF + sb * L::B_BYTES;
         if constexpr (WBITS == 4) {
           uint32_t s2[8], o2[8];
-          if constexpr (MODE == kF16Emu) load_so<WQ_F16, 8>(a.S16, a.O16, a, k, n0 + 8 * lane, s2, o2);
           if (!wait_bar_warp(BAR(FULL(s)), (uint32_t)((it / NR) & 1), abort_flag, a.status,
                              kWhereDequant))
             goto ddone;
           if (!wait_bar_warp(BAR(BEMPTY(sb)), (uint32_t)(((it / NB) & 1) ^ 1), abort_flag, a.status,
                              kWhereDequant))
             goto ddone;
+          if constexpr (MODE == kF16Emu) {
+            if (k < a.K) {
+              smem_so<8>(sbase + L::S_OFF + s * L::SO_BYTES, sbase + L::O_OFF + s * L::SO_BYTES,
+                         a.offset != nullptr, (k / a.group - (ks * BK) / a.group), 8 * lane, s2, o2);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) s2[j] = o2[j] = 0u;
+            }
+          }
           uint32_t wr[8], wsh[8];
 #pragma unroll
           for (int tt = 0; tt < 8; ++tt) wr[tt] = ld_shared_u32(bq + (8 * ko + tt) * 128 + 4 * lane);
@@ -419,16 +438,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
           uint32_t s2a[4], o2a[4], s2b[4], o2b[4];
-          if constexpr (MODE == kF16Emu) {
-            load_so<WQ_F16, 4>(a.S16, a.O16, a, k, n0 + 4 * lane, s2a, o2a);
-            load_so<WQ_F16, 4>(a.S16, a.O16, a, k, n0 + 4 * (lane + 32), s2b, o2b);
-          }
           if (!wait_bar_warp(BAR(FULL(s)), (uint32_t)((it / NR) & 1), abort_flag, a.status,
                              kWhereDequant))
             goto ddone;
           if (!wait_bar_warp(BAR(BEMPTY(sb)), (uint32_t)(((it / NB) & 1) ^ 1), abort_flag, a.status,
                              kWhereDequant))
             goto ddone;
+          if constexpr (MODE == kF16Emu) {
+            if (k < a.K) {
+              const int rr = k / a.group - (ks * BK) / a.group;
+              const uint32_t sa = sbase + L::S_OFF + s * L::SO_BYTES;
+              const uint32_t oa = sbase + L::O_OFF + s * L::SO_BYTES;
+              smem_so<4>(sa, oa, a.offset != nullptr, rr, 4 * lane, s2a, o2a);
+              smem_so<4>(sa, oa, a.offset != nullptr, rr, 4 * (lane + 32), s2b, o2b);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) s2a[j] = o2a[j] = s2b[j] = o2b[j] = 0u;
+            }
+          }
           uint32_t wa[8], wb[8];
 #pragma unroll
           for (int tt = 0; tt < 8; ++tt) {
@@ -826,7 +853,27 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  prefill_kernel<DT, WBITS, MODE><<<plan.grid, kThreads, L::SMEM, s>>>(tm_x, tm_w, args);
+  CUtensorMap tm_s = tm_w, tm_o = tm_w;  // placeholders unless F16EMU
+  args.so_bytes = 0;
+  if constexpr (MODE == kF16Emu) {
+    const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.G};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.N * 2};
+    const cuuint32_t rows = (cuuint32_t)(p.G < SO_ROWS ? p.G : SO_ROWS);
+    const cuuint32_t box[2] = {BN, rows};
+    const cuuint32_t estr[2] = {1, 1};
+    args.so_bytes = rows * BN * 2;
+    CUresult r = enc(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(args.S16), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (p.offset) {
+      r = enc(&tm_o, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(args.O16), dims,
+              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+  }
+  prefill_kernel<DT, WBITS, MODE><<<plan.grid, kThreads, L::SMEM, s>>>(tm_x, tm_w, tm_s, tm_o, args);
   return cudaGetLastError();
 }
 

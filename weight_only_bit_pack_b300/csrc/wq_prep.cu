@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(256)
     const typename Elem<DT>::T *row = x1 + m * K;
     float s = 0.f, amax = 0.f;
     // K % 8 == 0 (prefill precondition): 16-byte vectors of 8 values
+#pragma unroll 4
     for (int k = lane * 8; k < K; k += 256) {
       const uint4 v = *reinterpret_cast<const uint4 *>(row + k);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -67,6 +68,7 @@ __global__ void __launch_bounds__(256)
       if (lane == 0) e_row[m] = (int8_t)e;
       const float sc = exp2i(-e);
       __half *out = x16 + m * K;
+#pragma unroll 4
       for (int k = lane * 8; k < K; k += 256) {
         const uint4 v = *reinterpret_cast<const uint4 *>(row + k);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -82,30 +84,50 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// One block covers 32 columns; its 8 warps split the group rows, so every warp
+// load reads 32 consecutive columns (coalesced) and the G loads of a column
+// are spread over 8 warps.
 template <int DT>
 __global__ void __launch_bounds__(256)
     so_prep_kernel(const typename Elem<DT>::T *__restrict__ S, const typename Elem<DT>::T *__restrict__ O,
                    int G, int N, float qmax, int8_t *__restrict__ e_col, __half *__restrict__ S16,
                    __half *__restrict__ O16) {
   using E = Elem<DT>;
-  for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < N; n += gridDim.x * blockDim.x) {
-    float mx = 0.f;
-    for (int g = 0; g < G; ++g) {
+  __shared__ float s_max[8][32];
+  __shared__ float s_scale[32];
+  const int cx = threadIdx.x & 31, gy = threadIdx.x >> 5;
+  const int n = blockIdx.x * 32 + cx;
+  float mx = 0.f;
+  if (n < N) {
+#pragma unroll 4
+    for (int g = gy; g < G; g += 8) {
       const float sv = fabsf(E::to_f(S[(int64_t)g * N + n]));
       const float ov = O ? fabsf(E::to_f(O[(int64_t)g * N + n])) : 0.f;
       mx = fmaxf(mx, fmaf(qmax, sv, ov));
     }
+  }
+  s_max[gy][cx] = mx;
+  __syncthreads();
+  if (gy == 0) {
+    float m = s_max[0][cx];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m = fmaxf(m, s_max[i][cx]);
     int e = 0;
-    if (mx > 0.f && mx <= FLT_MAX) {
+    if (m > 0.f && m <= FLT_MAX) {
       int ex;
-      frexpf(mx, &ex);  // mx in [2^(ex-1), 2^ex)
-      e = ex - 13;      // mx * 2^-e in [2^12, 2^13)
+      frexpf(m, &ex);  // m in [2^(ex-1), 2^ex)
+      e = ex - 13;     // m * 2^-e in [2^12, 2^13)
       if (e < -100) e = -100;
       if (e > 100) e = 100;
     }
-    e_col[n] = (int8_t)e;
-    const float sc = exp2i(-e);
-    for (int g = 0; g < G; ++g) {
+    if (n < N) e_col[n] = (int8_t)e;
+    s_scale[cx] = exp2i(-e);
+  }
+  __syncthreads();
+  if (n < N) {
+    const float sc = s_scale[cx];
+#pragma unroll 4
+    for (int g = gy; g < G; g += 8) {
       S16[(int64_t)g * N + n] = __float2half_rn(E::to_f(S[(int64_t)g * N + n]) * sc);
       if (O) O16[(int64_t)g * N + n] = __float2half_rn(E::to_f(O[(int64_t)g * N + n]) * sc);
     }
@@ -133,7 +155,7 @@ cudaError_t launch_row_prep(const Problem &p, float *rowsum, int8_t *e_row, __ha
 cudaError_t launch_so_prep(const Problem &p, int8_t *e_col, __half *S16, __half *O16,
                            cudaStream_t s) {
   const int N = (int)p.N;
-  const int blocks = (N + 255) / 256;
+  const int blocks = (N + 31) / 32;
   const float qmax = p.wbits == 4 ? 8.f : 128.f;
   if (p.dtype == WQ_BF16)
     so_prep_kernel<WQ_BF16><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(p.scale),
