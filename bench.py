@@ -324,7 +324,7 @@ def run_ours(args, world, rank, local):
     ws_bytes = wq.matmul_add_rmsnorm_get_workspace(p.x1, w0, p.scale, p.offset, p.bias,
                                                    p.residual, p.gamma, p.eps, p.group,
                                                    kernel=kernel)
-    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(max(ws_bytes, 2048), dtype=torch.uint8, device=dev)  # header zeroed once
     chosen = int(wq.select_kernel(p.x1, w0, p.scale, p.offset, p.bias, p.residual, p.gamma, p.eps,
                                   p.group)) if kernel == 0 else kernel
 

@@ -82,12 +82,12 @@ typedef enum wq_status {
 } wq_status;
 
 /* Kernel selection for the *_ex entry points. WQ_KERNEL_AUTO is what the plain
- * entry points use: DECODE for small M, PREFILL for large M when the shapes
- * meet its alignment rules, GENERIC otherwise. */
+ * entry points use: DECODE for M <= 16, PREFILL for larger M, each when the
+ * shapes meet its alignment rules, GENERIC otherwise. */
 typedef enum wq_kernel {
     WQ_KERNEL_AUTO = 0,
     WQ_KERNEL_GENERIC = 1,     /* predicated CUDA-core kernel, any shape */
-    WQ_KERNEL_DECODE = 2,      /* weight-streaming mma.sync kernel, small M */
+    WQ_KERNEL_DECODE = 2,      /* weight-streaming TMA + mma.sync kernel, M <= 16, INT4 */
     WQ_KERNEL_PREFILL = 3      /* TMA + tcgen05/TMEM kernel, large M */
 } wq_kernel;
 
@@ -144,9 +144,15 @@ int32_t wq_matmul_add_rmsnorm_get_workspace(
 
 /* Second phase: enqueue the fused operator on `stream`.
  *   ws / ws_bytes  device workspace of at least the size the first phase
- *                  returned for the same arguments (WQ_ERR_WORKSPACE otherwise).
- *                  Its contents on entry do not matter; it holds partial sums,
- *                  counters and the device status word, and is overwritten.
+ *                  returned for the same arguments (WQ_ERR_WORKSPACE otherwise),
+ *                  256-byte aligned. Its first 2048 bytes (the header: the device
+ *                  status word and the counters of the decode kernel) must
+ *                  be zero before the workspace is used for the first time, e.g.
+ *                  one cudaMemsetAsync after allocating it; every call that ends
+ *                  without a device-side error leaves the header zero again, so
+ *                  no per-call clearing is needed. After a device-side error
+ *                  (see wq_read_device_status) zero the header again. The rest
+ *                  of the workspace may hold anything on entry.
  * Accumulation is fp32; y feeds the norm unrounded and y/normOut are rounded
  * once to x1's dtype. Results are bitwise identical from run to run for the
  * same arguments (no floating-point atomics; fixed reduction order). */

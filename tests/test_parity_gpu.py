@@ -34,7 +34,7 @@ def test_tiny_auto(wq):
     _check(wq, to_device(inputs.tiny()), 0)
 
 
-@pytest.mark.parametrize("kernel", [GENERIC])
+@pytest.mark.parametrize("kernel", [GENERIC, DECODE])
 def test_tiny_forced(wq, kernel):
     _check(wq, to_device(inputs.tiny()), kernel)
 
@@ -48,7 +48,7 @@ def test_prefill_rejects_fp16_per_group(wq):
     assert ei.value.status == Status.ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("kernel", [0, GENERIC, PREFILL])
+@pytest.mark.parametrize("kernel", [0, GENERIC, DECODE, PREFILL])
 def test_decode(wq, kernel):
     _check(wq, inputs.decode("cuda"), kernel)
 
@@ -161,7 +161,7 @@ def test_integer_inputs_bit_exact_y(wq):
     to_device(prob)
     mm = (x1.double() @ q.double())
     assert mm.abs().max() <= 2048
-    for kernel in (0, GENERIC, PREFILL):
+    for kernel in (0, GENERIC, DECODE, PREFILL):
         y, _ = run_gpu(wq, prob, kernel)
         assert torch.equal(y.cpu(), mm.to(torch.float16)), kernel
 
@@ -169,7 +169,7 @@ def test_integer_inputs_bit_exact_y(wq):
 def test_deterministic_across_runs(wq):
     prob = inputs.decode("cuda")
     w = gpu_weight(wq, prob)
-    for kernel in (0, GENERIC, PREFILL):
+    for kernel in (0, GENERIC, DECODE, PREFILL):
         a = run_gpu(wq, prob, kernel, w=w)
         b = run_gpu(wq, prob, kernel, w=w)
         assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])

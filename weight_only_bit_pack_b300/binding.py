@@ -187,7 +187,8 @@ def matmul_add_rmsnorm(x1, x2, scale, offset, bias, residual, gamma, eps: float,
     """Fused ``y = x1 @ (x2*scale + offset) + bias + residual``,
     ``normOut = y / sqrt(mean(y^2) + eps) * gamma`` (``wq_matmul_add_rmsnorm``).
 
-    Outputs and workspace are allocated with torch when not given. Pass
+    Outputs and workspace are allocated with torch when not given (a given
+    workspace must have had its first 2048 bytes zeroed once). Pass
     ``y=residual`` for the in-place variant. Returns ``(y, normOut)``.
     """
     if y is None:
@@ -200,7 +201,8 @@ def matmul_add_rmsnorm(x1, x2, scale, offset, bias, residual, gamma, eps: float,
     _check(lib.wq_matmul_add_rmsnorm_get_workspace_ex(*refs[:7], float(eps), int(group), refs[7],
                                                       refs[8], int(kernel), ctypes.byref(ws)))
     if workspace is None:
-        workspace = torch.empty(max(ws.value, 1), dtype=torch.uint8, device=residual.device)
+        # the header must start zeroed (include/wq.h); the library keeps it so
+        workspace = torch.zeros(max(ws.value, 2048), dtype=torch.uint8, device=residual.device)
     elif workspace.numel() < ws.value:
         raise WQError(Status.ERR_WORKSPACE, f"need {ws.value} bytes")
     _check(lib.wq_matmul_add_rmsnorm_ex(*refs[:7], float(eps), int(group), refs[7], refs[8],

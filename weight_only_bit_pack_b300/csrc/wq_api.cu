@@ -240,9 +240,21 @@ int32_t make_plan(const Problem &p, int32_t kernel, Plan &plan) {
     return WQ_OK;
   }
   int chosen = kernel;
-  if (chosen == WQ_KERNEL_AUTO) chosen = prefill_applicable(p) ? WQ_KERNEL_PREFILL : WQ_KERNEL_GENERIC;
-  if (chosen == WQ_KERNEL_DECODE)
-    return fail(WQ_ERR_UNSUPPORTED, "kernel %d is not available for this problem", chosen);
+  if (chosen == WQ_KERNEL_AUTO) {
+    if (p.M <= 16 && decode_applicable(p))
+      chosen = WQ_KERNEL_DECODE;
+    else if (prefill_applicable(p))
+      chosen = WQ_KERNEL_PREFILL;
+    else
+      chosen = WQ_KERNEL_GENERIC;
+  }
+  if (chosen == WQ_KERNEL_DECODE) {
+    if (!plan_decode(p, plan))
+      return fail(WQ_ERR_UNSUPPORTED,
+                  "the decode kernel needs 1 <= m <= 16, INT4 weights, n %% 32 == 0, k %% 8 == 0 "
+                  "and 16-byte aligned x1, x2, scale and offset");
+    return WQ_OK;
+  }
   if (chosen == WQ_KERNEL_PREFILL) {
     if (!plan_prefill(p, plan))
       return fail(WQ_ERR_UNSUPPORTED,
@@ -424,6 +436,10 @@ int32_t wq_matmul_add_rmsnorm_ex(
     case WQ_KERNEL_PREFILL:
       e = launch_prefill(p, plan, ws, s);
       if (e != cudaSuccess) return cuda_fail(e, "prefill kernel launch");
+      break;
+    case WQ_KERNEL_DECODE:
+      e = launch_decode(p, plan, ws, s);
+      if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
       break;
     default:
       return fail(WQ_ERR_UNSUPPORTED, "kernel %d is not available", plan.kernel);

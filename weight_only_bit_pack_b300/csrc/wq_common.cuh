@@ -66,4 +66,15 @@ __device__ __forceinline__ void st_stream_u4(void *p, uint4 v) {
                : "memory");
 }
 
+// Packed pair subtraction in the operand dtype (exact here: small integers).
+template <int DT>
+__device__ __forceinline__ uint32_t sub2(uint32_t v, uint32_t c) {
+  uint32_t r;
+  if (DT == WQ_BF16)
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(c));
+  else
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(c));
+  return r;
+}
+
 }  // namespace wq

@@ -27,9 +27,14 @@ struct Problem {
   void *y = nullptr, *normOut = nullptr;
 };
 
-// Workspace header: the first kWsHeader bytes of every matmul workspace.
-//   word 0: device status (0 = ok, else WQ_ERR_DEVICE_TIMEOUT | where << 8)
-constexpr uint64_t kWsHeader = 256;
+// Workspace header: the first kWsHeader bytes of every matmul workspace. The
+// caller zeroes it once; every kernel leaves it zero after a call that ends
+// without a device-side error (the prefill path clears it per call, the decode
+// kernel resets its counters as it finishes, the generic path leaves it alone).
+//   bytes    0..3     device status (0 = ok, else WQ_ERR_DEVICE_TIMEOUT | where << 8)
+//   bytes  128..135   decode: grid barrier counters (arrive, depart)
+//   bytes 1024..2047  decode: per-tile segment counters (at most 256 tiles)
+constexpr uint64_t kWsHeader = 2048;
 
 // Device properties cached per device (SM count, cluster support ...).
 struct DeviceInfo {
@@ -65,6 +70,7 @@ struct Plan {
 cudaError_t launch_pack_int4(const int32_t *in, uint8_t *out, int64_t K, int64_t N, cudaStream_t s);
 cudaError_t launch_generic(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
 cudaError_t launch_prefill(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
+cudaError_t launch_decode(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
 cudaError_t launch_row_prep(const Problem &p, float *rowsum, int8_t *e_row, __half *x16,
                             cudaStream_t s);
 cudaError_t launch_so_prep(const Problem &p, int8_t *e_col, __half *S16, __half *O16,
@@ -79,6 +85,8 @@ void set_last_error(int32_t code, const char *msg);
 bool plan_generic(const Problem &p, Plan &plan);
 bool prefill_applicable(const Problem &p);
 bool plan_prefill(const Problem &p, Plan &plan);
+bool decode_applicable(const Problem &p);
+bool plan_decode(const Problem &p, Plan &plan);
 void plan_epilogue(const Problem &p, Plan &plan);
 
 }  // namespace wq

@@ -47,6 +47,7 @@
 #include "wq_common.cuh"
 #include "wq_internal.h"
 #include "wq_sm100.cuh"
+#include "wq_sync.cuh"
 
 namespace wq {
 namespace {
@@ -63,7 +64,6 @@ constexpr int kThreads = 512;
 constexpr int kDqWarp0 = 4, kDqWarps = 8;
 constexpr int kEpiWarp0 = 12, kEpiWarps = 4;
 constexpr uint32_t kTmemCols = 512;
-constexpr long long kWaitBudget = 4000000000LL;  // clock64 cycles, about 2 s
 
 // Where a bounded wait gave up (upper bits of the status word).
 enum Where : uint32_t {
@@ -114,53 +114,6 @@ struct Layout {
 #define ACCFULL(b) (2 * NR + 2 * NB + (b))
 #define ACCEMPTY(b) (2 * NR + 2 * NB + 2 + (b))
 #define DRAIN() (2 * NR + 2 * NB + 4)
-
-__device__ __forceinline__ void record_timeout(uint32_t *status, uint32_t where) {
-  atomicOr(status, (uint32_t)WQ_ERR_DEVICE_TIMEOUT | (where << 8));
-}
-
-// Bounded wait on an mbarrier phase; gives up when another role aborted or the
-// budget ran out (then it aborts the CTA and records where).
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                         uint32_t *status, uint32_t where) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitBudget) {
-      *abort_flag = 1;
-      record_timeout(status, where);
-      return false;
-    }
-  }
-}
-
-// Warp-collective form: every lane polls (each gets the barrier's acquire) and
-// the warp takes one decision, so no lane leaves a loop its warp-mates stay in.
-__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                              uint32_t *status, uint32_t where) {
-  const bool ok = wait_bar(bar, parity, abort_flag, status, where);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// Wait used only while draining: ignores the abort flag, bounded budget.
-__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitBudget) return;
-  }
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -229,17 +182,6 @@ __device__ __forceinline__ void smem_so(uint32_t s_base, uint32_t o_base, bool h
     s2[j] = dup_half(sw[j >> 1], j & 1);
     o2[j] = dup_half(ow[j >> 1], j & 1);
   }
-}
-
-// Packed pair subtraction in the operand dtype (exact here: small integers).
-template <int DT>
-__device__ __forceinline__ uint32_t sub2(uint32_t v, uint32_t c) {
-  uint32_t r;
-  if (DT == WQ_BF16)
-    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(c));
-  else
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(c));
-  return r;
 }
 
 // Byte offset of the 16-byte chunk (row r, k-octet c) in a K-major 128-byte
