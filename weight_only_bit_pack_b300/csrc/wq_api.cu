@@ -251,8 +251,9 @@ int32_t make_plan(const Problem &p, int32_t kernel, Plan &plan) {
   if (chosen == WQ_KERNEL_DECODE) {
     if (!plan_decode(p, plan))
       return fail(WQ_ERR_UNSUPPORTED,
-                  "the decode kernel needs 1 <= m <= 16, INT4 weights, n %% 32 == 0, k %% 8 == 0 "
-                  "and 16-byte aligned x1, x2, scale and offset");
+                  "the decode kernel needs 1 <= m <= 16, INT4 weights, n %% 32 == 0, k %% 8 == 0, "
+                  "16-byte aligned x1, x2, scale and offset and 8-byte aligned bias, residual, "
+                  "gamma, y and normOut");
     return WQ_OK;
   }
   if (chosen == WQ_KERNEL_PREFILL) {

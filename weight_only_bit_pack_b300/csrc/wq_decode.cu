@@ -14,22 +14,26 @@
 // of one tile and the start of the next (or more), so each CTA produces one
 // partial sum per tile it touches (a "segment").
 //
-// Warp roles (4*KH consumer warps + 1 producer warp):
-//   producer   one elected lane streams the run through an NS-deep ring of
-//              stages: the 64 x 128-byte box of packed weights and the 64 x MP
-//              box of x1 (both 128-byte swizzled), plus the scale (and offset)
-//              rows of the groups the stage touches, all by TMA, completion on
-//              the stage's full mbarrier.
-//   consumers  warp w takes the 64 columns 64*(w%4) .. +63 and the stages j
-//              with j % KH == w / 4 (j counts the run's units). Per 16 k-rows it
-//              turns four 32-bit words of nibbles into the A fragments of four
-//              m16n8k16 MMAs (A = W^T, 16 columns x 16 k, exact integers q in
-//              bf16/fp16), loads B = x1^T (16 k x 8 rows) with ldmatrix and
-//              accumulates fp32. The scale is applied to each group's fp32 sum
-//              when the group ends (the offset to the group's x1 row sum, from
-//              the same MMA with an all-ones A), so the dequantized weight is
-//              exact and only fp32 accumulation rounds.
-// Segment end. The KH k-phases add in shared memory (fixed order) and the CTA
+// Warp roles (16 or 8 consumer warps + 2 producer warps):
+//   producers  the last two warps, one elected lane each, stream stages j = p, p+2, ... of
+//              the run through a ring as deep as shared memory allows: the 128 x 128-byte box of packed
+//              weights, two 64 x MP boxes of x1 (all 128-byte swizzled), and the
+//              scale (and offset) rows of the groups the stage touches, all by
+//              TMA, completion on the stage's full mbarrier.
+//   consumers  column group c (of four) takes 64 columns and k-phase h (four
+//              for M <= 8, two for M <= 16) the stages with j % KH == h. Per 16 k-rows
+//              a thread reads its CPW/8 columns of four k-rows with one vector
+//              load each and turns them into the A fragments of m16n8k16 MMAs
+//              (A = W^T: 16 columns x 16 k; B = x1^T, 16 k x 8 rows, by ldmatrix;
+//              fp32 accumulation). A holds the exact integer q (an AND/XOR makes
+//              the 16-bit float 136 + q, or 1032 + q in fp16, and a packed
+//              subtraction leaves q). With an offset, A keeps 136 + q and one
+//              more MMA with an all-ones A gives the x1 row sums d of the same
+//              rows, which the offset needs anyway: the exact sum is acc - 136 d.
+//              When a group ends its sums are scaled in fp32: tot += S * acc
+//              (+ (O - 136 S) * d). The dequantized weight is never rounded;
+//              only fp32 accumulation rounds.
+// Segment end. The k-phases add in shared memory (a fixed tree) and the CTA
 // writes the segment's M x 256 fp32 partial to the workspace, then counts it on
 // the tile's counter. The CTA that brings the counter to the number of
 // segments of the tile finishes the tile: it sums the segments in CTA order,
@@ -64,10 +68,11 @@ namespace {
 using namespace sm100;
 
 constexpr int DNT = 256;                    // columns per n-tile
-constexpr int DKB = 64;                     // k-rows per stage
-constexpr uint32_t DW = DKB * DNT / 2;      // 8 KB of packed INT4 per stage
-constexpr uint32_t DSO = 2 * DNT * 2;       // 1 KB: the two group rows a stage can touch
-constexpr int NS = 8;                       // pipeline depth (stages)
+constexpr int DKB = 128;                    // k-rows per stage
+constexpr uint32_t DW = DKB * DNT / 2;      // 16 KB of packed INT4 per stage
+constexpr int kMaxSoRows = 4;               // group rows a 128-row stage can touch (group >= 32)
+constexpr int kMaxStages = 16;              // ring depth bound (barrier storage)
+constexpr int kProducers = 2;               // producer warps (alternate stages)
 constexpr int kTileCounters = 256;          // N <= 65535 gives at most 256 tiles
 constexpr uint32_t kGbarOff = 128;          // header: grid counters (arrive, depart)
 constexpr uint32_t kTcntOff = 1024;         // header: per-tile segment counters
@@ -75,22 +80,43 @@ constexpr uint32_t kTcntOff = 1024;         // header: per-tile segment counters
 template <int MT>
 struct DCfg {
   static constexpr int MP = 8 * MT;                // rows held (x1 box height)
-  static constexpr int KH = MT == 1 ? 4 : 2;       // k-phases
-  static constexpr int CW = 4 * KH;                // consumer warps
+  static constexpr int CPW = 64;                   // columns per consumer warp
+  static constexpr int NCG = DNT / CPW;            // column groups
+  static constexpr int CW = 8;                     // consumer warps
+  static constexpr int KH = CW / NCG;              // k-phases
   static constexpr int CT = CW * 32;               // consumer threads
-  static constexpr int THREADS = CT + 32;          // + producer warp
-  static constexpr uint32_t XB = MP * 128;         // x1 box bytes per stage
-  static constexpr uint32_t OFF_X = DW;            // slot: W | X | S | O
-  static constexpr uint32_t OFF_S = DW + (XB + 1023) / 1024 * 1024;
-  static constexpr uint32_t OFF_O = OFF_S + DSO;
-  static constexpr uint32_t SLOT = OFF_O + DSO;    // a multiple of 1024
-  static constexpr uint32_t OFF_RED = NS * SLOT;   // KH x MP x 256 fp32
-  static constexpr uint32_t OFF_MISC = OFF_RED + KH * MP * DNT * 4;
-  static constexpr uint32_t OFF_BAR = OFF_MISC + 2048;  // misc: 1/RMS, per-warp row sums, flags
-  static_assert((16 + CW * 16 + 2) * 4 <= 2048, "misc area");
-  static constexpr uint32_t SMEM = OFF_BAR + 8 * 2 * NS + 1024;  // + base alignment slack
-  static_assert(SLOT % 1024 == 0, "stage slots keep the 128-byte swizzle atoms aligned");
+  static constexpr int THREADS = CT + 32 * kProducers;
+  static constexpr uint32_t XB = MP * 128;         // one 64-k x1 box
+  static_assert(KH * NCG == CW && KH == 2, "warp split");
 };
+
+// Shared-memory layout of one call (the ring depth follows from the slot size).
+struct DLayout {
+  uint32_t slot, off_x, off_s, off_o, off_red, off_misc, off_bar, smem;
+  int NS;
+};
+
+inline DLayout decode_layout(int MT, int so_rows, bool has_o, uint32_t budget) {
+  DLayout L;
+  const uint32_t MP = 8u * MT, XB = MP * 128u;
+  L.off_x = DW;                              // slot: W | two x1 boxes | S rows | O rows
+  L.off_s = DW + 2 * XB;
+  L.off_o = L.off_s + (uint32_t)so_rows * DNT * 2u;
+  const uint32_t end = L.off_o + (has_o ? (uint32_t)so_rows * DNT * 2u : 0u);
+  L.slot = (end + 1023u) / 1024u * 1024u;    // keeps the 128-byte swizzle atoms aligned
+  const uint32_t fixed = 2u * MP * DNT * 4u  // k-phase reduction buffer
+                         + 2048u             // misc: 1/RMS, per-warp row sums, flags
+                         + 8u * 2u * kMaxStages + 1024u;  // barriers, base alignment slack
+  int ns = (int)((budget - fixed) / L.slot);
+  ns -= ns % kProducers;
+  if (ns > kMaxStages) ns = kMaxStages;
+  L.NS = ns;
+  L.off_red = (uint32_t)ns * L.slot;
+  L.off_misc = L.off_red + 2u * MP * DNT * 4u;
+  L.off_bar = L.off_misc + 2048u;
+  L.smem = L.off_bar + 8u * 2u * kMaxStages + 1024u;
+  return L;
+}
 
 enum DWhere : uint32_t { kDWhereProducer = 11, kDWhereConsumer = 12, kDWhereGrid = 15 };
 
@@ -103,15 +129,16 @@ struct DecodeArgs {
   float *part;        // G x SMAX x MP x 256 segment partials
   float *y32;         // nTiles x MP x 256 fp32 y
   float *ss;          // nTiles x 16 per-row sums of y^2
-  int M, K, N, group, Ns;
+  int M, K, N, group, Ns, so_rows;
   int nTiles, kst, U, per, G, SMAX, npf;
   float eps;
+  int NS;                                      // ring depth
+  uint32_t slot, off_x, off_s, off_o, off_red, off_misc, off_bar;  // shared-memory layout
 };
 
-// Four nibble pairs -> two A-fragment registers of exact integers q: `lo` holds
-// the low nibbles of byte i of wa (k) and wb (k+1), `hi` the high nibbles.
-// (nib ^ 8) | magic is the 16-bit float 128 + q + 8 (bf16) or 1024 + q + 8
-// (fp16); subtracting 136 / 1032 leaves q exactly.
+// Byte i of wa (k-row k) and of wb (k-row k+1) -> two A-fragment registers:
+// `lo` pairs their low nibbles, `hi` their high nibbles, each as 136 + q (bf16)
+// or 1032 + q (fp16): (nib ^ 8) | magic is exactly that 16-bit float.
 template <int DT>
 __device__ __forceinline__ void nib_pairs(uint32_t wa, uint32_t wb, int i, uint32_t &lo,
                                           uint32_t &hi) {
@@ -119,8 +146,28 @@ __device__ __forceinline__ void nib_pairs(uint32_t wa, uint32_t wb, int i, uint3
   const uint32_t sel = (uint32_t)i | ((uint32_t)i << 4) | ((uint32_t)(4 + i) << 8) |
                        ((uint32_t)(4 + i) << 12);
   const uint32_t x = __byte_perm(wa, wb, sel);
-  lo = sub2<DT>((x & 0x000F000Fu) ^ MAGIC, MAGIC);
-  hi = sub2<DT>(((x >> 4) & 0x000F000Fu) ^ MAGIC, MAGIC);
+  lo = (x & 0x000F000Fu) ^ MAGIC;
+  hi = ((x >> 4) & 0x000F000Fu) ^ MAGIC;
+}
+
+// Same pairs as exact integers q (the 136 / 1032 subtracted in the operand dtype).
+template <int DT>
+__device__ __forceinline__ void nib_pairs_q(uint32_t wa, uint32_t wb, int i, uint32_t &lo,
+                                            uint32_t &hi) {
+  constexpr uint32_t MAGIC = DT == WQ_BF16 ? 0x43084308u : 0x64086408u;
+  nib_pairs<DT>(wa, wb, i, lo, hi);
+  lo = sub2<DT>(lo, MAGIC);
+  hi = sub2<DT>(hi, MAGIC);
+}
+
+template <int NW>
+__device__ __forceinline__ void ldsw(uint32_t addr, uint32_t (&w)[NW]) {
+  if constexpr (NW == 4)
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
+  else if constexpr (NW == 2)
+    asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "r"(addr));
+  else
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[0]) : "r"(addr));
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
@@ -151,16 +198,18 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
   using C = DCfg<MT>;
   using E = Elem<DT>;
   using T = typename E::T;
-  constexpr int MP = C::MP, KH = C::KH, CT = C::CT;
+  constexpr int MP = C::MP, KH = C::KH, CT = C::CT, CPW = C::CPW;
+  constexpr int NB = DKB / 16;  // 16-k blocks per stage
   constexpr bool BF = DT == WQ_BF16;
   extern __shared__ uint8_t dsm_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(smem);
-  auto FULL = [&](int s) { return sb + C::OFF_BAR + 8u * s; };
-  auto EMPTY = [&](int s) { return sb + C::OFF_BAR + 8u * (NS + s); };
-  float *red = reinterpret_cast<float *>(smem + C::OFF_RED);
-  float *misc = reinterpret_cast<float *>(smem + C::OFF_MISC);
+  const int NS = a.NS;
+  auto FULL = [&](int s) { return sb + a.off_bar + 8u * s; };
+  auto EMPTY = [&](int s) { return sb + a.off_bar + 8u * (kMaxStages + s); };
+  float *red = reinterpret_cast<float *>(smem + a.off_red);
+  float *misc = reinterpret_cast<float *>(smem + a.off_misc);
   float *s_rstd = misc;                                              // [16]
   float *s_ssw = misc + 16;                                          // [CW][16]
   volatile int *abort_flag = reinterpret_cast<volatile int *>(misc + 16 + C::CW * 16);
@@ -174,7 +223,7 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(FULL(s), 1);
-      mbar_init(EMPTY(s), 4);  // the four column warps of the stage's k-phase
+      mbar_init(EMPTY(s), C::NCG);  // the column-group warps of the stage's k-phase
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -187,44 +236,55 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
   }
   if (warp == C::CW && lane == 0) {
     const int npf = u1 - u0 < a.npf ? u1 - u0 : a.npf;
+    int tile = u0 / a.kst, st = u0 - tile * a.kst;
     for (int j = 0; j < npf; ++j) {
-      const int u = u0 + j, tile = u / a.kst, st = u - tile * a.kst;
       tma_prefetch_l2_2d(&tm_w, tile * (DNT / 2), st * DKB);
+      if (++st == a.kst) { st = 0; ++tile; }
     }
   }
   __syncthreads();
   griddep_wait();  // the previous grid on the stream has finished and flushed
   griddep_launch_dependents();
 
-  if (warp == C::CW) {
-    // ---------------------------------------------------------------- producer
+  if (warp >= C::CW) {
+    // ---------------------------------------------------------------- producers
+    const int p = warp - C::CW;
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();  // each weight byte is used once per call
-      const uint32_t so_bytes = a.Ns != 1 ? (a.group ? 2u : 1u) * DNT * 2u : 0u;
-      const uint32_t bytes = DW + C::XB + (HAS_O ? 2u : 1u) * so_bytes;
-      int slot = 0;
+      const uint32_t so_bytes = a.Ns != 1 ? (uint32_t)a.so_rows * DNT * 2u : 0u;
+      const uint32_t bytes = DW + 2u * C::XB + (HAS_O ? 2u : 1u) * so_bytes;
+      int slot = p;
       uint32_t ph = 0;
       int issued = 0;
-      for (int u = u0; u < u1; ++u) {
+      int tile = (u0 + p) / a.kst, st = (u0 + p) - tile * a.kst;
+      for (int u = u0 + p; u < u1; u += kProducers) {
         if (!wait_bar(EMPTY(slot), ph ^ 1u, abort_flag, a.status, kDWhereProducer)) break;
-        const int tile = u / a.kst, st = u - tile * a.kst;
         const int row0 = st * DKB;
-        const uint32_t dst = sb + (uint32_t)slot * C::SLOT;
+        const uint32_t dst = sb + (uint32_t)slot * a.slot;
         mbar_arrive_expect_tx(FULL(slot), bytes);
         tma_load_2d_hint(dst, &tm_w, tile * (DNT / 2), row0, FULL(slot), pol);
-        tma_load_2d(dst + C::OFF_X, &tm_x, row0, 0, FULL(slot));
+        tma_load_2d(dst + a.off_x, &tm_x, row0, 0, FULL(slot));
+        tma_load_2d(dst + a.off_x + C::XB, &tm_x, row0 + 64, 0, FULL(slot));
         if (a.Ns != 1) {
           // the scale (and offset) rows of the groups this stage touches
           const int g0 = a.group ? row0 / a.group : 0;
-          tma_load_2d(dst + C::OFF_S, &tm_s, tile * DNT, g0, FULL(slot));
-          if (HAS_O) tma_load_2d(dst + C::OFF_O, &tm_o, tile * DNT, g0, FULL(slot));
+          tma_load_2d(dst + a.off_s, &tm_s, tile * DNT, g0, FULL(slot));
+          if (HAS_O) tma_load_2d(dst + a.off_o, &tm_o, tile * DNT, g0, FULL(slot));
         }
         ++issued;
-        if (++slot == NS) { slot = 0; ph ^= 1u; }
+        slot += kProducers;
+        if (slot >= NS) { slot -= NS; ph ^= 1u; }
+        st += kProducers;
+        while (st >= a.kst) { st -= a.kst; ++tile; }
       }
       // every copy issued has landed before the CTA may exit
-      for (int j = (issued > NS ? issued - NS : 0); j < issued; ++j)
-        drain_bar(FULL(j % NS), (uint32_t)((j / NS) & 1));
+      int dslot = p;
+      uint32_t dph = 0;
+      for (int q = 0; q < issued; ++q) {
+        if (q + NS / kProducers >= issued) drain_bar(FULL(dslot), dph);
+        dslot += kProducers;
+        if (dslot >= NS) { dslot -= NS; dph ^= 1u; }
+      }
     }
     __syncwarp();
     return;
@@ -232,15 +292,20 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
 
   // ------------------------------------------------------------------ consumers
   const int ctid = threadIdx.x;
-  const int wc = warp & 3, kh = warp >> 2;
+  const int cg = warp % C::NCG, kh = warp / C::NCG;  // column group, k-phase
   const int g = lane >> 2, t = lane & 3;
-  const uint32_t ones = BF ? 0x3F803F80u : 0x3C003C00u;  // 1.0 in both halves
+  const uint32_t ones = BF ? 0x3F803F80u : 0x3C003C00u;      // 1.0 in both halves
+  const float bias136 = BF ? 136.f : 1032.f;                  // A = bias136 + q
   const T *bias = static_cast<const T *>(a.bias);
   const T *res = static_cast<const T *>(a.residual);
   const T *gam = static_cast<const T *>(a.gamma);
   T *yout = static_cast<T *>(a.y);
   T *nout = static_cast<T *>(a.normOut);
 
+  // this thread's 8 columns start at column c0 of the tile; their nibbles are the
+  // 4-byte word at byte woff of a 128-byte weight row, before the swizzle
+  const int c0 = cg * CPW + g * (CPW / 8);
+  const uint32_t woff = (uint32_t)(c0 / 2);
   // ldmatrix row of this lane in an x1 box (rows m at 128-byte pitch, swizzled)
   int ldm_m, ldm_c;
   {
@@ -254,6 +319,9 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
     sscal = E::to_f(static_cast<const T *>(a.scale)[0]);
     if (HAS_O) oscal = E::to_f(static_cast<const T *>(a.offset)[0]);
   }
+  // a stage whose rows lie in one group can be copied to registers and handed
+  // back to the producer before any arithmetic
+  const bool early = a.so_rows == 1;
 
   const int t0c = u0 / a.kst;                   // first tile of this CTA's run
   const int t1c = u1 > u0 ? (u1 - 1) / a.kst : t0c - 1;
@@ -274,22 +342,37 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
         for (int c = 0; c < 4; ++c) tot[mt][i][c] = acc[mt][i][c] = 0.f;
       d1[mt][0] = d1[mt][1] = 0.f;
     }
-    float sf[8], of[8];
+    // scale / offset of this thread's 8 columns in scale row `row` of a stage copy
+    auto load_so = [&](uint32_t base, int row, float (&sf)[8], float (&of)[8]) {
+      if (a.Ns == 1) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) { sf[q] = sscal; of[q] = oscal; }
-    int cur = -1;
-    auto flush = [&]() {
+        for (int q = 0; q < 8; ++q) { sf[q] = sscal; of[q] = oscal; }
+      } else {
+        const uint32_t o = (uint32_t)(row * DNT + c0) * 2u;
+        lds8f<DT>(base + a.off_s + o, sf);
+        if constexpr (HAS_O) {
+          lds8f<DT>(base + a.off_o + o, of);
+        } else {
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
+          for (int q = 0; q < 8; ++q) of[q] = 0.f;
+        }
+      }
+    };
+    // fold the group's sums into tot: S * acc (+ (O - 136 S) * d when A holds
+    // 136 + q, which is the case with an offset; without one A holds q itself)
+    auto flush = [&](const float (&sf)[8], const float (&of)[8]) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float sl = sf[2 * i], sh = sf[2 * i + 1];
+      for (int i = 0; i < 4; ++i) {
+        const float sl = sf[2 * i], sh = sf[2 * i + 1];
+        const float cl = HAS_O ? fmaf(-bias136, sl, of[2 * i]) : 0.f;
+        const float ch = HAS_O ? fmaf(-bias136, sh, of[2 * i + 1]) : 0.f;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
           if constexpr (HAS_O) {
-            const float ol = of[2 * i], oh = of[2 * i + 1];
-            tot[mt][i][0] += fmaf(sl, acc[mt][i][0], ol * d1[mt][0]);
-            tot[mt][i][1] += fmaf(sl, acc[mt][i][1], ol * d1[mt][1]);
-            tot[mt][i][2] += fmaf(sh, acc[mt][i][2], oh * d1[mt][0]);
-            tot[mt][i][3] += fmaf(sh, acc[mt][i][3], oh * d1[mt][1]);
+            tot[mt][i][0] = fmaf(cl, d1[mt][0], fmaf(sl, acc[mt][i][0], tot[mt][i][0]));
+            tot[mt][i][1] = fmaf(cl, d1[mt][1], fmaf(sl, acc[mt][i][1], tot[mt][i][1]));
+            tot[mt][i][2] = fmaf(ch, d1[mt][0], fmaf(sh, acc[mt][i][2], tot[mt][i][2]));
+            tot[mt][i][3] = fmaf(ch, d1[mt][1], fmaf(sh, acc[mt][i][3], tot[mt][i][3]));
           } else {
             tot[mt][i][0] = fmaf(sl, acc[mt][i][0], tot[mt][i][0]);
             tot[mt][i][1] = fmaf(sl, acc[mt][i][1], tot[mt][i][1]);
@@ -299,89 +382,101 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) acc[mt][i][c] = 0.f;
         }
-        d1[mt][0] = d1[mt][1] = 0.f;
       }
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) d1[mt][0] = d1[mt][1] = 0.f;
     };
 
     for (int st = sbeg; st < send; ++st) {
       if ((j & (KH - 1)) == kh) {
         const bool ok = wait_bar_warp(FULL(slot), ph, abort_flag, a.status, kDWhereConsumer);
+        bool released = false;
         if (ok) {
-          const uint32_t base = sb + (uint32_t)slot * C::SLOT;
+          const uint32_t base = sb + (uint32_t)slot * a.slot;
           const int srow = st * DKB;
-          const int gs = a.group ? srow / a.group : 0;  // group of the stage's first row
-          const int gnext = a.group ? (gs + 1) * a.group : 0x7fffffff;
+          // the stage's operands of this warp: nibbles of k-rows 16kb + 2t + {0, 1, 8, 9}
+          // (through the swizzle) and B = x1^T (box kb/4; row m at m*128, chunk c at
+          // c ^ (m & 7)), all loaded before any arithmetic
+          uint32_t w[NB][4], b[NB][MT][2];
 #pragma unroll
-          for (int kb = 0; kb < DKB / 16; ++kb) {
-            const int row0 = srow + 16 * kb;
-            // a 64-row stage crosses at most one group boundary per 32 rows
-            const int grp = row0 >= gnext ? row0 / a.group : gs;
-            if (grp != cur) {
-              if (cur >= 0) flush();
-              cur = grp;
-              if (a.Ns != 1) {
-                const uint32_t so = base + C::OFF_S + (uint32_t)((grp - gs) * DNT + 64 * wc + 8 * g) * 2u;
-                lds8f<DT>(so, sf);
-                if constexpr (HAS_O) lds8f<DT>(so + DSO, of);
-              }
-            }
-            // four words of nibbles: stage rows 16kb + 2t + {0, 1, 8, 9}, bytes
-            // 4g..4g+3 of this warp's 32-byte column span, through the swizzle
-            uint32_t w[4];
+          for (int kb = 0; kb < NB; ++kb) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int rl = 16 * kb + 2 * t + (q & 1) + 8 * (q >> 1);
-              const uint32_t chunk = (uint32_t)((2 * wc + (g >> 2)) ^ (rl & 7));
-              w[q] = lds32(base + (uint32_t)rl * 128u + (chunk << 4) + (uint32_t)((g & 3) << 2));
+              const uint32_t phys = (((woff >> 4) ^ (uint32_t)(rl & 7)) << 4) | (woff & 15u);
+              w[kb][q] = lds32(base + (uint32_t)rl * 128u + phys);
             }
-            // B = x1^T for these 16 k (x1 box: row m at m*128, 16-byte chunk c at c ^ (m & 7))
-            uint32_t b[MT][2];
-            {
-              const int cidx = 2 * kb + ldm_c;
-              const uint32_t baddr =
-                  base + C::OFF_X + (uint32_t)ldm_m * 128u + ((uint32_t)(cidx ^ (ldm_m & 7)) << 4);
-              if constexpr (MT == 2)
-                ldmatrix_x4(baddr, b[0][0], b[0][1], b[1][0], b[1][1]);
-              else
-                ldmatrix_x2(baddr, b[0][0], b[0][1]);
+            const int cidx = 2 * (kb & 3) + ldm_c;
+            const uint32_t baddr = base + a.off_x + (uint32_t)(kb >> 2) * C::XB +
+                                   (uint32_t)ldm_m * 128u + ((uint32_t)(cidx ^ (ldm_m & 7)) << 4);
+            if constexpr (MT == 2)
+              ldmatrix_x4(baddr, b[kb][0][0], b[kb][0][1], b[kb][1][0], b[kb][1][1]);
+            else
+              ldmatrix_x2(baddr, b[kb][0][0], b[kb][0][1]);
+          }
+          float sf[8], of[8];
+          load_so(base, 0, sf, of);
+          if (early) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(EMPTY(slot));  // the arrive orders the loads before it
+            released = true;
+          }
+          const int gs = a.group ? srow / a.group : 0;  // group of the stage's first row
+          int cur = gs;
+          int gend = (!early && a.group) ? (gs + 1) * a.group : 0x7fffffff;
+#pragma unroll
+          for (int kb = 0; kb < NB; ++kb) {
+            const int row0 = srow + 16 * kb;
+            if (row0 >= gend) {  // group boundary inside a stage that is still held
+              if (cur - gs < a.so_rows) flush(sf, of);
+              ++cur;
+              gend += a.group;
+              if (cur - gs < a.so_rows) load_so(base, cur - gs, sf, of);
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               uint32_t a0, a1, a2, a3;
-              nib_pairs<DT>(w[0], w[1], i, a0, a1);
-              nib_pairs<DT>(w[2], w[3], i, a2, a3);
+              if constexpr (HAS_O) {
+                nib_pairs<DT>(w[kb][0], w[kb][1], i, a0, a1);
+                nib_pairs<DT>(w[kb][2], w[kb][3], i, a2, a3);
+              } else {
+                nib_pairs_q<DT>(w[kb][0], w[kb][1], i, a0, a1);
+                nib_pairs_q<DT>(w[kb][2], w[kb][3], i, a2, a3);
+              }
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt)
-                mma_16816<BF>(acc[mt][i], a0, a1, a2, a3, b[mt][0], b[mt][1]);
+                mma_16816<BF>(acc[mt][i], a0, a1, a2, a3, b[kb][mt][0], b[kb][mt][1]);
             }
             if constexpr (HAS_O) {
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt) {
                 float dd[4] = {d1[mt][0], d1[mt][1], d1[mt][0], d1[mt][1]};
-                mma_16816<BF>(dd, ones, ones, ones, ones, b[mt][0], b[mt][1]);
+                mma_16816<BF>(dd, ones, ones, ones, ones, b[kb][mt][0], b[kb][mt][1]);
                 d1[mt][0] = dd[0];
                 d1[mt][1] = dd[1];
               }
             }
           }
+          // a group past the copied scale rows lies wholly beyond K: its sums are zero
+          if (cur - gs < a.so_rows) flush(sf, of);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(EMPTY(slot));
+        if (!released && lane == 0) mbar_arrive(EMPTY(slot));
       }
       ++j;
       if (++slot == NS) { slot = 0; ph ^= 1u; }
     }
-    if (cur >= 0) flush();
 
-    // ---- segment end: k-phases add in shared memory, the partial goes to the workspace
+    // ---- segment end: the k-phases add in shared memory, the partial goes out
+    auto red_idx = [&](int mt, int i, int c) {
+      return (8 * mt + 2 * t + (c & 1)) * DNT + c0 + 2 * i + (c >> 1);
+    };
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          red[(kh * MP + 8 * mt + 2 * t + (c & 1)) * DNT + 64 * wc + 8 * g + 2 * i + (c >> 1)] =
-              tot[mt][i][c];
+        for (int c = 0; c < 4; ++c) red[kh * MP * DNT + red_idx(mt, i, c)] = tot[mt][i][c];
     named_bar_sync(1, CT);
     float4 *dstp = reinterpret_cast<float4 *>(
         a.part + ((int64_t)cta * a.SMAX + (tile - t0c)) * (MP * DNT));
@@ -394,15 +489,14 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
       }
       __stcg(dstp + q, v);
     }
-    __threadfence();
+    // the CTA barrier orders every thread's partial stores before thread 0's
+    // release; the finisher's acquire then orders them before its loads
     named_bar_sync(1, CT);
     if (ctid == 0) {
       const int c_first = (tile * a.kst) / a.per;
       const int c_last = ((tile + 1) * a.kst - 1) / a.per;
-      const uint32_t old = atomicAdd(a.tcnt + tile, 1u);
-      const int last = old == (uint32_t)(c_last - c_first);
-      if (last) __threadfence();
-      *s_fin = last;
+      const uint32_t old = atom_add_acq_rel(a.tcnt + tile, 1u);
+      *s_fin = old == (uint32_t)(c_last - c_first);
     }
     named_bar_sync(1, CT);
     const bool finisher = *s_fin != 0;
@@ -412,22 +506,47 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
       const int c_last = ((tile + 1) * a.kst - 1) / a.per;
       for (int q = ctid; q < C::CW * 16; q += CT) s_ssw[q] = 0.f;
       named_bar_sync(1, CT);
-      for (int idx = ctid; idx < MP * DNT; idx += CT) {
-        const int m = idx / DNT, col = idx - m * DNT;  // a warp shares one row m
+      // float4 q covers columns 4q' .. 4q'+3 of row m = q / 64; a warp shares one row
+      const int nseg = c_last - c_first + 1;
+      for (int q = ctid; q < MP * DNT / 4; q += CT) {
+        const int m = q / (DNT / 4), col = 4 * (q - m * (DNT / 4));
         const int n = tile * DNT + col;
-        float v = 0.f;
-#pragma unroll 4
-        for (int cc = c_first; cc <= c_last; ++cc) {
-          const int seg = tile - (cc * a.per) / a.kst;
-          v += __ldcg(a.part + ((int64_t)cc * a.SMAX + seg) * (MP * DNT) + idx);
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int e0 = 0; e0 < nseg; e0 += 8) {
+          // eight segment loads in flight, then added in CTA order
+          float4 pv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int cc = c_first + e0 + e;
+            pv[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e0 + e < nseg) {
+              const int seg = tile - (cc * a.per) / a.kst;
+              pv[e] = __ldcg(reinterpret_cast<const float4 *>(
+                                 a.part + ((int64_t)cc * a.SMAX + seg) * (MP * DNT)) + q);
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            v.x += pv[e].x; v.y += pv[e].y; v.z += pv[e].z; v.w += pv[e].w;
+          }
         }
-        float yv = 0.f;
-        if (m < a.M && n < a.N) {
-          yv = v + (bias ? E::to_f(bias[n]) : 0.f) + E::to_f(res[(int64_t)m * a.N + n]);
-          yout[(int64_t)m * a.N + n] = E::from_f(yv);
+        float yv[4] = {0.f, 0.f, 0.f, 0.f};
+        if (m < a.M && n < a.N) {  // N % 32 == 0: all four columns or none
+          const uint2 rr = *reinterpret_cast<const uint2 *>(res + (int64_t)m * a.N + n);
+          uint2 bb = make_uint2(0u, 0u);
+          if (bias) bb = *reinterpret_cast<const uint2 *>(bias + n);
+          const float2 r01 = unpack2<DT>(rr.x), r23 = unpack2<DT>(rr.y);
+          const float2 b01 = unpack2<DT>(bb.x), b23 = unpack2<DT>(bb.y);
+          yv[0] = v.x + b01.x + r01.x;
+          yv[1] = v.y + b01.y + r01.y;
+          yv[2] = v.z + b23.x + r23.x;
+          yv[3] = v.w + b23.y + r23.y;
+          *reinterpret_cast<uint2 *>(yout + (int64_t)m * a.N + n) =
+              make_uint2(pack2<DT>(yv[0], yv[1]), pack2<DT>(yv[2], yv[3]));
         }
-        __stcg(a.y32 + (int64_t)tile * (MP * DNT) + idx, yv);
-        float sq = yv * yv;
+        __stcg(reinterpret_cast<float4 *>(a.y32 + (int64_t)tile * (MP * DNT)) + q,
+               make_float4(yv[0], yv[1], yv[2], yv[3]));
+        float sq = yv[0] * yv[0] + yv[1] * yv[1] + yv[2] * yv[2] + yv[3] * yv[3];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
         if (lane == 0) s_ssw[warp * 16 + m] += sq;
@@ -441,7 +560,6 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
       if (ctid == 0) a.tcnt[tile] = 0u;  // the last user of this counter in this call
       if (nfin < 4) fin_tiles[nfin] = tile;
       ++nfin;
-      __threadfence();
     }
   }
 
@@ -477,12 +595,18 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
   }
   for (int f = 0; f < nfin && f < 4; ++f) {
     const int tile = fin_tiles[f];
-    for (int idx = ctid; idx < MP * DNT; idx += CT) {
-      const int m = idx / DNT, col = idx - m * DNT;
+    for (int q = ctid; q < MP * DNT / 4; q += CT) {
+      const int m = q / (DNT / 4), col = 4 * (q - m * (DNT / 4));
       const int n = tile * DNT + col;
-      if (m < a.M && n < a.N)
-        nout[(int64_t)m * a.N + n] =
-            E::from_f(__ldcg(a.y32 + (int64_t)tile * (MP * DNT) + idx) * s_rstd[m] * E::to_f(gam[n]));
+      if (m < a.M && n < a.N) {
+        const float4 yv = __ldcg(reinterpret_cast<const float4 *>(a.y32 + (int64_t)tile * (MP * DNT)) + q);
+        const uint2 gg = *reinterpret_cast<const uint2 *>(gam + n);
+        const float2 g01 = unpack2<DT>(gg.x), g23 = unpack2<DT>(gg.y);
+        const float rs = s_rstd[m];
+        *reinterpret_cast<uint2 *>(nout + (int64_t)m * a.N + n) =
+            make_uint2(pack2<DT>(yv.x * rs * g01.x, yv.y * rs * g01.y),
+                       pack2<DT>(yv.z * rs * g23.x, yv.w * rs * g23.y));
+      }
     }
   }
 }
@@ -518,6 +642,20 @@ struct DecodeGeom {
 
 uint64_t dalign256(uint64_t v) { return (v + 255) / 256 * 256; }
 
+// Scale rows one stage's TMA copies: the most group rows any 128-row stage
+// touches (1 for per-channel scales).
+int decode_so_rows(const Problem &p) {
+  if (p.smode != kPerGroup) return 1;
+  const int64_t kst = (p.K + DKB - 1) / DKB;
+  int64_t most = 1;
+  for (int64_t s = 0; s < kst; ++s) {
+    const int64_t r0 = s * DKB, r1 = (s + 1) * DKB < p.K ? (s + 1) * DKB : p.K;
+    const int64_t n = (r1 - 1) / p.group - r0 / p.group + 1;
+    if (n > most) most = n;
+  }
+  return (int)(most < p.G ? most : p.G);
+}
+
 DecodeGeom decode_geom(const Problem &p) {
   DecodeGeom gm;
   gm.MP = p.M <= 8 ? 8 : 16;
@@ -546,6 +684,15 @@ bool decode_applicable(const Problem &p) {
   const void *ptrs[] = {p.x1, p.x2, p.scale, p.offset};
   for (const void *q : ptrs)
     if (!daligned16(q)) return false;
+  // the epilogue moves four 16-bit values at a time
+  const void *vecs[] = {p.bias, p.residual, p.gamma, p.y, p.normOut};
+  for (const void *q : vecs)
+    if (reinterpret_cast<uintptr_t>(q) % 8 != 0) return false;
+  const int so_rows = decode_so_rows(p);
+  if (so_rows > kMaxSoRows) return false;
+  const uint32_t budget = device_info().smem_optin > 0 ? (uint32_t)device_info().smem_optin : 232448u;
+  if (decode_layout(p.M <= 8 ? 1 : 2, so_rows, p.offset != nullptr && p.Ns != 1, budget).NS < 4)
+    return false;
   const DecodeGeom gm = decode_geom(p);
   return gm.SMAX <= 4;  // a CTA finishes at most four tiles
 }
@@ -563,15 +710,20 @@ static cudaError_t launch_decode_t(const Problem &p, const Plan &plan, void *ws,
   using C = DCfg<MT>;
   EncodeTiledFn enc = dencode_fn();
   if (!enc) return cudaErrorNotSupported;
+  const uint32_t budget = (uint32_t)device_info().smem_optin;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
+  std::call_once(attr_once, [budget] {
+    // the cap is the device's opt-in maximum; each call asks for its own layout's size
     attr_err = cudaFuncSetAttribute(decode_kernel<DT, MT, HAS_O>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)budget);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const DecodeGeom gm = decode_geom(p);
   if (gm.G > device_info().sms) return cudaErrorInvalidConfiguration;
+  const int so_rows = decode_so_rows(p);
+  const DLayout L = decode_layout(MT, so_rows, HAS_O && p.Ns != 1, budget);
+  if (L.NS < 4 || L.smem > budget) return cudaErrorInvalidConfiguration;
 
   const CUtensorMapDataType fty =
       DT == WQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -590,7 +742,7 @@ static cudaError_t launch_decode_t(const Problem &p, const Plan &plan, void *ws,
   {
     const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.M};
     const cuuint64_t strides[1] = {(cuuint64_t)p.K * 2};
-    const cuuint32_t box[2] = {DKB, (cuuint32_t)C::MP};
+    const cuuint32_t box[2] = {64, (cuuint32_t)C::MP};  // 128-byte rows: two boxes per stage
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&tm_x, fty, 2, const_cast<void *>(p.x1), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -602,7 +754,7 @@ static cudaError_t launch_decode_t(const Problem &p, const Plan &plan, void *ws,
   if (p.Ns != 1) {
     const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.G};
     const cuuint64_t strides[1] = {(cuuint64_t)p.N * 2};
-    const cuuint32_t box[2] = {DNT, p.smode == kPerGroup ? 2u : 1u};
+    const cuuint32_t box[2] = {DNT, (cuuint32_t)so_rows};
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&tm_s, fty, 2, const_cast<void *>(p.scale), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -626,15 +778,19 @@ static cudaError_t launch_decode_t(const Problem &p, const Plan &plan, void *ws,
   args.ss = reinterpret_cast<float *>(wsb + gm.ss_off);
   args.M = (int)p.M; args.K = (int)p.K; args.N = (int)p.N;
   args.group = (int)p.group; args.Ns = (int)p.Ns;
+  args.so_rows = so_rows;
   args.nTiles = gm.nTiles; args.kst = gm.kst; args.U = gm.U; args.per = gm.per; args.G = gm.G;
   args.SMAX = gm.SMAX;
   args.npf = gm.per < 16 ? gm.per : 16;
   args.eps = p.eps;
+  args.NS = L.NS;
+  args.slot = L.slot; args.off_x = L.off_x; args.off_s = L.off_s; args.off_o = L.off_o;
+  args.off_red = L.off_red; args.off_misc = L.off_misc; args.off_bar = L.off_bar;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)gm.G, 1, 1);
   cfg.blockDim = dim3(C::THREADS, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.dynamicSmemBytes = L.smem;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
