@@ -21,14 +21,16 @@ __device__ __forceinline__ void record_timeout(uint32_t *status, uint32_t where)
 
 // Bounded wait on an mbarrier phase; gives up when another role aborted or the
 // budget ran out (then it aborts the CTA and records where).
-constexpr uint32_t kSleepNs = 1000000;  // longest suspension of one wait attempt (1 ms)
+// Longest suspension of one wait attempt while draining (1 ms). Waits on the
+// critical path poll instead: a suspended warp resumes too late.
+constexpr uint32_t kSleepNs = 1000000;
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                          uint32_t *status, uint32_t where) {
   if (sm100::mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (sm100::mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
+    if (sm100::mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > kWaitBudget) {
       *abort_flag = 1;
