@@ -81,12 +81,12 @@ struct PrefillArgs {
   const float *rowsum;       // RAWQ with offset: sum_k x1[m, k]
   const int8_t *e_row;       // F16EMU: row exponents
   const int8_t *e_col;       // F16EMU: column exponents
-  const __half *S16, *O16;   // F16EMU: scaled fp16 scale / offset (G x N)
+  const uint32_t *S16, *O16; // F16EMU: scaled fp16 scale / offset pairs (G x N words)
   long long M;
   int K, N, group, Ns, nTilesN, kTiles;
   long long nTiles;
   float eps;
-  uint32_t so_bytes;         // F16EMU: bytes of one scale/offset row box (rows x 256 x 2)
+  uint32_t so_bytes;         // F16EMU: bytes of one scale/offset row box (rows x 256 x 4)
 };
 
 template <int WBITS>
@@ -95,7 +95,7 @@ struct Layout {
   static constexpr uint32_t A_BYTES = BM * BK * 2;            // 16 KB
   static constexpr uint32_t BQ_BYTES = BK * BN * WBITS / 8;   // 8 or 16 KB
   static constexpr uint32_t B_BYTES = BN * BK * 2;            // 32 KB
-  static constexpr uint32_t SO_BYTES = SO_ROWS * BN * 2;      // 1.5 KB: fp16 rows of S16 / O16
+  static constexpr uint32_t SO_BYTES = SO_ROWS * BN * 4;      // 3 KB: rows of S16 / O16 pairs
   static constexpr uint32_t A_OFF = 0;
   static constexpr uint32_t BQ_OFF = A_OFF + NR * A_BYTES;
   static constexpr uint32_t B_OFF = BQ_OFF + NR * BQ_BYTES;
@@ -127,11 +127,6 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
   return v;
 }
 
-// (lo, hi) 16-bit halves of a packed pair, both set to the half `h` of w.
-__device__ __forceinline__ uint32_t dup_half(uint32_t w, int h) {
-  return __byte_perm(w, w, h ? 0x3232 : 0x1010);
-}
-
 // Packed pair arithmetic in the activation dtype: (v - c) * s + o, one rounding
 // for the subtraction (exact here: small integers) and one for the fma.
 template <int DT>
@@ -153,34 +148,25 @@ __device__ __forceinline__ uint32_t sub_fma2(uint32_t v, uint32_t c, uint32_t s,
   return r;
 }
 
-// Reads the fp16 S16/O16 values of CNT consecutive columns (starting at
-// column c of the tile) in group row `row` of the stage's scale/offset rows,
-// duplicated into packed pairs. Rows past the last group were zero-filled by
-// the copy (callers skip k-rows past K, whose rows may be stale).
+// Reads the S16/O16 pairs (both halves hold the value) of CNT consecutive
+// columns, starting at column c of the tile, in group row `row` of the stage's
+// scale/offset rows. Rows past the last group were zero-filled by the copy
+// (callers skip k-rows past K, whose rows may be stale).
 template <int CNT>
 __device__ __forceinline__ void smem_so(uint32_t s_base, uint32_t o_base, bool has_o, int row, int c,
                                         uint32_t (&s2)[CNT], uint32_t (&o2)[CNT]) {
-  const uint32_t off = (uint32_t)(row * BN + c) * 2u;
-  uint32_t sw[CNT / 2], ow[CNT / 2];
-  if constexpr (CNT == 8) {
+  const uint32_t off = (uint32_t)(row * BN + c) * 4u;
+#pragma unroll
+  for (int q = 0; q < CNT / 4; ++q) {
     asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(sw[0]), "=r"(sw[1]), "=r"(sw[2]), "=r"(sw[3]) : "r"(s_base + off));
+                 : "=r"(s2[4 * q]), "=r"(s2[4 * q + 1]), "=r"(s2[4 * q + 2]), "=r"(s2[4 * q + 3])
+                 : "r"(s_base + off + 16u * q));
     if (has_o)
       asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                   : "=r"(ow[0]), "=r"(ow[1]), "=r"(ow[2]), "=r"(ow[3]) : "r"(o_base + off));
+                   : "=r"(o2[4 * q]), "=r"(o2[4 * q + 1]), "=r"(o2[4 * q + 2]), "=r"(o2[4 * q + 3])
+                   : "r"(o_base + off + 16u * q));
     else
-      ow[0] = ow[1] = ow[2] = ow[3] = 0u;
-  } else {
-    asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(sw[0]), "=r"(sw[1]) : "r"(s_base + off));
-    if (has_o)
-      asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(ow[0]), "=r"(ow[1]) : "r"(o_base + off));
-    else
-      ow[0] = ow[1] = 0u;
-  }
-#pragma unroll
-  for (int j = 0; j < CNT; ++j) {
-    s2[j] = dup_half(sw[j >> 1], j & 1);
-    o2[j] = dup_half(ow[j >> 1], j & 1);
+      o2[4 * q] = o2[4 * q + 1] = o2[4 * q + 2] = o2[4 * q + 3] = 0u;
   }
 }
 
@@ -327,6 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // shared-memory bank conflicts.
     const int dw = warp - kDqWarp0;
     const int ko = (dw + lane) & 7;
+    // INT4: this thread's eight swizzled 16-byte stores of a B stage (row 8*lane + j, chunk ko)
+    uint32_t sto[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sto[j] = sw128_chunk(8 * lane + j, ko);
     // INT4: nibble r, u = r ^ 8 = q + 8, and (magic | u) is the 16-bit float
     // 128 + u (bf16) or 1024 + u (fp16); subtracting `magic` gives q exactly.
     const uint32_t magic4 = MDT == WQ_BF16 ? 0x43084308u : 0x64086408u;
@@ -359,8 +349,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int tt = 0; tt < 8; ++tt) wr[tt] = ld_shared_u32(bq + (8 * ko + tt) * 128 + 4 * lane);
           __syncwarp();
           if (lane == 0) mbar_arrive(BAR(RAWEMPTY(s)));
+          if constexpr (MODE != kF16Emu) {
 #pragma unroll
-          for (int tt = 0; tt < 8; ++tt) wsh[tt] = wr[tt] >> 4;
+            for (int tt = 0; tt < 8; ++tt) wsh[tt] = wr[tt] >> 4;
+          }
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint32_t b = (uint32_t)(j >> 1);
@@ -368,15 +360,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t c[4];
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
-              const uint32_t x = (j & 1) ? __byte_perm(wsh[2 * p], wsh[2 * p + 1], sel)
-                                         : __byte_perm(wr[2 * p], wr[2 * p + 1], sel);
-              const uint32_t v = (x & 0x000F000Fu) ^ magic4;
-              if constexpr (MODE == kF16Emu)
-                c[p] = sub_fma2<WQ_F16>(v, magic4, s2[j], o2[j]);
-              else
+              if constexpr (MODE == kF16Emu) {
+                // fp16 operands: an odd column's nibble is used in place at bits
+                // 7:4, as 1152 + 16 q; its S16 was stored divided by 16
+                const uint32_t x = __byte_perm(wr[2 * p], wr[2 * p + 1], sel);
+                const uint32_t mg = (j & 1) ? 0x64806480u : magic4;
+                const uint32_t v = (x & ((j & 1) ? 0x00F000F0u : 0x000F000Fu)) ^ mg;
+                c[p] = sub_fma2<WQ_F16>(v, mg, s2[j], o2[j]);
+              } else {
+                const uint32_t x = (j & 1) ? __byte_perm(wsh[2 * p], wsh[2 * p + 1], sel)
+                                           : __byte_perm(wr[2 * p], wr[2 * p + 1], sel);
+                const uint32_t v = (x & 0x000F000Fu) ^ magic4;
                 c[p] = sub2<MDT>(v, magic4);
+              }
             }
-            st_shared_v4(bst + sw128_chunk(8 * lane + j, ko), c[0], c[1], c[2], c[3]);
+            st_shared_v4(bst + sto[j], c[0], c[1], c[2], c[3]);
           }
         } else {
           uint32_t s2a[4], o2a[4], s2b[4], o2b[4];
@@ -706,10 +704,10 @@ bool plan_prefill(const Problem &p, Plan &plan) {
     plan.ecol_off = off;
     off += align256((uint64_t)p.N);
     plan.s16_off = off;
-    off += align256((uint64_t)p.G * p.N * 2);
+    off += align256((uint64_t)p.G * p.N * 4);
     if (p.offset) {
       plan.o16_off = off;
-      off += align256((uint64_t)p.G * p.N * 2);
+      off += align256((uint64_t)p.G * p.N * 4);
     }
     plan.x16_off = off;
     off += align256((uint64_t)p.M * p.K * 2);
@@ -761,8 +759,8 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
   } else {
     int8_t *e_row = reinterpret_cast<int8_t *>(wsb + plan.erow_off);
     int8_t *e_col = reinterpret_cast<int8_t *>(wsb + plan.ecol_off);
-    __half *S16 = reinterpret_cast<__half *>(wsb + plan.s16_off);
-    __half *O16 = p.offset ? reinterpret_cast<__half *>(wsb + plan.o16_off) : nullptr;
+    uint32_t *S16 = reinterpret_cast<uint32_t *>(wsb + plan.s16_off);
+    uint32_t *O16 = p.offset ? reinterpret_cast<uint32_t *>(wsb + plan.o16_off) : nullptr;
     __half *x16 = reinterpret_cast<__half *>(wsb + plan.x16_off);
     e = launch_row_prep(p, nullptr, e_row, x16, s);
     if (e != cudaSuccess) return e;
@@ -799,17 +797,17 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
   args.so_bytes = 0;
   if constexpr (MODE == kF16Emu) {
     const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.G};
-    const cuuint64_t strides[1] = {(cuuint64_t)p.N * 2};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.N * 4};
     const cuuint32_t rows = (cuuint32_t)(p.G < SO_ROWS ? p.G : SO_ROWS);
     const cuuint32_t box[2] = {BN, rows};
     const cuuint32_t estr[2] = {1, 1};
-    args.so_bytes = rows * BN * 2;
-    CUresult r = enc(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(args.S16), dims,
+    args.so_bytes = rows * BN * 4;
+    CUresult r = enc(&tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(args.S16), dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (p.offset) {
-      r = enc(&tm_o, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(args.O16), dims,
+      r = enc(&tm_o, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(args.O16), dims,
               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;

@@ -11,6 +11,10 @@
 //   qmax*|S16| + |O16| lies in [2^12, 2^13): then q*S16 is an exact fp16 value
 //   for every 4-bit q (an 8-bit bf16 significand times a 3-bit integer fits the
 //   11-bit fp16 significand), and only the offset add rounds, at 2^-12.
+//   Each value is stored twice, as the two halves of a 32-bit word (the form
+//   the packed fp16 arithmetic of the dequantization consumes). With `odd16`
+//   the scale of every odd column is stored divided by 16 (exact): the kernel
+//   reads those columns' nibbles in place at bits 7:4, i.e. as 16 q.
 // Both passes are deterministic (fixed reduction order).
 #include <cfloat>
 
@@ -87,11 +91,17 @@ __global__ void __launch_bounds__(256)
 // One block covers 32 columns; its 8 warps split the group rows, so every warp
 // load reads 32 consecutive columns (coalesced) and the G loads of a column
 // are spread over 8 warps.
+__device__ __forceinline__ uint32_t half_pair(float v) {
+  const __half h = __float2half_rn(v);
+  const uint32_t b = (uint32_t)__half_as_ushort(h);
+  return b | (b << 16);
+}
+
 template <int DT>
 __global__ void __launch_bounds__(256)
     so_prep_kernel(const typename Elem<DT>::T *__restrict__ S, const typename Elem<DT>::T *__restrict__ O,
-                   int G, int N, float qmax, int8_t *__restrict__ e_col, __half *__restrict__ S16,
-                   __half *__restrict__ O16) {
+                   int G, int N, float qmax, int odd16, int8_t *__restrict__ e_col,
+                   uint32_t *__restrict__ S16, uint32_t *__restrict__ O16) {
   using E = Elem<DT>;
   __shared__ float s_max[8][32];
   __shared__ float s_scale[32];
@@ -126,10 +136,11 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   if (n < N) {
     const float sc = s_scale[cx];
+    const float ssc = (odd16 && (n & 1)) ? sc * 0.0625f : sc;  // exact power-of-two factors
 #pragma unroll 4
     for (int g = gy; g < G; g += 8) {
-      S16[(int64_t)g * N + n] = __float2half_rn(E::to_f(S[(int64_t)g * N + n]) * sc);
-      if (O) O16[(int64_t)g * N + n] = __float2half_rn(E::to_f(O[(int64_t)g * N + n]) * sc);
+      S16[(int64_t)g * N + n] = half_pair(E::to_f(S[(int64_t)g * N + n]) * ssc);
+      if (O) O16[(int64_t)g * N + n] = half_pair(E::to_f(O[(int64_t)g * N + n]) * sc);
     }
   }
 }
@@ -152,19 +163,20 @@ cudaError_t launch_row_prep(const Problem &p, float *rowsum, int8_t *e_row, __ha
   return cudaGetLastError();
 }
 
-cudaError_t launch_so_prep(const Problem &p, int8_t *e_col, __half *S16, __half *O16,
+cudaError_t launch_so_prep(const Problem &p, int8_t *e_col, uint32_t *S16, uint32_t *O16,
                            cudaStream_t s) {
   const int N = (int)p.N;
   const int blocks = (N + 31) / 32;
   const float qmax = p.wbits == 4 ? 8.f : 128.f;
+  const int odd16 = p.wbits == 4 ? 1 : 0;
   if (p.dtype == WQ_BF16)
     so_prep_kernel<WQ_BF16><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(p.scale),
                                                    static_cast<const __nv_bfloat16 *>(p.offset),
-                                                   (int)p.G, N, qmax, e_col, S16, O16);
+                                                   (int)p.G, N, qmax, odd16, e_col, S16, O16);
   else
     so_prep_kernel<WQ_F16><<<blocks, 256, 0, s>>>(static_cast<const __half *>(p.scale),
                                                   static_cast<const __half *>(p.offset), (int)p.G,
-                                                  N, qmax, e_col, S16, O16);
+                                                  N, qmax, odd16, e_col, S16, O16);
   return cudaGetLastError();
 }
 
