@@ -439,7 +439,13 @@ def run_ours(args, world, rank, local):
     roof["alg_bytes_per_launch"] = ab["total"]
     roof["flops_per_launch"] = flops
 
-    kernels_per_call = {1: 2, 2: 2, 3: 1}.get(chosen, 2)
+    # our kernels per call: generic = matmul + epilogue; decode = one kernel;
+    # prefill = the tcgen05 kernel plus its row pre-pass (per-group scales, or
+    # an offset) and its scale pre-pass (per-group scales)
+    if chosen == 3:
+        kernels_per_call = 1 + (1 if (p.group or p.offset is not None) else 0) + (1 if p.group else 0)
+    else:
+        kernels_per_call = {1: 2, 2: 1}.get(chosen, 2)
     line = {
         "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
