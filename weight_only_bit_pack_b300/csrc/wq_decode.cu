@@ -37,8 +37,8 @@
 // writes the segment's M x 256 fp32 partial to the workspace, then counts it on
 // the tile's counter. The CTA that brings the counter to the number of
 // segments of the tile finishes the tile: it sums the segments in CTA order,
-// adds bias and residual, writes y (and an fp32 copy to the workspace) and the
-// tile's per-row sum of y^2, and clears the counter for the next call.
+// adds bias and residual, writes y (and y*gamma in fp32 to the workspace) and
+// the tile's per-row sum of y^2, and clears the counter for the next call.
 // RMSNorm. Every CTA then arrives at a grid-wide counter; once all have, each
 // sums the tiles' row sums in tile order, forms 1/RMS per row and writes normOut
 // for the tiles it finished. The last CTA to leave clears the counter. All
@@ -489,6 +489,23 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
       }
       __stcg(dstp + q, v);
     }
+    // Every CTA fetches the residual, bias and gamma of the positions it would
+    // finish now, so a finisher does not wait for them after the partial sums.
+    // Position qq of this thread is float4 q = ctid + CT*qq: columns 4q' .. 4q'+3
+    // of row m = q / 64 (N % 32 == 0: all four columns or none).
+    constexpr int QPT = MP * DNT / 4 / CT;
+    uint2 rres[QPT], rbia[QPT], rgam[QPT];
+#pragma unroll
+    for (int qq = 0; qq < QPT; ++qq) {
+      const int q = ctid + CT * qq;
+      const int m = q / (DNT / 4), n = tile * DNT + 4 * (q - m * (DNT / 4));
+      rres[qq] = rbia[qq] = rgam[qq] = make_uint2(0u, 0u);
+      if (m < a.M && n < a.N) {
+        rres[qq] = __ldg(reinterpret_cast<const uint2 *>(res + (int64_t)m * a.N + n));
+        if (bias) rbia[qq] = __ldg(reinterpret_cast<const uint2 *>(bias + n));
+        rgam[qq] = __ldg(reinterpret_cast<const uint2 *>(gam + n));
+      }
+    }
     // the CTA barrier orders every thread's partial stores before thread 0's
     // release; the finisher's acquire then orders them before its loads
     named_bar_sync(1, CT);
@@ -504,58 +521,64 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
       // ---- finish the tile: segments in CTA order + bias + residual -> y, sum(y^2)
       const int c_first = (tile * a.kst) / a.per;
       const int c_last = ((tile + 1) * a.kst - 1) / a.per;
-      for (int q = ctid; q < C::CW * 16; q += CT) s_ssw[q] = 0.f;
-      named_bar_sync(1, CT);
-      // float4 q covers columns 4q' .. 4q'+3 of row m = q / 64; a warp shares one row
       const int nseg = c_last - c_first + 1;
-      for (int q = ctid; q < MP * DNT / 4; q += CT) {
-        const int m = q / (DNT / 4), col = 4 * (q - m * (DNT / 4));
-        const int n = tile * DNT + col;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int e0 = 0; e0 < nseg; e0 += 8) {
-          // eight segment loads in flight, then added in CTA order
-          float4 pv[8];
+      for (int q = ctid; q < C::CW * 16; q += CT) s_ssw[q] = 0.f;
+      float4 v[QPT];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int cc = c_first + e0 + e;
-            pv[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (e0 + e < nseg) {
-              const int seg = tile - (cc * a.per) / a.kst;
-              pv[e] = __ldcg(reinterpret_cast<const float4 *>(
-                                 a.part + ((int64_t)cc * a.SMAX + seg) * (MP * DNT)) + q);
-            }
-          }
+      for (int qq = 0; qq < QPT; ++qq) v[qq] = make_float4(0.f, 0.f, 0.f, 0.f);
+      constexpr int EB = MT == 1 ? 8 : 4;  // segment loads per position in flight at once
+      for (int e0 = 0; e0 < nseg; e0 += EB) {
+        float4 pv[QPT][EB];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            v.x += pv[e].x; v.y += pv[e].y; v.z += pv[e].z; v.w += pv[e].w;
-          }
+        for (int e = 0; e < EB; ++e) {
+          const int cc = c_first + e0 + e;
+          const bool live = e0 + e < nseg;
+          const int seg = live ? tile - (cc * a.per) / a.kst : 0;
+          const float4 *src = reinterpret_cast<const float4 *>(
+              a.part + ((int64_t)(live ? cc : c_first) * a.SMAX + seg) * (MP * DNT));
+#pragma unroll
+          for (int qq = 0; qq < QPT; ++qq)
+            pv[qq][e] = live ? __ldcg(src + ctid + CT * qq) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        float yv[4] = {0.f, 0.f, 0.f, 0.f};
-        if (m < a.M && n < a.N) {  // N % 32 == 0: all four columns or none
-          const uint2 rr = *reinterpret_cast<const uint2 *>(res + (int64_t)m * a.N + n);
-          uint2 bb = make_uint2(0u, 0u);
-          if (bias) bb = *reinterpret_cast<const uint2 *>(bias + n);
-          const float2 r01 = unpack2<DT>(rr.x), r23 = unpack2<DT>(rr.y);
-          const float2 b01 = unpack2<DT>(bb.x), b23 = unpack2<DT>(bb.y);
-          yv[0] = v.x + b01.x + r01.x;
-          yv[1] = v.y + b01.y + r01.y;
-          yv[2] = v.z + b23.x + r23.x;
-          yv[3] = v.w + b23.y + r23.y;
+#pragma unroll
+        for (int qq = 0; qq < QPT; ++qq)
+#pragma unroll
+          for (int e = 0; e < EB; ++e) {  // added in CTA order
+            v[qq].x += pv[qq][e].x; v[qq].y += pv[qq][e].y;
+            v[qq].z += pv[qq][e].z; v[qq].w += pv[qq][e].w;
+          }
+      }
+      named_bar_sync(1, CT);  // s_ssw cleared
+#pragma unroll
+      for (int qq = 0; qq < QPT; ++qq) {
+        const int q = ctid + CT * qq;
+        const int m = q / (DNT / 4), n = tile * DNT + 4 * (q - m * (DNT / 4));
+        float yv[4] = {0.f, 0.f, 0.f, 0.f}, yg[4] = {0.f, 0.f, 0.f, 0.f};
+        if (m < a.M && n < a.N) {
+          const float2 r01 = unpack2<DT>(rres[qq].x), r23 = unpack2<DT>(rres[qq].y);
+          const float2 b01 = unpack2<DT>(rbia[qq].x), b23 = unpack2<DT>(rbia[qq].y);
+          const float2 g01 = unpack2<DT>(rgam[qq].x), g23 = unpack2<DT>(rgam[qq].y);
+          yv[0] = v[qq].x + b01.x + r01.x;
+          yv[1] = v[qq].y + b01.y + r01.y;
+          yv[2] = v[qq].z + b23.x + r23.x;
+          yv[3] = v[qq].w + b23.y + r23.y;
+          yg[0] = yv[0] * g01.x; yg[1] = yv[1] * g01.y; yg[2] = yv[2] * g23.x; yg[3] = yv[3] * g23.y;
           *reinterpret_cast<uint2 *>(yout + (int64_t)m * a.N + n) =
               make_uint2(pack2<DT>(yv[0], yv[1]), pack2<DT>(yv[2], yv[3]));
         }
+        // y * gamma in fp32: normOut needs only 1/RMS more
         __stcg(reinterpret_cast<float4 *>(a.y32 + (int64_t)tile * (MP * DNT)) + q,
-               make_float4(yv[0], yv[1], yv[2], yv[3]));
+               make_float4(yg[0], yg[1], yg[2], yg[3]));
         float sq = yv[0] * yv[0] + yv[1] * yv[1] + yv[2] * yv[2] + yv[3] * yv[3];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-        if (lane == 0) s_ssw[warp * 16 + m] += sq;
+        if (lane == 0) s_ssw[warp * 16 + m] += sq;  // a warp shares one row m
       }
       named_bar_sync(1, CT);
       if (ctid < MP) {
-        float v = 0.f;
-        for (int w = 0; w < C::CW; ++w) v += s_ssw[w * 16 + ctid];
-        __stcg(a.ss + tile * 16 + ctid, v);
+        float sv = 0.f;
+        for (int w = 0; w < C::CW; ++w) sv += s_ssw[w * 16 + ctid];
+        __stcg(a.ss + tile * 16 + ctid, sv);
       }
       if (ctid == 0) a.tcnt[tile] = 0u;  // the last user of this counter in this call
       if (nfin < 4) fin_tiles[nfin] = tile;
@@ -599,13 +622,10 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
       const int m = q / (DNT / 4), col = 4 * (q - m * (DNT / 4));
       const int n = tile * DNT + col;
       if (m < a.M && n < a.N) {
-        const float4 yv = __ldcg(reinterpret_cast<const float4 *>(a.y32 + (int64_t)tile * (MP * DNT)) + q);
-        const uint2 gg = *reinterpret_cast<const uint2 *>(gam + n);
-        const float2 g01 = unpack2<DT>(gg.x), g23 = unpack2<DT>(gg.y);
+        const float4 yg = __ldcg(reinterpret_cast<const float4 *>(a.y32 + (int64_t)tile * (MP * DNT)) + q);
         const float rs = s_rstd[m];
         *reinterpret_cast<uint2 *>(nout + (int64_t)m * a.N + n) =
-            make_uint2(pack2<DT>(yv.x * rs * g01.x, yv.y * rs * g01.y),
-                       pack2<DT>(yv.z * rs * g23.x, yv.w * rs * g23.y));
+            make_uint2(pack2<DT>(yg.x * rs, yg.y * rs), pack2<DT>(yg.z * rs, yg.w * rs));
       }
     }
   }
