@@ -8,31 +8,32 @@
 // built to keep HBM busy on every SM and to spend few instructions per weight.
 //
 // Work split (stream-K). Output columns come in n-tiles of 256 (128 bytes of
-// packed INT4 per k-row); K comes in 64-row stages. The nTiles x kst units
+// packed INT4 per k-row); K comes in 128-row stages. The nTiles x kst units
 // (tile, stage), in tile-major order, are cut into G equal contiguous runs of
 // `per` units, one per CTA, G <= SM count, one CTA per SM. A run covers the end
 // of one tile and the start of the next (or more), so each CTA produces one
 // partial sum per tile it touches (a "segment").
 //
-// Warp roles (16 or 8 consumer warps + 2 producer warps):
+// Warp roles (8 consumer warps + 2 producer warps):
 //   producers  the last two warps, one elected lane each, stream stages j = p, p+2, ... of
 //              the run through a ring as deep as shared memory allows: the 128 x 128-byte box of packed
 //              weights, two 64 x MP boxes of x1 (all 128-byte swizzled), and the
 //              scale (and offset) rows of the groups the stage touches, all by
 //              TMA, completion on the stage's full mbarrier.
-//   consumers  column group c (of four) takes 64 columns and k-phase h (four
-//              for M <= 8, two for M <= 16) the stages with j % KH == h. Per 16 k-rows
-//              a thread reads its CPW/8 columns of four k-rows with one vector
-//              load each and turns them into the A fragments of m16n8k16 MMAs
-//              (A = W^T: 16 columns x 16 k; B = x1^T, 16 k x 8 rows, by ldmatrix;
-//              fp32 accumulation). A holds the exact integer q (an AND/XOR makes
-//              the 16-bit float 136 + q, or 1032 + q in fp16, and a packed
-//              subtraction leaves q). With an offset, A keeps 136 + q and one
-//              more MMA with an all-ones A gives the x1 row sums d of the same
-//              rows, which the offset needs anyway: the exact sum is acc - 136 d.
-//              When a group ends its sums are scaled in fp32: tot += S * acc
-//              (+ (O - 136 S) * d). The dequantized weight is never rounded;
-//              only fp32 accumulation rounds.
+//   consumers  column group c (of four) takes 64 columns and k-phase h (of
+//              two) the stages with j % 2 == h; the ring depth is even, so a
+//              slot always serves the same producer and the same k-phase.
+//              Per stage a warp copies its operands to registers (the packed
+//              weights of its 64 columns by transposed ldmatrix, so one register
+//              pairs k-rows k, k+1 of four columns, and x1 by ldmatrix), hands
+//              the slot back when the stage lies in one group, and feeds
+//              m16n8k16 MMAs (A = W^T: 16 columns x 16 k; B = x1^T, 16 k x 8
+//              rows; fp32 accumulation). One AND/XOR (and a shift) turns a
+//              nibble pair into A's 16-bit floats 136 + q (1032 + q in fp16),
+//              exact; one more MMA with an all-ones A gives the x1 row sums d of
+//              the same rows, and when a group ends its sums are scaled in
+//              fp32: tot += S * acc + (O - 136 S) * d. The dequantized weight is
+//              never rounded; only fp32 accumulation rounds.
 // Segment end. The k-phases add in shared memory (a fixed tree) and the CTA
 // writes the segment's M x 256 fp32 partial to the workspace, then counts it on
 // the tile's counter. The CTA that brings the counter to the number of
@@ -76,6 +77,7 @@ constexpr int kProducers = 2;               // producer warps (alternate stages)
 constexpr int kTileCounters = 256;          // N <= 65535 gives at most 256 tiles
 constexpr uint32_t kGbarOff = 128;          // header: grid counters (arrive, depart)
 constexpr uint32_t kTcntOff = 1024;         // header: per-tile segment counters
+constexpr int kRingMultiple = 2;            // ring depth: a multiple of producers and k-phases
 
 template <int MT>
 struct DCfg {
@@ -88,6 +90,9 @@ struct DCfg {
   static constexpr int THREADS = CT + 32 * kProducers;
   static constexpr uint32_t XB = MP * 128;         // one 64-k x1 box
   static_assert(KH * NCG == CW && KH == 2, "warp split");
+  static_assert(kRingMultiple % KH == 0 && kRingMultiple % kProducers == 0,
+                "a ring slot keeps one producer and one k-phase");
+  static_assert((MP * DNT / 4) % 32 == 0 && CT % 32 == 0, "tile positions come in whole warps");
 };
 
 // Shared-memory layout of one call (the ring depth follows from the slot size).
@@ -108,7 +113,11 @@ inline DLayout decode_layout(int MT, int so_rows, bool has_o, uint32_t budget) {
                          + 2048u             // misc: 1/RMS, per-warp row sums, flags
                          + 8u * 2u * kMaxStages + 1024u;  // barriers, base alignment slack
   int ns = (int)((budget - fixed) / L.slot);
-  ns -= ns % kProducers;
+  // Each slot must belong to one producer and to one k-phase for good: stage j
+  // goes to slot j % NS, producer j % 2 and k-phase j % KH. A k-phase that
+  // waited on a slot last filled for another k-phase could run a whole phase
+  // ahead of it, and a parity wait cannot tell phase p from phase p + 2.
+  ns -= ns % kRingMultiple;
   if (ns > kMaxStages) ns = kMaxStages;
   L.NS = ns;
   L.off_red = (uint32_t)ns * L.slot;
@@ -136,58 +145,23 @@ struct DecodeArgs {
   uint32_t slot, off_x, off_s, off_o, off_red, off_misc, off_bar;  // shared-memory layout
 };
 
-// Byte i of wa (k-row k) and of wb (k-row k+1) -> two A-fragment registers:
-// `lo` pairs their low nibbles, `hi` their high nibbles, each as 136 + q (bf16)
-// or 1032 + q (fp16): (nib ^ 8) | magic is exactly that 16-bit float.
+// One A-fragment register from a transposed ldmatrix word r: r holds the 16-bit
+// group of four columns (nibble c = column 4e + c) of k-rows k (low half) and
+// k + 1 (high half); nibble c of both halves becomes the 16-bit float 136 + q
+// (bf16) or 1032 + q (fp16): (nib ^ 8) | magic is exactly that float.
 template <int DT>
-__device__ __forceinline__ void nib_pairs(uint32_t wa, uint32_t wb, int i, uint32_t &lo,
-                                          uint32_t &hi) {
+__device__ __forceinline__ uint32_t nib_col(uint32_t r, int c) {
   constexpr uint32_t MAGIC = DT == WQ_BF16 ? 0x43084308u : 0x64086408u;
-  const uint32_t sel = (uint32_t)i | ((uint32_t)i << 4) | ((uint32_t)(4 + i) << 8) |
-                       ((uint32_t)(4 + i) << 12);
-  const uint32_t x = __byte_perm(wa, wb, sel);
-  lo = (x & 0x000F000Fu) ^ MAGIC;
-  hi = ((x >> 4) & 0x000F000Fu) ^ MAGIC;
+  return ((c ? r >> (4 * c) : r) & 0x000F000Fu) ^ MAGIC;
 }
 
-// Same pairs as exact integers q (the 136 / 1032 subtracted in the operand dtype).
+// Four consecutive 16-bit values at addr -> f[0..3].
 template <int DT>
-__device__ __forceinline__ void nib_pairs_q(uint32_t wa, uint32_t wb, int i, uint32_t &lo,
-                                            uint32_t &hi) {
-  constexpr uint32_t MAGIC = DT == WQ_BF16 ? 0x43084308u : 0x64086408u;
-  nib_pairs<DT>(wa, wb, i, lo, hi);
-  lo = sub2<DT>(lo, MAGIC);
-  hi = sub2<DT>(hi, MAGIC);
-}
-
-template <int NW>
-__device__ __forceinline__ void ldsw(uint32_t addr, uint32_t (&w)[NW]) {
-  if constexpr (NW == 4)
-    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
-  else if constexpr (NW == 2)
-    asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "r"(addr));
-  else
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[0]) : "r"(addr));
-}
-
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-
-template <int DT>
-__device__ __forceinline__ void lds8f(uint32_t addr, float (&f)[8]) {
-  uint32_t v[4];
-  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
-               : "r"(addr));
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float2 p = unpack2<DT>(v[q]);
-    f[2 * q] = p.x;
-    f[2 * q + 1] = p.y;
-  }
+__device__ __forceinline__ void lds4f(uint32_t addr, float *f) {
+  uint32_t v0, v1;
+  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v0), "=r"(v1) : "r"(addr));
+  const float2 p = unpack2<DT>(v0), q = unpack2<DT>(v1);
+  f[0] = p.x; f[1] = p.y; f[2] = q.x; f[3] = q.y;
 }
 
 template <int DT, int MT, bool HAS_O>
@@ -302,10 +276,20 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
   T *yout = static_cast<T *>(a.y);
   T *nout = static_cast<T *>(a.normOut);
 
-  // this thread's 8 columns start at column c0 of the tile; their nibbles are the
-  // 4-byte word at byte woff of a 128-byte weight row, before the swizzle
-  const int c0 = cg * CPW + g * (CPW / 8);
-  const uint32_t woff = (uint32_t)(c0 / 2);
+  // Columns of the warp: cb .. cb + 63, in 16-bit groups of four (element e =
+  // columns 4e .. 4e+3). A transposed ldmatrix.x4 of 16 k-rows gives lane (g, t)
+  // the elements 16cg + g (matrices 0, 2) and 16cg + 8 + g (matrices 1, 3) of
+  // k-rows 2t, 2t+1 (matrices 0, 1) and 2t+8, 2t+9 (matrices 2, 3). MMA tile c
+  // (of four) takes nibble c of each: its row g is column cb + 4g + c and its
+  // row g + 8 is column cb + 32 + 4g + c.
+  const int cb = cg * CPW;
+  static_assert(CPW == 64, "four 16-column MMA tiles per warp");
+  uint32_t wlane;  // this lane's row address offset within a 16-row block, swizzled
+  {
+    const int mi = lane >> 3, rr = lane & 7;
+    const uint32_t chunk = 2u * cg + (uint32_t)(mi & 1);
+    wlane = (uint32_t)(8 * (mi >> 1) + rr) * 128u + ((chunk ^ (uint32_t)rr) << 4);
+  }
   // ldmatrix row of this lane in an x1 box (rows m at 128-byte pitch, swizzled)
   int ldm_m, ldm_c;
   {
@@ -327,7 +311,7 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
   const int t1c = u1 > u0 ? (u1 - 1) / a.kst : t0c - 1;
   int fin_tiles[4];
   int nfin = 0;
-  int j = 0, slot = 0;
+  int j = 0, jph = 0, slot = 0;  // jph = j % KH
   uint32_t ph = 0;
 
   for (int tile = t0c; tile <= t1c; ++tile) {
@@ -348,39 +332,36 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
 #pragma unroll
         for (int q = 0; q < 8; ++q) { sf[q] = sscal; of[q] = oscal; }
       } else {
-        const uint32_t o = (uint32_t)(row * DNT + c0) * 2u;
-        lds8f<DT>(base + a.off_s + o, sf);
+        // sf[c] / sf[4 + c]: columns cb + 4g + c / cb + 32 + 4g + c
+        const uint32_t o = (uint32_t)(row * DNT + cb + 4 * g) * 2u;
+        lds4f<DT>(base + a.off_s + o, sf);
+        lds4f<DT>(base + a.off_s + o + 64u, sf + 4);
         if constexpr (HAS_O) {
-          lds8f<DT>(base + a.off_o + o, of);
+          lds4f<DT>(base + a.off_o + o, of);
+          lds4f<DT>(base + a.off_o + o + 64u, of + 4);
         } else {
 #pragma unroll
           for (int q = 0; q < 8; ++q) of[q] = 0.f;
         }
       }
     };
-    // fold the group's sums into tot: S * acc (+ (O - 136 S) * d when A holds
-    // 136 + q, which is the case with an offset; without one A holds q itself)
+    // fold the group's sums into tot. A holds 136 + q (1032 + q in fp16) and d
+    // the x1 row sums of the same k-rows, so the group's exact sum is
+    // S * (acc - 136 d) + O * d = S * acc + (O - 136 S) * d.
     auto flush = [&](const float (&sf)[8], const float (&of)[8]) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float sl = sf[2 * i], sh = sf[2 * i + 1];
-        const float cl = HAS_O ? fmaf(-bias136, sl, of[2 * i]) : 0.f;
-        const float ch = HAS_O ? fmaf(-bias136, sh, of[2 * i + 1]) : 0.f;
+      for (int c = 0; c < 4; ++c) {
+        const float sl = sf[c], sh = sf[4 + c];  // rows g, g + 8 of MMA tile c
+        const float cl = fmaf(-bias136, sl, of[c]);
+        const float ch = fmaf(-bias136, sh, of[4 + c]);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          if constexpr (HAS_O) {
-            tot[mt][i][0] = fmaf(cl, d1[mt][0], fmaf(sl, acc[mt][i][0], tot[mt][i][0]));
-            tot[mt][i][1] = fmaf(cl, d1[mt][1], fmaf(sl, acc[mt][i][1], tot[mt][i][1]));
-            tot[mt][i][2] = fmaf(ch, d1[mt][0], fmaf(sh, acc[mt][i][2], tot[mt][i][2]));
-            tot[mt][i][3] = fmaf(ch, d1[mt][1], fmaf(sh, acc[mt][i][3], tot[mt][i][3]));
-          } else {
-            tot[mt][i][0] = fmaf(sl, acc[mt][i][0], tot[mt][i][0]);
-            tot[mt][i][1] = fmaf(sl, acc[mt][i][1], tot[mt][i][1]);
-            tot[mt][i][2] = fmaf(sh, acc[mt][i][2], tot[mt][i][2]);
-            tot[mt][i][3] = fmaf(sh, acc[mt][i][3], tot[mt][i][3]);
-          }
+          tot[mt][c][0] = fmaf(cl, d1[mt][0], fmaf(sl, acc[mt][c][0], tot[mt][c][0]));
+          tot[mt][c][1] = fmaf(cl, d1[mt][1], fmaf(sl, acc[mt][c][1], tot[mt][c][1]));
+          tot[mt][c][2] = fmaf(ch, d1[mt][0], fmaf(sh, acc[mt][c][2], tot[mt][c][2]));
+          tot[mt][c][3] = fmaf(ch, d1[mt][1], fmaf(sh, acc[mt][c][3], tot[mt][c][3]));
 #pragma unroll
-          for (int c = 0; c < 4; ++c) acc[mt][i][c] = 0.f;
+          for (int e = 0; e < 4; ++e) acc[mt][c][e] = 0.f;
         }
       }
 #pragma unroll
@@ -388,24 +369,20 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
     };
 
     for (int st = sbeg; st < send; ++st) {
-      if ((j & (KH - 1)) == kh) {
+      if (jph == kh) {
         const bool ok = wait_bar_warp(FULL(slot), ph, abort_flag, a.status, kDWhereConsumer);
         bool released = false;
         if (ok) {
           const uint32_t base = sb + (uint32_t)slot * a.slot;
           const int srow = st * DKB;
-          // the stage's operands of this warp: nibbles of k-rows 16kb + 2t + {0, 1, 8, 9}
-          // (through the swizzle) and B = x1^T (box kb/4; row m at m*128, chunk c at
-          // c ^ (m & 7)), all loaded before any arithmetic
+          // the stage's operands of this warp, all loaded before any arithmetic:
+          // the packed weights by transposed ldmatrix (16 k-rows x 64 columns
+          // per kb) and B = x1^T (box kb/4; row m at m*128, chunk c at c ^ (m & 7))
           uint32_t w[NB][4], b[NB][MT][2];
 #pragma unroll
           for (int kb = 0; kb < NB; ++kb) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int rl = 16 * kb + 2 * t + (q & 1) + 8 * (q >> 1);
-              const uint32_t phys = (((woff >> 4) ^ (uint32_t)(rl & 7)) << 4) | (woff & 15u);
-              w[kb][q] = lds32(base + (uint32_t)rl * 128u + phys);
-            }
+            ldmatrix_x4_trans(base + (uint32_t)kb * 2048u + wlane, w[kb][0], w[kb][1], w[kb][2],
+                              w[kb][3]);
             const int cidx = 2 * (kb & 3) + ldm_c;
             const uint32_t baddr = base + a.off_x + (uint32_t)(kb >> 2) * C::XB +
                                    (uint32_t)ldm_m * 128u + ((uint32_t)(cidx ^ (ldm_m & 7)) << 4);
@@ -434,27 +411,19 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
               if (cur - gs < a.so_rows) load_so(base, cur - gs, sf, of);
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint32_t a0, a1, a2, a3;
-              if constexpr (HAS_O) {
-                nib_pairs<DT>(w[kb][0], w[kb][1], i, a0, a1);
-                nib_pairs<DT>(w[kb][2], w[kb][3], i, a2, a3);
-              } else {
-                nib_pairs_q<DT>(w[kb][0], w[kb][1], i, a0, a1);
-                nib_pairs_q<DT>(w[kb][2], w[kb][3], i, a2, a3);
-              }
+            for (int c = 0; c < 4; ++c) {
+              const uint32_t a0 = nib_col<DT>(w[kb][0], c), a1 = nib_col<DT>(w[kb][1], c);
+              const uint32_t a2 = nib_col<DT>(w[kb][2], c), a3 = nib_col<DT>(w[kb][3], c);
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt)
-                mma_16816<BF>(acc[mt][i], a0, a1, a2, a3, b[kb][mt][0], b[kb][mt][1]);
+                mma_16816<BF>(acc[mt][c], a0, a1, a2, a3, b[kb][mt][0], b[kb][mt][1]);
             }
-            if constexpr (HAS_O) {
 #pragma unroll
-              for (int mt = 0; mt < MT; ++mt) {
-                float dd[4] = {d1[mt][0], d1[mt][1], d1[mt][0], d1[mt][1]};
-                mma_16816<BF>(dd, ones, ones, ones, ones, b[kb][mt][0], b[kb][mt][1]);
-                d1[mt][0] = dd[0];
-                d1[mt][1] = dd[1];
-              }
+            for (int mt = 0; mt < MT; ++mt) {  // d: x1 row sums of the block (A = all ones)
+              float dd[4] = {d1[mt][0], d1[mt][1], d1[mt][0], d1[mt][1]};
+              mma_16816<BF>(dd, ones, ones, ones, ones, b[kb][mt][0], b[kb][mt][1]);
+              d1[mt][0] = dd[0];
+              d1[mt][1] = dd[1];
             }
           }
           // a group past the copied scale rows lies wholly beyond K: its sums are zero
@@ -464,12 +433,13 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
         if (!released && lane == 0) mbar_arrive(EMPTY(slot));
       }
       ++j;
+      if (++jph == KH) jph = 0;
       if (++slot == NS) { slot = 0; ph ^= 1u; }
     }
 
     // ---- segment end: the k-phases add in shared memory, the partial goes out
-    auto red_idx = [&](int mt, int i, int c) {
-      return (8 * mt + 2 * t + (c & 1)) * DNT + c0 + 2 * i + (c >> 1);
+    auto red_idx = [&](int mt, int c, int e) {  // MMA tile c, accumulator element e
+      return (8 * mt + 2 * t + (e & 1)) * DNT + cb + 32 * (e >> 1) + 4 * g + c;
     };
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
@@ -493,14 +463,15 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
     // finish now, so a finisher does not wait for them after the partial sums.
     // Position qq of this thread is float4 q = ctid + CT*qq: columns 4q' .. 4q'+3
     // of row m = q / 64 (N % 32 == 0: all four columns or none).
-    constexpr int QPT = MP * DNT / 4 / CT;
+    constexpr int NQ = MP * DNT / 4;                 // float4 positions of a tile
+    constexpr int QPT = (NQ + CT - 1) / CT;          // per thread (warp-uniform tail)
     uint2 rres[QPT], rbia[QPT], rgam[QPT];
 #pragma unroll
     for (int qq = 0; qq < QPT; ++qq) {
       const int q = ctid + CT * qq;
       const int m = q / (DNT / 4), n = tile * DNT + 4 * (q - m * (DNT / 4));
       rres[qq] = rbia[qq] = rgam[qq] = make_uint2(0u, 0u);
-      if (m < a.M && n < a.N) {
+      if (q < NQ && m < a.M && n < a.N) {
         rres[qq] = __ldg(reinterpret_cast<const uint2 *>(res + (int64_t)m * a.N + n));
         if (bias) rbia[qq] = __ldg(reinterpret_cast<const uint2 *>(bias + n));
         rgam[qq] = __ldg(reinterpret_cast<const uint2 *>(gam + n));
@@ -538,7 +509,8 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
               a.part + ((int64_t)(live ? cc : c_first) * a.SMAX + seg) * (MP * DNT));
 #pragma unroll
           for (int qq = 0; qq < QPT; ++qq)
-            pv[qq][e] = live ? __ldcg(src + ctid + CT * qq) : make_float4(0.f, 0.f, 0.f, 0.f);
+            pv[qq][e] = (live && ctid + CT * qq < NQ) ? __ldcg(src + ctid + CT * qq)
+                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int qq = 0; qq < QPT; ++qq)
@@ -552,6 +524,7 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
 #pragma unroll
       for (int qq = 0; qq < QPT; ++qq) {
         const int q = ctid + CT * qq;
+        if (q >= NQ) break;  // whole warps (NQ and CT are multiples of 32)
         const int m = q / (DNT / 4), n = tile * DNT + 4 * (q - m * (DNT / 4));
         float yv[4] = {0.f, 0.f, 0.f, 0.f}, yg[4] = {0.f, 0.f, 0.f, 0.f};
         if (m < a.M && n < a.N) {
