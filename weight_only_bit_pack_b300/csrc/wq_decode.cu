@@ -326,13 +326,13 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
         for (int c = 0; c < 4; ++c) tot[mt][i][c] = acc[mt][i][c] = 0.f;
       d1[mt][0] = d1[mt][1] = 0.f;
     }
-    // scale / offset of this thread's 8 columns in scale row `row` of a stage copy
+    // scale / offset of this thread's 8 columns in scale row `row` of a stage
+    // copy: sf[c] is column cb + 4g + c, sf[4 + c] column cb + 32 + 4g + c
     auto load_so = [&](uint32_t base, int row, float (&sf)[8], float (&of)[8]) {
       if (a.Ns == 1) {
 #pragma unroll
         for (int q = 0; q < 8; ++q) { sf[q] = sscal; of[q] = oscal; }
       } else {
-        // sf[c] / sf[4 + c]: columns cb + 4g + c / cb + 32 + 4g + c
         const uint32_t o = (uint32_t)(row * DNT + cb + 4 * g) * 2u;
         lds4f<DT>(base + a.off_s + o, sf);
         lds4f<DT>(base + a.off_s + o + 64u, sf + 4);
