@@ -12,12 +12,13 @@
 //   warps 4-11   dequant: packed weight -> B operand (W^T, 256 x 64, K-major,
 //                128-byte swizzle), in one of two exact forms (below).
 //   warps 12-15  epilogue (one per TMEM lane quarter): y = acc + bias +
-//                residual, written to HBM and kept (fp32) in TMEM; per-row
-//                partial sum(y^2) published to the workspace; then, for the
+//                residual, written to HBM; per-row partial sum(y^2) (of the
+//                fp32 y) published to the workspace; the accumulator is handed
+//                back to the MMA as soon as it has been read. Then, for the
 //                previous tile, wait until every n-tile of its row block has
 //                published, sum the partials in a fixed order, and write
-//                normOut = y * rstd * gamma from TMEM. y is never read back
-//                from memory.
+//                normOut = y * rstd * gamma from the y this thread stored
+//                (still in L2: a row block of y is 128 x N x 2 bytes).
 // Operand modes (both keep the dequantized weight exact or within 2^-12):
 //   RAWQ   per-tensor / per-channel scales: B holds the integer q itself (exact
 //          in fp16 and bf16), the MMA accumulates x1*q in fp32, and the epilogue
@@ -31,7 +32,8 @@
 //          result outside the operator's stated tolerance at these K.
 // Pipelines: NR raw stages (x1 + packed weight) and NB dequantized-weight
 // stages, each guarded by full/empty mbarriers; two accumulator buffers, so
-// the epilogue of tile j overlaps the main loop of tile j+1.
+// the epilogue of tile j overlaps the main loop of tile j+1, and the wait for
+// a row block never holds an accumulator.
 //
 // Cross-CTA row reduction: all CTAs are co-resident (grid <= SMs, 1 CTA/SM)
 // and a CTA publishes tile j before it waits for the row block of tile j-1;
@@ -452,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long prev_t = -1;
     bool ok = true;
 
-    auto normalize = [&](long long t, int buf) -> bool {
+    auto normalize = [&](long long t) -> bool {
       const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
       const long long m = (long long)rb * BM + rit;
       const bool row_ok = m < a.M;
@@ -479,33 +481,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < a.nTilesN; ++j) tot += __ldcg(rp + j);
       }
       const float rstd = rsqrtf(tot / (float)a.N + a.eps);
-      const uint32_t taddr = lane_addr + (uint32_t)(buf * BN);
+      if (!row_ok) return true;
       const int n0 = nt * BN;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(taddr + 32 * c, r);
-        tmem_wait_ld();
+      const int n1 = n0 + BN < a.N ? n0 + BN : a.N;
+      // the row's y of this tile, as this thread stored it, 8 columns a load
+      // (N % 16 == 0 keeps every 8-column group whole)
+#pragma unroll 4
+      for (int n = n0; n < n1; n += 8) {
+        const uint4 yv = __ldcg(reinterpret_cast<const uint4 *>(yout + m * a.N + n));
+        const uint4 g = *reinterpret_cast<const uint4 *>(gam + n);
+        const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w}, gw[4] = {g.x, g.y, g.z, g.w};
+        uint32_t o[4];
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int n = n0 + 32 * c + 8 * v;
-          if (n < a.N && row_ok) {
-            const uint4 g = *reinterpret_cast<const uint4 *>(gam + n);
-            const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 g2 = unpack2<DT>(gw[i]);
-              o[i] = pack2<DT>(__uint_as_float(r[8 * v + 2 * i]) * rstd * g2.x,
-                               __uint_as_float(r[8 * v + 2 * i + 1]) * rstd * g2.y);
-            }
-            *reinterpret_cast<uint4 *>(nout + m * a.N + n) = make_uint4(o[0], o[1], o[2], o[3]);
-          }
+        for (int i = 0; i < 4; ++i) {
+          const float2 y2 = unpack2<DT>(yw[i]), g2 = unpack2<DT>(gw[i]);
+          o[i] = pack2<DT>(y2.x * rstd * g2.x, y2.y * rstd * g2.y);
         }
+        *reinterpret_cast<uint4 *>(nout + m * a.N + n) = make_uint4(o[0], o[1], o[2], o[3]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(ACCEMPTY(buf)));
       return true;
     };
 
@@ -541,7 +534,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           const int n = n0 + 32 * c + 8 * v;
-          float yv[8];
           if (n < a.N) {
             // mm = the operator's x1 @ W for these 8 columns
             float mmv[8];
@@ -587,6 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint4 rr = *reinterpret_cast<const uint4 *>(res + m * a.N + n);
               rw[0] = rr.x; rw[1] = rr.y; rw[2] = rr.z; rw[3] = rr.w;
             }
+            float yv[8];
             uint32_t yo[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -601,16 +594,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int i = 0; i < 8; ++i) ss = fmaf(yv[i], yv[i], ss);
               *reinterpret_cast<uint4 *>(yout + m * a.N + n) = make_uint4(yo[0], yo[1], yo[2], yo[3]);
             }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) yv[i] = 0.f;
           }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) r[8 * v + i] = __float_as_uint(yv[i]);
         }
-        tmem_st32(taddr + 32 * c, r);
       }
-      tmem_wait_st();
+      // the accumulator has been read: hand it back to the MMA issuer
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(ACCEMPTY(buf)));
       if (row_ok) a.rowpart[m * a.nTilesN + nt] = ss;
       // each epilogue warp publishes its 32 rows; the row block is complete
       // when all kEpiWarps warps of all n-tiles have published
@@ -621,14 +611,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (prev_t >= 0) {
-        if (!normalize(prev_t, buf ^ 1)) {
+        if (!normalize(prev_t)) {
           ok = false;
           break;
         }
       }
       prev_t = t;
     }
-    if (ok && prev_t >= 0) normalize(prev_t, (lt - 1) & 1);
+    if (ok && prev_t >= 0) normalize(prev_t);
   }
 
   tc_fence_before();
