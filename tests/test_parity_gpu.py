@@ -91,6 +91,12 @@ PREFILL_EDGE = [
                            mode="channel")),
     ("wide_rows_79_ntiles", dict(M_shape=(200,), K=128, N=20000 + 224, dtype=torch.bfloat16,
                                  wbits=4, mode="group", group=32)),
+    # enough n-tiles that 256-row tiles (two 128-row MMA halves) are chosen:
+    # the last row block ends inside its first half, its second half is empty
+    ("halves_m_tail_bf16_g64", dict(M_shape=(600,), K=128, N=148 * 256, dtype=torch.bfloat16,
+                                    wbits=4, mode="group", group=64)),
+    ("halves_fp16_channel_offset", dict(M_shape=(200,), K=192, N=79 * 256, dtype=torch.float16,
+                                        wbits=4, mode="channel")),
 ]
 
 

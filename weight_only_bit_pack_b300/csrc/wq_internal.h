@@ -64,6 +64,7 @@ struct Plan {
            o16_off = 0, x16_off = 0;
   int64_t n_tiles = 0, m_tiles = 0;
   int grid = 0;
+  int m_halves = 1;  // prefill: 128-row MMA halves per output tile (1 or 2)
 };
 
 // Launchers (return cudaError_t of the launch).

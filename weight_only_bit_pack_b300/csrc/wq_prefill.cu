@@ -3,12 +3,14 @@
 // "Function description": mm_out = x1 @ (x2*antiquantScale + antiquantOffset)
 // + bias; y = mm_out + residual; normOut = y / RMS(y) * gamma).
 //
-// One persistent CTA per SM walks output tiles of BM x BN = 128 x 256 in
-// row-block-major order. Warp roles (16 warps):
-//   warp 0       TMA producer: x1 tile (128 x 64, 128-byte swizzle) and the
+// One persistent CTA per SM walks output tiles of (128 MH) x 256 in
+// row-block-major order, MH = 1 or (INT4 weights, M > 128) 2: with two 128-row
+// halves one dequantized weight tile feeds twice the MMAs. Warp roles (16 warps):
+//   warp 0       TMA producer: x1 tile (128 MH x 64, 128-byte swizzle) and the
 //                packed weight tile (64 k-rows x 256 n, INT4 or INT8) per k-step.
-//   warp 1       TMEM owner (512 columns = two 128 x 256 fp32 accumulators) and
-//                tcgen05.mma issuer (M=128, N=256, K=16, kind::f16).
+//   warp 1       TMEM owner (512 columns: two 128 x 256 fp32 accumulators, or
+//                the two halves of one) and tcgen05.mma issuer (M=128, N=256,
+//                K=16, kind::f16; one MMA per half).
 //   warps 4-11   dequant: packed weight -> B operand (W^T, 256 x 64, K-major,
 //                128-byte swizzle), in one of two exact forms (below).
 //   warps 12-15  epilogue (one per TMEM lane quarter): y = acc + bias +
@@ -31,9 +33,10 @@
 //          2^(e_m + e_n). Rounding W to bf16 instead (2^-9) would put the
 //          result outside the operator's stated tolerance at these K.
 // Pipelines: NR raw stages (x1 + packed weight) and NB dequantized-weight
-// stages, each guarded by full/empty mbarriers; two accumulator buffers, so
-// the epilogue of tile j overlaps the main loop of tile j+1, and the wait for
-// a row block never holds an accumulator.
+// stages, each guarded by full/empty mbarriers. With MH = 1 two accumulator
+// buffers let the epilogue of tile j overlap the main loop of tile j+1; with
+// MH = 2 the single accumulator is handed back as soon as the epilogue has
+// read it. The wait for a row block never holds an accumulator.
 //
 // Cross-CTA row reduction: all CTAs are co-resident (grid <= SMs, 1 CTA/SM)
 // and a CTA publishes tile j before it waits for the row block of tile j-1;
@@ -58,9 +61,12 @@ using namespace sm100;
 
 constexpr int BM = 128, BN = 256, BK = 64;
 // Stage counts: NR raw stages (x1 tile + packed weight tile + scale/offset
-// rows) and NB dequantized-weight stages; INT8 tiles are twice as large, so
-// they get one raw stage less to stay inside 227 KB of shared memory.
-template <int WBITS> struct Stages { static constexpr int NR = WBITS == 4 ? 4 : 3, NB = 3; };
+// rows) and NB dequantized-weight stages, within 227 KB of shared memory:
+// INT8 tiles are twice as large, and a 256-row x1 tile twice as large again.
+template <int WBITS, int MH> struct Stages {
+  static_assert(MH == 1 || (MH == 2 && WBITS == 4), "256-row tiles with INT4 weights only");
+  static constexpr int NR = MH == 2 ? 3 : (WBITS == 4 ? 4 : 3), NB = MH == 2 ? 2 : 3;
+};
 constexpr int SO_ROWS = 3;  // group rows a 64-deep k-stage can touch (group >= 32)
 constexpr int kThreads = 512;
 constexpr int kDqWarp0 = 4, kDqWarps = 8;
@@ -91,10 +97,11 @@ struct PrefillArgs {
   uint32_t so_bytes;         // F16EMU: bytes of one scale/offset row box (rows x 256 x 4)
 };
 
-template <int WBITS>
+template <int WBITS, int MH>
 struct Layout {
-  static constexpr int NR = Stages<WBITS>::NR, NB = Stages<WBITS>::NB;
-  static constexpr uint32_t A_BYTES = BM * BK * 2;            // 16 KB
+  static constexpr int NR = Stages<WBITS, MH>::NR, NB = Stages<WBITS, MH>::NB;
+  static constexpr uint32_t A_HALF = BM * BK * 2;             // 16 KB: one 128-row half
+  static constexpr uint32_t A_BYTES = MH * A_HALF;
   static constexpr uint32_t BQ_BYTES = BK * BN * WBITS / 8;   // 8 or 16 KB
   static constexpr uint32_t B_BYTES = BN * BK * 2;            // 32 KB
   static constexpr uint32_t SO_BYTES = SO_ROWS * BN * 4;      // 3 KB: rows of S16 / O16 pairs
@@ -178,12 +185,14 @@ __device__ __forceinline__ uint32_t sw128_chunk(int r, int c) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-template <int DT, int WBITS, int MODE>
+template <int DT, int WBITS, int MODE, int MH>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                    const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_o,
                    const PrefillArgs a) {
-  using L = Layout<WBITS>;
+  using L = Layout<WBITS, MH>;
+  constexpr int NACC = 2 / MH;   // accumulator buffers of MH x 256 TMEM columns
+  constexpr int TM = BM * MH;    // output rows per tile
   using E = Elem<DT>;
   using T = typename E::T;
   constexpr int MDT = MODE == kF16Emu ? WQ_F16 : DT;  // operand dtype of the MMA
@@ -208,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(BFULL(s)), kDqWarps);
       mbar_init(BAR(BEMPTY(s)), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NACC; ++b) {
       mbar_init(BAR(ACCFULL(b)), 1);
       mbar_init(BAR(ACCEMPTY(b)), kEpiWarps);
     }
@@ -246,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t bytes = L::A_BYTES + L::BQ_BYTES;
           if (MODE == kF16Emu) bytes += (a.offset ? 2u : 1u) * a.so_bytes;
           mbar_arrive_expect_tx(BAR(FULL(s)), bytes);
-          tma_load_2d(sbase + L::A_OFF + s * L::A_BYTES, &tm_x, ks * BK, rb * BM, BAR(FULL(s)));
+          tma_load_2d(sbase + L::A_OFF + s * L::A_BYTES, &tm_x, ks * BK, rb * TM, BAR(FULL(s)));
           tma_load_2d_hint(sbase + L::BQ_OFF + s * L::BQ_BYTES, &tm_w, nt * (BN * WBITS / 8),
                            ks * BK, BAR(FULL(s)), pol_w);
           if (MODE == kF16Emu) {
@@ -272,12 +281,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       long long it = 0;
       int lt = 0;
       for (long long t = blockIdx.x; t < a.nTiles; t += gridDim.x, ++lt) {
-        const int buf = lt & 1;
-        if (!wait_bar_warp(BAR(ACCEMPTY(buf)), (uint32_t)(((lt >> 1) & 1) ^ 1), abort_flag, a.status,
-                           kWhereMma))
+        const int buf = lt % NACC;
+        if (!wait_bar_warp(BAR(ACCEMPTY(buf)), (uint32_t)(((lt / NACC) & 1) ^ 1), abort_flag,
+                           a.status, kWhereMma))
           goto mdone;
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+        const uint32_t d = tmem_base + (uint32_t)(buf * BN);  // half h at + h * BN
         for (int ks = 0; ks < a.kTiles; ++ks, ++it) {
           const int s = (int)(it % NR), sb = (int)(it % NB);
           if (!wait_bar_warp(BAR(FULL(s)), (uint32_t)((it / NR) & 1), abort_flag, a.status, kWhereMma))
@@ -291,8 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t baddr = sbase + L::B_OFF + sb * L::B_BYTES;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
-              mma_f16(d, desc_kmajor_sw128(aaddr + kk * 32), desc_kmajor_sw128(baddr + kk * 32),
-                      idesc, (ks | kk) != 0 ? 1u : 0u);
+#pragma unroll
+              for (int h = 0; h < MH; ++h)
+                mma_f16(d + (uint32_t)(h * BN), desc_kmajor_sw128(aaddr + h * L::A_HALF + kk * 32),
+                        desc_kmajor_sw128(baddr + kk * 32), idesc, (ks | kk) != 0 ? 1u : 0u);
             mma_commit(BAR(BEMPTY(sb)));
             mma_commit(BAR(RAWEMPTY(s)));
           }
@@ -456,8 +467,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     auto normalize = [&](long long t) -> bool {
       const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
-      const long long m = (long long)rb * BM + rit;
-      const bool row_ok = m < a.M;
       // wait until every n-tile of this row block published its partial sums
       {
         const uint32_t target = (uint32_t)(kEpiWarps * a.nTilesN);
@@ -475,133 +484,139 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!__all_sync(0xffffffffu, done)) return false;
       }
-      float tot = 0.f;
-      if (row_ok) {
-        const float *rp = a.rowpart + m * a.nTilesN;
-        for (int j = 0; j < a.nTilesN; ++j) tot += __ldcg(rp + j);
-      }
-      const float rstd = rsqrtf(tot / (float)a.N + a.eps);
-      if (!row_ok) return true;
       const int n0 = nt * BN;
       const int n1 = n0 + BN < a.N ? n0 + BN : a.N;
-      // the row's y of this tile, as this thread stored it, 8 columns a load
-      // (N % 16 == 0 keeps every 8-column group whole)
+#pragma unroll 1
+      for (int h = 0; h < MH; ++h) {
+        const long long m = (long long)rb * TM + h * BM + rit;
+        if (m >= a.M) break;
+        float tot = 0.f;
+        const float *rp = a.rowpart + m * a.nTilesN;
+        for (int j = 0; j < a.nTilesN; ++j) tot += __ldcg(rp + j);
+        const float rstd = rsqrtf(tot / (float)a.N + a.eps);
+        // the row's y of this tile, as this thread stored it, 8 columns a load
+        // (N % 16 == 0 keeps every 8-column group whole)
 #pragma unroll 4
-      for (int n = n0; n < n1; n += 8) {
-        const uint4 yv = __ldcg(reinterpret_cast<const uint4 *>(yout + m * a.N + n));
-        const uint4 g = *reinterpret_cast<const uint4 *>(gam + n);
-        const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w}, gw[4] = {g.x, g.y, g.z, g.w};
-        uint32_t o[4];
+        for (int n = n0; n < n1; n += 8) {
+          const uint4 yv = __ldcg(reinterpret_cast<const uint4 *>(yout + m * a.N + n));
+          const uint4 g = *reinterpret_cast<const uint4 *>(gam + n);
+          const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w}, gw[4] = {g.x, g.y, g.z, g.w};
+          uint32_t o[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 y2 = unpack2<DT>(yw[i]), g2 = unpack2<DT>(gw[i]);
-          o[i] = pack2<DT>(y2.x * rstd * g2.x, y2.y * rstd * g2.y);
+          for (int i = 0; i < 4; ++i) {
+            const float2 y2 = unpack2<DT>(yw[i]), g2 = unpack2<DT>(gw[i]);
+            o[i] = pack2<DT>(y2.x * rstd * g2.x, y2.y * rstd * g2.y);
+          }
+          *reinterpret_cast<uint4 *>(nout + m * a.N + n) = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        *reinterpret_cast<uint4 *>(nout + m * a.N + n) = make_uint4(o[0], o[1], o[2], o[3]);
       }
       return true;
     };
 
     for (long long t = blockIdx.x; t < a.nTiles && ok; t += gridDim.x, ++lt) {
-      const int buf = lt & 1;
-      if (!wait_bar_warp(BAR(ACCFULL(buf)), (uint32_t)((lt >> 1) & 1), abort_flag, a.status,
+      const int buf = lt % NACC;
+      if (!wait_bar_warp(BAR(ACCFULL(buf)), (uint32_t)((lt / NACC) & 1), abort_flag, a.status,
                          kWhereEpiAcc)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
-      const long long m = (long long)rb * BM + rit;
-      const bool row_ok = m < a.M;
       const int n0 = nt * BN;
-      const uint32_t taddr = lane_addr + (uint32_t)(buf * BN);
-      float ss = 0.f;
-      // per-row factor of this thread's row
-      float rs = 0.f;   // RAWQ + offset: sum_k x1[m, k]
-      int em = 0;       // F16EMU: row exponent
-      if (row_ok) {
-        if constexpr (MODE == kRawQ) {
-          if (a.offset) rs = a.rowsum[m];
-        } else {
-          em = a.e_row[m];
-        }
-      }
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(taddr + 32 * c, r);
-        tmem_wait_ld();
+      for (int h = 0; h < MH; ++h) {
+        const long long m = (long long)rb * TM + h * BM + rit;
+        const bool row_ok = m < a.M;
+        const uint32_t taddr = lane_addr + (uint32_t)((buf + h) * BN);
+        float ss = 0.f;
+        // per-row factor of this thread's row
+        float rs = 0.f;   // RAWQ + offset: sum_k x1[m, k]
+        int em = 0;       // F16EMU: row exponent
+        if (row_ok) {
+          if constexpr (MODE == kRawQ) {
+            if (a.offset) rs = a.rowsum[m];
+          } else {
+            em = a.e_row[m];
+          }
+        }
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(taddr + 32 * c, r);
+          tmem_wait_ld();
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int n = n0 + 32 * c + 8 * v;
-          if (n < a.N) {
-            // mm = the operator's x1 @ W for these 8 columns
-            float mmv[8];
-            if constexpr (MODE == kRawQ) {
-              uint32_t sw[4], ow[4] = {0u, 0u, 0u, 0u};
-              if (a.Ns == 1) {
-                const uint32_t sb = *reinterpret_cast<const uint16_t *>(a.scale);
-                sw[0] = sw[1] = sw[2] = sw[3] = sb | (sb << 16);
-                if (a.offset) {
-                  const uint32_t ob = *reinterpret_cast<const uint16_t *>(a.offset);
-                  ow[0] = ow[1] = ow[2] = ow[3] = ob | (ob << 16);
+          for (int v = 0; v < 4; ++v) {
+            const int n = n0 + 32 * c + 8 * v;
+            if (n < a.N) {
+              // mm = the operator's x1 @ W for these 8 columns
+              float mmv[8];
+              if constexpr (MODE == kRawQ) {
+                uint32_t sw[4], ow[4] = {0u, 0u, 0u, 0u};
+                if (a.Ns == 1) {
+                  const uint32_t sb = *reinterpret_cast<const uint16_t *>(a.scale);
+                  sw[0] = sw[1] = sw[2] = sw[3] = sb | (sb << 16);
+                  if (a.offset) {
+                    const uint32_t ob = *reinterpret_cast<const uint16_t *>(a.offset);
+                    ow[0] = ow[1] = ow[2] = ow[3] = ob | (ob << 16);
+                  }
+                } else {
+                  const uint4 sv = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.scale) + n);
+                  sw[0] = sv.x; sw[1] = sv.y; sw[2] = sv.z; sw[3] = sv.w;
+                  if (a.offset) {
+                    const uint4 ov = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.offset) + n);
+                    ow[0] = ov.x; ow[1] = ov.y; ow[2] = ov.z; ow[3] = ov.w;
+                  }
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float2 s2 = unpack2<DT>(sw[i]);
+                  const float2 o2 = unpack2<DT>(ow[i]);
+                  mmv[2 * i] = fmaf(s2.x, __uint_as_float(r[8 * v + 2 * i]), o2.x * rs);
+                  mmv[2 * i + 1] = fmaf(s2.y, __uint_as_float(r[8 * v + 2 * i + 1]), o2.y * rs);
                 }
               } else {
-                const uint4 sv = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.scale) + n);
-                sw[0] = sv.x; sw[1] = sv.y; sw[2] = sv.z; sw[3] = sv.w;
-                if (a.offset) {
-                  const uint4 ov = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.offset) + n);
-                  ow[0] = ov.x; ow[1] = ov.y; ow[2] = ov.z; ow[3] = ov.w;
+                const uint2 ev = *reinterpret_cast<const uint2 *>(a.e_col + n);
+                const uint32_t ew[2] = {ev.x, ev.y};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const int en = (int)(int8_t)((ew[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+                  mmv[i] = __uint_as_float(r[8 * v + i]) * __int_as_float((em + en + 127) << 23);
                 }
               }
+              uint32_t bw[4] = {0u, 0u, 0u, 0u}, rw[4] = {0u, 0u, 0u, 0u};
+              if (bias) {
+                const uint4 bb = *reinterpret_cast<const uint4 *>(bias + n);
+                bw[0] = bb.x; bw[1] = bb.y; bw[2] = bb.z; bw[3] = bb.w;
+              }
+              if (row_ok) {
+                const uint4 rr = *reinterpret_cast<const uint4 *>(res + m * a.N + n);
+                rw[0] = rr.x; rw[1] = rr.y; rw[2] = rr.z; rw[3] = rr.w;
+              }
+              float yv[8];
+              uint32_t yo[4];
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                const float2 s2 = unpack2<DT>(sw[i]);
-                const float2 o2 = unpack2<DT>(ow[i]);
-                mmv[2 * i] = fmaf(s2.x, __uint_as_float(r[8 * v + 2 * i]), o2.x * rs);
-                mmv[2 * i + 1] = fmaf(s2.y, __uint_as_float(r[8 * v + 2 * i + 1]), o2.y * rs);
+                const float2 b2 = unpack2<DT>(bw[i]);
+                const float2 r2 = unpack2<DT>(rw[i]);
+                yv[2 * i] = mmv[2 * i] + b2.x + r2.x;
+                yv[2 * i + 1] = mmv[2 * i + 1] + b2.y + r2.y;
+                yo[i] = pack2<DT>(yv[2 * i], yv[2 * i + 1]);
               }
-            } else {
-              const uint2 ev = *reinterpret_cast<const uint2 *>(a.e_col + n);
-              const uint32_t ew[2] = {ev.x, ev.y};
+              if (row_ok) {
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const int en = (int)(int8_t)((ew[i >> 2] >> (8 * (i & 3))) & 0xFFu);
-                mmv[i] = __uint_as_float(r[8 * v + i]) * __int_as_float((em + en + 127) << 23);
+                for (int i = 0; i < 8; ++i) ss = fmaf(yv[i], yv[i], ss);
+                *reinterpret_cast<uint4 *>(yout + m * a.N + n) =
+                    make_uint4(yo[0], yo[1], yo[2], yo[3]);
               }
-            }
-            uint32_t bw[4] = {0u, 0u, 0u, 0u}, rw[4] = {0u, 0u, 0u, 0u};
-            if (bias) {
-              const uint4 bb = *reinterpret_cast<const uint4 *>(bias + n);
-              bw[0] = bb.x; bw[1] = bb.y; bw[2] = bb.z; bw[3] = bb.w;
-            }
-            if (row_ok) {
-              const uint4 rr = *reinterpret_cast<const uint4 *>(res + m * a.N + n);
-              rw[0] = rr.x; rw[1] = rr.y; rw[2] = rr.z; rw[3] = rr.w;
-            }
-            float yv[8];
-            uint32_t yo[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 b2 = unpack2<DT>(bw[i]);
-              const float2 r2 = unpack2<DT>(rw[i]);
-              yv[2 * i] = mmv[2 * i] + b2.x + r2.x;
-              yv[2 * i + 1] = mmv[2 * i + 1] + b2.y + r2.y;
-              yo[i] = pack2<DT>(yv[2 * i], yv[2 * i + 1]);
-            }
-            if (row_ok) {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) ss = fmaf(yv[i], yv[i], ss);
-              *reinterpret_cast<uint4 *>(yout + m * a.N + n) = make_uint4(yo[0], yo[1], yo[2], yo[3]);
             }
           }
         }
-      }
+        if (row_ok) a.rowpart[m * a.nTilesN + nt] = ss;
+      }  // halves
       // the accumulator has been read: hand it back to the MMA issuer
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(ACCEMPTY(buf)));
-      if (row_ok) a.rowpart[m * a.nTilesN + nt] = ss;
       // each epilogue warp publishes its 32 rows; the row block is complete
       // when all kEpiWarps warps of all n-tiles have published
       __syncwarp();
@@ -675,9 +690,22 @@ bool plan_prefill(const Problem &p, Plan &plan) {
   plan.kernel = WQ_KERNEL_PREFILL;
   plan.mode = p.smode == kPerGroup ? kF16Emu : kRawQ;
   plan.n_tiles = (p.N + BN - 1) / BN;
-  plan.m_tiles = (p.M + BM - 1) / BM;
+  // 256-row tiles (INT4): one dequantized weight tile feeds two MMAs, which
+  // makes a row cost about kHalvesCost of a 128-row tile's; taken when that
+  // outweighs the coarser last wave of tiles over the SMs.
+  const int64_t sms = device_info().sms;
+  auto waves = [&](int64_t rows) {
+    const int64_t tiles = plan.n_tiles * ((p.M + rows - 1) / rows);
+    return (tiles + sms - 1) / sms;
+  };
+  constexpr double kHalvesCost = 0.8;
+  plan.m_halves = (p.wbits == 4 && p.M > BM &&
+                   (double)waves(2 * BM) * 2.0 * kHalvesCost < (double)waves(BM))
+                      ? 2
+                      : 1;
+  plan.m_tiles = (p.M + BM * plan.m_halves - 1) / (BM * plan.m_halves);
   const int64_t tiles = plan.n_tiles * plan.m_tiles;
-  plan.grid = (int)(tiles < device_info().sms ? tiles : device_info().sms);
+  plan.grid = (int)(tiles < sms ? tiles : sms);
   uint64_t off = kWsHeader;
   plan.cnt_off = off;
   off += align256((uint64_t)plan.m_tiles * 4);
@@ -706,13 +734,13 @@ bool plan_prefill(const Problem &p, Plan &plan) {
   return true;
 }
 
-template <int DT, int WBITS, int MODE>
+template <int DT, int WBITS, int MODE, int MH>
 static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws, cudaStream_t s) {
-  using L = Layout<WBITS>;
+  using L = Layout<WBITS, MH>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(prefill_kernel<DT, WBITS, MODE>,
+    attr_err = cudaFuncSetAttribute(prefill_kernel<DT, WBITS, MODE, MH>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -765,7 +793,7 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
   {
     const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.M};
     const cuuint64_t strides[1] = {(cuuint64_t)p.K * 2};
-    const cuuint32_t box[2] = {BK, BM};
+    const cuuint32_t box[2] = {BK, BM * MH};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(&tm_x, a_type, 2, const_cast<void *>(a_src), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -803,17 +831,27 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
       if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
   }
-  prefill_kernel<DT, WBITS, MODE><<<plan.grid, kThreads, L::SMEM, s>>>(tm_x, tm_w, tm_s, tm_o, args);
+  prefill_kernel<DT, WBITS, MODE, MH>
+      <<<plan.grid, kThreads, L::SMEM, s>>>(tm_x, tm_w, tm_s, tm_o, args);
   return cudaGetLastError();
+}
+
+template <int DT, int WBITS, int MODE>
+static cudaError_t launch_prefill_h(const Problem &p, const Plan &plan, void *ws, cudaStream_t s) {
+  if constexpr (WBITS == 4) {
+    if (plan.m_halves == 2) return launch_prefill_t<DT, WBITS, MODE, 2>(p, plan, ws, s);
+  }
+  if (plan.m_halves != 1) return cudaErrorNotSupported;
+  return launch_prefill_t<DT, WBITS, MODE, 1>(p, plan, ws, s);
 }
 
 template <int DT, int WBITS>
 static cudaError_t launch_prefill_m(const Problem &p, const Plan &plan, void *ws, cudaStream_t s) {
   if (plan.mode == kF16Emu) {
-    if constexpr (DT == WQ_BF16) return launch_prefill_t<DT, WBITS, kF16Emu>(p, plan, ws, s);
+    if constexpr (DT == WQ_BF16) return launch_prefill_h<DT, WBITS, kF16Emu>(p, plan, ws, s);
     return cudaErrorNotSupported;
   }
-  return launch_prefill_t<DT, WBITS, kRawQ>(p, plan, ws, s);
+  return launch_prefill_h<DT, WBITS, kRawQ>(p, plan, ws, s);
 }
 
 cudaError_t launch_prefill(const Problem &p, const Plan &plan, void *ws, cudaStream_t s) {
