@@ -97,6 +97,8 @@ PREFILL_EDGE = [
                                     wbits=4, mode="group", group=64)),
     ("halves_fp16_channel_offset", dict(M_shape=(200,), K=192, N=79 * 256, dtype=torch.float16,
                                         wbits=4, mode="channel")),
+    ("int8_bf16_tensor_79_ntiles", dict(M_shape=(200,), K=96, N=79 * 256, dtype=torch.bfloat16,
+                                        wbits=8, mode="tensor", bias=False)),
 ]
 
 

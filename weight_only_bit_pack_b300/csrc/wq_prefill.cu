@@ -5,7 +5,8 @@
 //
 // One persistent CTA per SM walks output tiles of (128 MH) x 256 in
 // row-block-major order, MH = 1 or (INT4 weights, M > 128) 2: with two 128-row
-// halves one dequantized weight tile feeds twice the MMAs. Warp roles (16 warps):
+// halves one dequantized INT4 weight tile feeds twice the MMAs (INT8 weights
+// are cheap to dequantize and gain nothing from it). Warp roles (16 warps):
 //   warp 0       TMA producer: x1 tile (128 MH x 64, 128-byte swizzle) and the
 //                packed weight tile (64 k-rows x 256 n, INT4 or INT8) per k-step.
 //   warp 1       TMEM owner (512 columns: two 128 x 256 fp32 accumulators, or
@@ -64,7 +65,6 @@ constexpr int BM = 128, BN = 256, BK = 64;
 // rows) and NB dequantized-weight stages, within 227 KB of shared memory:
 // INT8 tiles are twice as large, and a 256-row x1 tile twice as large again.
 template <int WBITS, int MH> struct Stages {
-  static_assert(MH == 1 || (MH == 2 && WBITS == 4), "256-row tiles with INT4 weights only");
   static constexpr int NR = MH == 2 ? 3 : (WBITS == 4 ? 4 : 3), NB = MH == 2 ? 2 : 3;
 };
 constexpr int SO_ROWS = 3;  // group rows a 64-deep k-stage can touch (group >= 32)
@@ -97,14 +97,16 @@ struct PrefillArgs {
   uint32_t so_bytes;         // F16EMU: bytes of one scale/offset row box (rows x 256 x 4)
 };
 
-template <int WBITS, int MH>
+template <int WBITS, int MH, int MODE>
 struct Layout {
+  static_assert(MH == 1 || (MH == 2 && WBITS == 4), "256-row tiles with INT4 weights only");
   static constexpr int NR = Stages<WBITS, MH>::NR, NB = Stages<WBITS, MH>::NB;
   static constexpr uint32_t A_HALF = BM * BK * 2;             // 16 KB: one 128-row half
   static constexpr uint32_t A_BYTES = MH * A_HALF;
   static constexpr uint32_t BQ_BYTES = BK * BN * WBITS / 8;   // 8 or 16 KB
   static constexpr uint32_t B_BYTES = BN * BK * 2;            // 32 KB
-  static constexpr uint32_t SO_BYTES = SO_ROWS * BN * 4;      // 3 KB: rows of S16 / O16 pairs
+  // F16EMU: rows of S16 / O16 pairs (3 KB); RAWQ reads scales in the epilogue
+  static constexpr uint32_t SO_BYTES = MODE == kF16Emu ? SO_ROWS * BN * 4 : 0;
   static constexpr uint32_t A_OFF = 0;
   static constexpr uint32_t BQ_OFF = A_OFF + NR * A_BYTES;
   static constexpr uint32_t B_OFF = BQ_OFF + NR * BQ_BYTES;
@@ -190,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                    const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_o,
                    const PrefillArgs a) {
-  using L = Layout<WBITS, MH>;
+  using L = Layout<WBITS, MH, MODE>;
   constexpr int NACC = 2 / MH;   // accumulator buffers of MH x 256 TMEM columns
   constexpr int TM = BM * MH;    // output rows per tile
   using E = Elem<DT>;
@@ -698,7 +700,7 @@ bool plan_prefill(const Problem &p, Plan &plan) {
     const int64_t tiles = plan.n_tiles * ((p.M + rows - 1) / rows);
     return (tiles + sms - 1) / sms;
   };
-  constexpr double kHalvesCost = 0.8;
+  constexpr double kHalvesCost = 0.75;
   plan.m_halves = (p.wbits == 4 && p.M > BM &&
                    (double)waves(2 * BM) * 2.0 * kHalvesCost < (double)waves(BM))
                       ? 2
@@ -736,7 +738,7 @@ bool plan_prefill(const Problem &p, Plan &plan) {
 
 template <int DT, int WBITS, int MODE, int MH>
 static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws, cudaStream_t s) {
-  using L = Layout<WBITS, MH>;
+  using L = Layout<WBITS, MH, MODE>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
