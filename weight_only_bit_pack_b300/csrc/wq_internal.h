@@ -74,8 +74,10 @@ cudaError_t launch_prefill(const Problem &p, const Plan &plan, void *ws, cudaStr
 cudaError_t launch_decode(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
 cudaError_t launch_row_prep(const Problem &p, float *rowsum, int8_t *e_row, __half *x16,
                             cudaStream_t s);
-cudaError_t launch_so_prep(const Problem &p, int8_t *e_col, uint32_t *S16, uint32_t *O16,
-                           cudaStream_t s);
+// S16/O16 rows are ld words long (ld >= N; INT4 rows are padded to whole
+// 256-column tiles and stored in the dequant's interleaved column order).
+cudaError_t launch_so_prep(const Problem &p, int64_t ld, int8_t *e_col, uint32_t *S16,
+                           uint32_t *O16, cudaStream_t s);
 cudaError_t launch_epilogue(const Problem &p, const Plan &plan, const void *ws, bool pdl,
                             cudaStream_t s);
 

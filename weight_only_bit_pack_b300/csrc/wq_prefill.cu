@@ -159,23 +159,23 @@ __device__ __forceinline__ uint32_t sub_fma2(uint32_t v, uint32_t c, uint32_t s,
   return r;
 }
 
-// Reads the S16/O16 pairs (both halves hold the value) of CNT consecutive
-// columns, starting at column c of the tile, in group row `row` of the stage's
-// scale/offset rows. Rows past the last group were zero-filled by the copy
-// (callers skip k-rows past K, whose rows may be stale).
-template <int CNT>
-__device__ __forceinline__ void smem_so(uint32_t s_base, uint32_t o_base, bool has_o, int row, int c,
+// Reads the S16/O16 pairs (both halves hold the value) of CNT columns in group
+// row `row` of the stage's scale/offset rows: four columns per 16-byte chunk,
+// chunk q at word w + QSTRIDE * q of the row. Rows past the last group were
+// zero-filled by the copy (callers skip k-rows past K, whose rows may be stale).
+template <int CNT, int QSTRIDE>
+__device__ __forceinline__ void smem_so(uint32_t s_base, uint32_t o_base, bool has_o, int row, int w,
                                         uint32_t (&s2)[CNT], uint32_t (&o2)[CNT]) {
-  const uint32_t off = (uint32_t)(row * BN + c) * 4u;
+  const uint32_t off = (uint32_t)(row * BN + w) * 4u;
 #pragma unroll
   for (int q = 0; q < CNT / 4; ++q) {
     asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(s2[4 * q]), "=r"(s2[4 * q + 1]), "=r"(s2[4 * q + 2]), "=r"(s2[4 * q + 3])
-                 : "r"(s_base + off + 16u * q));
+                 : "r"(s_base + off + 4u * QSTRIDE * q));
     if (has_o)
       asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                    : "=r"(o2[4 * q]), "=r"(o2[4 * q + 1]), "=r"(o2[4 * q + 2]), "=r"(o2[4 * q + 3])
-                   : "r"(o_base + off + 16u * q));
+                   : "r"(o_base + off + 4u * QSTRIDE * q));
     else
       o2[4 * q] = o2[4 * q + 1] = o2[4 * q + 2] = o2[4 * q + 3] = 0u;
   }
@@ -352,8 +352,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             goto ddone;
           if constexpr (MODE == kF16Emu) {
             if (k < a.K) {
-              smem_so<8>(sbase + L::S_OFF + s * L::SO_BYTES, sbase + L::O_OFF + s * L::SO_BYTES,
-                         a.offset != nullptr, (k / a.group - (ks * BK) / a.group), 8 * lane, s2, o2);
+              // columns 8 lane .. 8 lane + 7, stored as words 4 lane .. and 128 + 4 lane ..
+              smem_so<8, 128>(sbase + L::S_OFF + s * L::SO_BYTES, sbase + L::O_OFF + s * L::SO_BYTES,
+                              a.offset != nullptr, (k / a.group - (ks * BK) / a.group), 4 * lane, s2,
+                              o2);
             } else {
 #pragma unroll
               for (int j = 0; j < 8; ++j) s2[j] = o2[j] = 0u;
@@ -404,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int rr = k / a.group - (ks * BK) / a.group;
               const uint32_t sa = sbase + L::S_OFF + s * L::SO_BYTES;
               const uint32_t oa = sbase + L::O_OFF + s * L::SO_BYTES;
-              smem_so<4>(sa, oa, a.offset != nullptr, rr, 4 * lane, s2a, o2a);
-              smem_so<4>(sa, oa, a.offset != nullptr, rr, 4 * (lane + 32), s2b, o2b);
+              smem_so<4, 4>(sa, oa, a.offset != nullptr, rr, 4 * lane, s2a, o2a);
+              smem_so<4, 4>(sa, oa, a.offset != nullptr, rr, 4 * (lane + 32), s2b, o2b);
             } else {
 #pragma unroll
               for (int j = 0; j < 4; ++j) s2a[j] = o2a[j] = s2b[j] = o2b[j] = 0u;
@@ -672,6 +674,12 @@ bool aligned16(const void *p) { return p == nullptr || (reinterpret_cast<uintptr
 
 static uint64_t align256(uint64_t v) { return (v + 255) / 256 * 256; }
 
+// Words per S16/O16 row: INT4 rows are padded to whole n-tiles (their columns
+// are stored in the dequant's interleaved order, see so_prep_kernel).
+static int64_t so_ld(const Problem &p, const Plan &plan) {
+  return p.wbits == 4 ? plan.n_tiles * BN : p.N;
+}
+
 bool prefill_applicable(const Problem &p) {
   if (p.M < 1 || p.N < 1) return false;
   if (p.K % 8 != 0) return false;                       // x1 row stride: 16-byte multiple for TMA
@@ -723,11 +731,12 @@ bool plan_prefill(const Problem &p, Plan &plan) {
     off += align256((uint64_t)p.M);
     plan.ecol_off = off;
     off += align256((uint64_t)p.N);
+    const uint64_t ld = (uint64_t)so_ld(p, plan);
     plan.s16_off = off;
-    off += align256((uint64_t)p.G * p.N * 4);
+    off += align256((uint64_t)p.G * ld * 4);
     if (p.offset) {
       plan.o16_off = off;
-      off += align256((uint64_t)p.G * p.N * 4);
+      off += align256((uint64_t)p.G * ld * 4);
     }
     plan.x16_off = off;
     off += align256((uint64_t)p.M * p.K * 2);
@@ -784,7 +793,7 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
     __half *x16 = reinterpret_cast<__half *>(wsb + plan.x16_off);
     e = launch_row_prep(p, nullptr, e_row, x16, s);
     if (e != cudaSuccess) return e;
-    e = launch_so_prep(p, e_col, S16, O16, s);
+    e = launch_so_prep(p, so_ld(p, plan), e_col, S16, O16, s);
     if (e != cudaSuccess) return e;
     args.e_row = e_row; args.e_col = e_col; args.S16 = S16; args.O16 = O16;
     a_src = x16;
@@ -816,8 +825,9 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
   CUtensorMap tm_s = tm_w, tm_o = tm_w;  // placeholders unless F16EMU
   args.so_bytes = 0;
   if constexpr (MODE == kF16Emu) {
-    const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.G};
-    const cuuint64_t strides[1] = {(cuuint64_t)p.N * 4};
+    const int64_t ld = so_ld(p, plan);
+    const cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)p.G};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
     const cuuint32_t rows = (cuuint32_t)(p.G < SO_ROWS ? p.G : SO_ROWS);
     const cuuint32_t box[2] = {BN, rows};
     const cuuint32_t estr[2] = {1, 1};

@@ -100,7 +100,7 @@ __device__ __forceinline__ uint32_t half_pair(float v) {
 template <int DT>
 __global__ void __launch_bounds__(256)
     so_prep_kernel(const typename Elem<DT>::T *__restrict__ S, const typename Elem<DT>::T *__restrict__ O,
-                   int G, int N, float qmax, int odd16, int8_t *__restrict__ e_col,
+                   int G, int N, int ld, float qmax, int int4, int8_t *__restrict__ e_col,
                    uint32_t *__restrict__ S16, uint32_t *__restrict__ O16) {
   using E = Elem<DT>;
   __shared__ float s_max[8][32];
@@ -134,13 +134,24 @@ __global__ void __launch_bounds__(256)
     s_scale[cx] = exp2i(-e);
   }
   __syncthreads();
-  if (n < N) {
+  // Destination word of column n in a row of ld words. INT4: within each
+  // 256-column tile, column 8l + i goes to word 4l + i (i < 4) or 128 + 4l +
+  // (i - 4), so that the dequant lane l reads its eight columns as two 16-byte
+  // chunks that the warp's lanes take side by side (no bank conflicts); the
+  // rows are padded to whole tiles (ld >= N), the padding holds zeros.
+  int dst = n;
+  if (int4) {
+    const int c = n & 255, l = c >> 3, i = c & 7;
+    dst = (n - c) + (i < 4 ? 4 * l + i : 128 + 4 * l + (i - 4));
+  }
+  if (n < ld) {
     const float sc = s_scale[cx];
-    const float ssc = (odd16 && (n & 1)) ? sc * 0.0625f : sc;  // exact power-of-two factors
+    const float ssc = (int4 && (n & 1)) ? sc * 0.0625f : sc;  // exact power-of-two factors
 #pragma unroll 4
     for (int g = gy; g < G; g += 8) {
-      S16[(int64_t)g * N + n] = half_pair(E::to_f(S[(int64_t)g * N + n]) * ssc);
-      if (O) O16[(int64_t)g * N + n] = half_pair(E::to_f(O[(int64_t)g * N + n]) * sc);
+      const bool live = n < N;
+      S16[(int64_t)g * ld + dst] = live ? half_pair(E::to_f(S[(int64_t)g * N + n]) * ssc) : 0u;
+      if (O) O16[(int64_t)g * ld + dst] = live ? half_pair(E::to_f(O[(int64_t)g * N + n]) * sc) : 0u;
     }
   }
 }
@@ -163,20 +174,20 @@ cudaError_t launch_row_prep(const Problem &p, float *rowsum, int8_t *e_row, __ha
   return cudaGetLastError();
 }
 
-cudaError_t launch_so_prep(const Problem &p, int8_t *e_col, uint32_t *S16, uint32_t *O16,
-                           cudaStream_t s) {
+cudaError_t launch_so_prep(const Problem &p, int64_t ld, int8_t *e_col, uint32_t *S16,
+                           uint32_t *O16, cudaStream_t s) {
   const int N = (int)p.N;
-  const int blocks = (N + 31) / 32;
+  const int blocks = (int)((ld + 31) / 32);
   const float qmax = p.wbits == 4 ? 8.f : 128.f;
-  const int odd16 = p.wbits == 4 ? 1 : 0;
+  const int int4 = p.wbits == 4 ? 1 : 0;
   if (p.dtype == WQ_BF16)
     so_prep_kernel<WQ_BF16><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(p.scale),
                                                    static_cast<const __nv_bfloat16 *>(p.offset),
-                                                   (int)p.G, N, qmax, odd16, e_col, S16, O16);
+                                                   (int)p.G, N, (int)ld, qmax, int4, e_col, S16, O16);
   else
     so_prep_kernel<WQ_F16><<<blocks, 256, 0, s>>>(static_cast<const __half *>(p.scale),
                                                   static_cast<const __half *>(p.offset), (int)p.G,
-                                                  N, qmax, odd16, e_col, S16, O16);
+                                                  N, (int)ld, qmax, int4, e_col, S16, O16);
   return cudaGetLastError();
 }
 
