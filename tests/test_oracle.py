@@ -244,7 +244,8 @@ def test_rmsnorm_unit_rms_as_eps_vanishes():
     x, q, S, O, b, r, gm = _rand_problem(rng, 5, 64, 40, "group", 32)
     for eps in (1e-2, 1e-6, 0.0):
         _, y, no = oracle.matmul_add_rmsnorm(x, q, S, O, b, r, gm, eps, group=32)
-        ms = np.mean(y * y, axis=1)
+        with np.errstate(over="ignore"):  # a planted mistake may blow y up; the check still fails
+            ms = np.mean(y * y, axis=1)
         rms = np.sqrt(np.mean((no / gm) ** 2, axis=1))
         np.testing.assert_allclose(rms, 1.0 / np.sqrt(1.0 + eps / ms), rtol=1e-12)
     np.testing.assert_allclose(rms, 1.0, rtol=1e-12)
