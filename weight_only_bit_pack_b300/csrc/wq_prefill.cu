@@ -517,6 +517,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
+    // Pulls this thread's residual rows of tile t into L2 (4 lines of 128 bytes
+    // per 256-column row), a whole main loop before the y pass reads them, so
+    // the pass does not wait on HBM for every 32-column chunk.
+    auto prefetch_residual = [&](long long t) {
+      if (t >= a.nTiles) return;
+      const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
+      const int n0 = nt * BN;
+#pragma unroll
+      for (int h = 0; h < MH; ++h) {
+        const long long m = (long long)rb * TM + h * BM + rit;
+        if (m >= a.M) break;
+        const char *rowp = reinterpret_cast<const char *>(res + m * a.N + n0);
+        const int bytes = (n0 + BN < a.N ? BN : a.N - n0) * (int)sizeof(T);
+        for (int b = 0; b < bytes; b += 128)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(rowp + b));
+      }
+    };
+    prefetch_residual(blockIdx.x);
     for (long long t = blockIdx.x; t < a.nTiles && ok; t += gridDim.x, ++lt) {
       const int buf = lt % NACC;
       if (!wait_bar_warp(BAR(ACCFULL(buf)), (uint32_t)((lt / NACC) & 1), abort_flag, a.status,
@@ -629,6 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         red_release_add(a.counters + rb, 1u);
       }
       __syncwarp();
+      prefetch_residual(t + gridDim.x);
       if (prev_t >= 0) {
         if (!normalize(prev_t)) {
           ok = false;
