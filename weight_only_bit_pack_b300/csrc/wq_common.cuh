@@ -52,14 +52,6 @@ __device__ __forceinline__ uint4 ld_stream_u4(const void *p) {
   return v;
 }
 
-__device__ __forceinline__ uint2 ld_stream_u2(const void *p) {
-  uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
-               : "=r"(v.x), "=r"(v.y)
-               : "l"(p));
-  return v;
-}
-
 __device__ __forceinline__ void st_stream_u4(void *p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)

@@ -40,36 +40,11 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
-// Same, with acquire at cluster scope, for mbarriers that CTAs of the cluster
-// arrive on remotely.
-__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity,
-                                                 volatile int *abort_flag, uint32_t *status,
-                                                 uint32_t where) {
-  if (sm100::mbar_try_wait_cluster(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-    if (sm100::mbar_try_wait_cluster(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitBudget) {
-      *abort_flag = 1;
-      record_timeout(status, where);
-      return false;
-    }
-  }
-}
-
 // Warp-collective form: every lane polls (each gets the barrier's acquire) and
 // the warp takes one decision, so no lane leaves a loop its warp-mates stay in.
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                               uint32_t *status, uint32_t where) {
   const bool ok = wait_bar(bar, parity, abort_flag, status, where);
-  return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ bool wait_bar_cluster_warp(uint32_t bar, uint32_t parity,
-                                                      volatile int *abort_flag, uint32_t *status,
-                                                      uint32_t where) {
-  const bool ok = wait_bar_cluster(bar, parity, abort_flag, status, where);
   return __all_sync(0xffffffffu, ok);
 }
 
