@@ -232,6 +232,19 @@ int32_t wq_matmul_add_rmsnorm_noalloc(
 int32_t wq_read_device_status(const void *ws, uint64_t ws_bytes, void *stream,
                               int32_t *device_status);
 
+/* Self-check of the device error channel (no counterpart on the pages): one
+ * thread waits, with the library's bounded wait, for an mbarrier phase that
+ * nothing completes; after `budget_cycles` SM clock cycles (clamped to
+ * [1000, 4e9]) the wait gives up and records WQ_ERR_DEVICE_TIMEOUT with place
+ * WQ_WHERE_SELF_CHECK in the status word of `ws`, exactly as an operator kernel
+ * whose wait ran out would, and the kernel exits. Nothing faults and the CUDA
+ * context stays usable; read the word with wq_read_device_status, then zero the
+ * workspace header before the workspace serves an operator call again.
+ * Asynchronous on `stream`. Returns WQ_ERR_NULL, WQ_ERR_WORKSPACE
+ * (ws_bytes < 2048) or WQ_ERR_CUDA. */
+#define WQ_WHERE_SELF_CHECK 31
+int32_t wq_check_device_timeout(void *ws, uint64_t ws_bytes, uint64_t budget_cycles, void *stream);
+
 /* Static description of a status code ("WQ_OK", "WQ_ERR_SHAPE", ...). */
 const char *wq_status_string(int32_t status);
 

@@ -10,7 +10,8 @@ first use of an op raises.
 _API = ("pack_int4", "pack_int4_get_workspace", "matmul_add_rmsnorm",
         "matmul_add_rmsnorm_get_workspace", "WQError", "Status", "Kernel", "lib",
         "read_device_status", "pack_int4_bytes", "select_kernel", "describe", "DType",
-        "matmul_add_rmsnorm_noalloc", "NOALLOC_SCRATCH_BYTES")
+        "matmul_add_rmsnorm_noalloc", "NOALLOC_SCRATCH_BYTES", "check_device_timeout",
+        "WHERE_SELF_CHECK")
 
 
 def __getattr__(name):

@@ -79,6 +79,8 @@ lib.wq_matmul_add_rmsnorm_select_kernel.argtypes = _T
 lib.wq_matmul_add_rmsnorm_noalloc.argtypes = _T + [ctypes.c_void_p]
 lib.wq_read_device_status.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p,
                                       ctypes.POINTER(ctypes.c_int32)]
+lib.wq_check_device_timeout.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint64,
+                                        ctypes.c_void_p]
 lib.wq_status_string.argtypes = [ctypes.c_int32]
 lib.wq_status_string.restype = ctypes.c_char_p
 lib.wq_last_error.argtypes = []
@@ -86,7 +88,8 @@ lib.wq_last_error.restype = ctypes.c_char_p
 for _f in ("wq_pack_int4_get_workspace", "wq_pack_int4", "wq_matmul_add_rmsnorm_get_workspace",
            "wq_matmul_add_rmsnorm", "wq_matmul_add_rmsnorm_get_workspace_ex",
            "wq_matmul_add_rmsnorm_ex", "wq_matmul_add_rmsnorm_select_kernel",
-           "wq_read_device_status", "wq_version", "wq_matmul_add_rmsnorm_noalloc"):
+           "wq_read_device_status", "wq_version", "wq_matmul_add_rmsnorm_noalloc",
+           "wq_check_device_timeout"):
     getattr(lib, _f).restype = ctypes.c_int32
 
 _TORCH2WQ = {torch.float16: DType.F16, torch.bfloat16: DType.BF16, torch.int8: DType.INT8,
@@ -216,6 +219,16 @@ def read_device_status(workspace: torch.Tensor, stream=None) -> int:
     _check(lib.wq_read_device_status(workspace.data_ptr(), workspace.numel(), _stream(stream),
                                      ctypes.byref(st)))
     return st.value
+
+
+WHERE_SELF_CHECK = 31  # WQ_WHERE_SELF_CHECK in include/wq.h
+
+
+def check_device_timeout(workspace: torch.Tensor, budget_cycles: int, stream=None) -> None:
+    """``wq_check_device_timeout``: a bounded device wait that must give up and
+    record WQ_ERR_DEVICE_TIMEOUT in the workspace status word."""
+    _check(lib.wq_check_device_timeout(workspace.data_ptr(), workspace.numel(),
+                                       ctypes.c_uint64(budget_cycles), _stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 8 << 20  # WQ_NOALLOC_SCRATCH_BYTES in include/wq.h

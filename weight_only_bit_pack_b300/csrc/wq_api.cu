@@ -471,4 +471,16 @@ int32_t wq_read_device_status(const void *ws, uint64_t ws_bytes, void *stream,
   return ok();
 }
 
+int32_t wq_check_device_timeout(void *ws, uint64_t ws_bytes, uint64_t budget_cycles,
+                                void *stream) {
+  if (!ws) return fail(WQ_ERR_NULL, "ws is required");
+  if (ws_bytes < kWsHeader) return fail(WQ_ERR_WORKSPACE, "workspace smaller than its header");
+  const uint64_t b = budget_cycles < 1000 ? 1000 : (budget_cycles > 4000000000ull ? 4000000000ull
+                                                                                   : budget_cycles);
+  cudaError_t e = launch_timeout_check(static_cast<uint32_t *>(ws), (long long)b,
+                                       (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "self-check kernel launch");
+  return ok();
+}
+
 }  // extern "C"

@@ -72,6 +72,7 @@ cudaError_t launch_pack_int4(const int32_t *in, uint8_t *out, int64_t K, int64_t
 cudaError_t launch_generic(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
 cudaError_t launch_prefill(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
 cudaError_t launch_decode(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
+cudaError_t launch_timeout_check(uint32_t *status, long long budget, cudaStream_t s);
 cudaError_t launch_row_prep(const Problem &p, float *rowsum, int8_t *e_row, __half *x16,
                             cudaStream_t s);
 // S16/O16 rows are ld words long (ld >= N; INT4 rows are padded to whole

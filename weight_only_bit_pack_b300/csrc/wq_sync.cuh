@@ -26,13 +26,14 @@ __device__ __forceinline__ void record_timeout(uint32_t *status, uint32_t where)
 constexpr uint32_t kSleepNs = 1000000;
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                         uint32_t *status, uint32_t where) {
+                                         uint32_t *status, uint32_t where,
+                                         long long budget = kWaitBudget) {
   if (sm100::mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (sm100::mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitBudget) {
+    if (clock64() - t0 > budget) {
       *abort_flag = 1;
       record_timeout(status, where);
       return false;
