@@ -153,9 +153,11 @@ int32_t wq_matmul_add_rmsnorm_get_workspace(
  *                  no per-call clearing is needed. After a device-side error
  *                  (see wq_read_device_status) zero the header again. The rest
  *                  of the workspace may hold anything on entry.
- * Accumulation is fp32; y feeds the norm unrounded and y/normOut are rounded
- * once to x1's dtype. Results are bitwise identical from run to run for the
- * same arguments (no floating-point atomics; fixed reduction order). */
+ * Accumulation is fp32; the RMS is taken over the unrounded y, and y and normOut
+ * are rounded once to x1's dtype (the large-M kernel scales the y it stored, so
+ * its normOut carries one more rounding of y: at most 2^-9 relative in bf16,
+ * 2^-11 in fp16). Results are bitwise identical from run to run for the same
+ * arguments (no floating-point atomics; fixed reduction order). */
 int32_t wq_matmul_add_rmsnorm(
     const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scale,
     const wq_tensor *offset, const wq_tensor *bias, const wq_tensor *residual,
