@@ -18,8 +18,12 @@ set larger than that is used alone.
 Timing: W eager warm-up steps, then the K timed steps are replayed from a CUDA
 graph (capture of the same C-ABI calls), bracketed by a barrier and a device
 synchronize, timed with CUDA events on the launching stream; max over ranks.
-``e2e`` repeats the K steps eagerly with the step's inputs copied from pinned
-host memory and both outputs copied back inside the timed region.
+``e2e`` repeats the steps with each step's inputs copied from pinned host
+memory and both outputs copied back inside the timed region, captured into
+CUDA graphs with the copies in, the call and the copies out on three streams
+(step i+1's inputs travel while step i computes; event edges keep every input
+set until its call and its outputs have been read), as a serving loop issues
+them; eager calls on one stream if the capture is refused.
 
 Multi-GPU (torchrun): "replicas only" -- each rank runs its own copy of the
 workload, with no collective on the data path; value = all ranks' FLOPs / the
