@@ -7,9 +7,12 @@ INT4/INT8 weights are already resident, as a deployed layer's weights are. The
 INT32 -> INT4 pack runs once per weight; it is timed in the same run and
 reported under "pack".
 
-Default workload: the bf16 decode step, M = 8 (1 x 8) x K 4096 x N 4096, INT4
-per-group g = 128. ``--config`` picks another: tiny, w8a16, prefill,
-sweep:<M>, sweep_pt:<M>.
+Default workload: the largest single-GPU configuration, the M-sweep's
+M = 16384 point (bf16, 16384 x 8192 x 28672, INT4 per-group g = 128).
+``--config`` picks another: tiny, decode, w8a16, prefill, sweep:<M>,
+sweep_pt:<M>. Unless ``--no-extra``, the same line also carries short
+device-timed runs of the other named workloads (decode, prefill, W8A16 and the
+sweep's M = 1 and 16) under "workloads".
 
 L2: every step uses the next of R distinct input sets (weights included) whose
 total size exceeds twice the L2 size, so no step finds its weights in L2; a
@@ -59,11 +62,12 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="decode")
+    ap.add_argument("--config", default="sweep:16384")
     ap.add_argument("--kernel", choices=["auto", "generic", "decode", "prefill"], default="auto")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pack", action="store_true")
+    ap.add_argument("--no-extra", action="store_true")
     return ap.parse_args()
 
 
@@ -81,6 +85,8 @@ def make_problem(config: str, device):
 
 
 def default_steps(config: str) -> int:
+    if config in ("sweep:16384", "sweep_pt:16384"):
+        return 30
     return {"tiny": 2000, "decode": 20000, "w8a16": 200, "prefill": 40}.get(
         config, 20000 if config.endswith(":1") or config.endswith(":16") else 100)
 
@@ -294,6 +300,145 @@ def cpu_baseline(p, seconds=10.0, max_reps=200):
 
 # ------------------------------------------------------------------ our arm
 
+class Runner:
+    """R distinct input sets of one workload on the device (weights packed once,
+    then copied), a zeroed workspace, and step(i) = one C-ABI call on set i % R."""
+
+    def __init__(self, wq, p, kernel, dev, stream):
+        self.p, self.kernel, self.stream = p, kernel, stream
+        self.w_src = p.x2
+        self.w0 = wq.pack_int4(p.x2) if p.wbits == 4 else p.x2.contiguous()
+        self.ab = alg_bytes(p)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.set_bytes = self.ab["total"]
+        R = 1 if self.set_bytes > 2 * l2 else int(math.ceil(2 * l2 / self.set_bytes)) + 1
+        self.R = max(1, min(R, 64))
+        self.sets = []
+        for i in range(self.R):
+            s = {"x1": p.x1.clone(), "w": self.w0.clone(), "scale": p.scale.clone(),
+                 "offset": None if p.offset is None else p.offset.clone(),
+                 "bias": None if p.bias is None else p.bias.clone(),
+                 "residual": p.residual.clone(), "gamma": p.gamma.clone(),
+                 "y": torch.empty_like(p.residual), "normOut": torch.empty_like(p.residual)}
+            self.sets.append(s)
+        ws_bytes = wq.matmul_add_rmsnorm_get_workspace(p.x1, self.w0, p.scale, p.offset, p.bias,
+                                                       p.residual, p.gamma, p.eps, p.group,
+                                                       kernel=kernel)
+        self.ws = torch.zeros(max(ws_bytes, 2048), dtype=torch.uint8, device=dev)  # header zeroed once
+        self.chosen = int(wq.select_kernel(p.x1, self.w0, p.scale, p.offset, p.bias, p.residual,
+                                           p.gamma, p.eps, p.group)) if kernel == 0 else kernel
+        self.wq = wq
+
+    def step(self, i):
+        s, p = self.sets[i % self.R], self.p
+        self.wq.matmul_add_rmsnorm(s["x1"], s["w"], s["scale"], s["offset"], s["bias"],
+                                   s["residual"], s["gamma"], p.eps, p.group, y=s["y"],
+                                   normOut=s["normOut"], workspace=self.ws, kernel=self.kernel,
+                                   stream=self.stream)
+
+    def kernels_per_call(self) -> int:
+        """Our kernel launches per call: generic = matmul + epilogue; decode = one;
+        prefill = the tcgen05 kernel plus its row pre-pass (per-group scales, or an
+        offset) and its scale pre-pass (per-group scales)."""
+        p = self.p
+        if self.chosen == 3:
+            return 1 + (1 if (p.group or p.offset is not None) else 0) + (1 if p.group else 0)
+        return {1: 2, 2: 1}.get(self.chosen, 2)
+
+    def l2_note(self) -> str:
+        if self.R > 1:
+            return f"rotating {self.R} distinct input sets, {self.R * self.set_bytes / 1e6:.0f} MB > 2x L2"
+        return f"one input set of {self.set_bytes / 1e6:.0f} MB > 2x L2"
+
+
+def capture_graphs(runner, K):
+    """The K steps captured into CUDA graphs (chunks of at most 1000 calls)."""
+    graphs, done = [], 0
+    while done < K:
+        n = min(1000, K - done)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=runner.stream):
+            for i in range(done, done + n):
+                runner.step(i)
+        graphs.append(g)
+        done += n
+    return graphs
+
+
+def roofline(p, ms_step, peaks):
+    ab = alg_bytes(p)
+    t_s = ms_step * 1e-3
+    flops = 2.0 * p.M * p.K * p.N
+    if ab["total"] / (peaks["hbm_gbs"] * 1e9) >= flops / (peaks["bf16_tflops"] * 1e12):
+        roof = {"bound": "hbm", "achieved": ab["total"] / t_s / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / t_s / 1e12, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    return roof
+
+
+def time_extra(wq, config, dev, stream, steps, warmup, peaks):
+    """Device time of one named workload (graph replay, CUDA events), for the
+    line's "workloads" key."""
+    p = make_problem(config, dev)
+    r = Runner(wq, p, 0, dev, stream)
+    for i in range(warmup):
+        r.step(i)
+    graphs = capture_graphs(r, steps)
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for g in graphs:
+        g.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = ev0.elapsed_time(ev1) / steps
+    roof = roofline(p, ms, peaks)
+    out = {"workload": p.name, "M": p.M, "K": p.K, "N": p.N, "kernel":
+           ["auto", "generic", "decode", "prefill"][r.chosen], "steps": steps, "ms_per_step": ms,
+           "TFLOP/s": 2.0 * p.M * p.K * p.N / (ms * 1e-3) / 1e12,
+           "weight_GBps": r.ab["weight"] / (ms * 1e-3) / 1e9,
+           "roofline_bound": roof["bound"], "roofline_frac": roof["frac"], "l2": r.l2_note()}
+    del graphs, r, p
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return out
+
+
+EXTRA = (("decode", 2000), ("sweep:1", 1000), ("sweep:16", 1000), ("w8a16", 50), ("prefill", 20))
+
+
+def traffic_record(kernel_name, workload):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary
+    (profiles/traffic.md), or None when no capture matches this workload or the
+    kernel's source has changed since the capture (sha256 of its .cu file)."""
+    import hashlib
+    import re
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    for m in re.finditer(r"^traffic: (.*)$", text, flags=re.M):
+        kv = dict(x.split("=", 1) for x in m.group(1).split())
+        if kv.get("kernel") != kernel_name or kv.get("workload") != workload:
+            continue
+        src = os.path.join(ROOT, "weight_only_bit_pack_b300", "csrc", kv.get("source", ""))
+        try:
+            sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        except OSError:
+            return None
+        if sha != kv.get("source_sha"):
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    return None
+
+
 def run_ours(args, world, rank, local):
     import weight_only_bit_pack_b300 as wq
     from weight_only_bit_pack_b300 import build as wqbuild
@@ -306,54 +451,17 @@ def run_ours(args, world, rank, local):
 
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.set_stream(stream)
-    # one packed weight, then R distinct copies of every input
-    w_src = p.x2
-    if p.wbits == 4:
-        w0 = wq.pack_int4(w_src)
-    else:
-        w0 = w_src.contiguous()
-    ab = alg_bytes(p)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    set_bytes = ab["total"]
-    R = 1 if set_bytes > 2 * l2 else int(math.ceil(2 * l2 / set_bytes)) + 1
-    R = max(1, min(R, 64))
-    sets = []
-    for i in range(R):
-        s = {"x1": p.x1.clone(), "w": w0.clone(), "scale": p.scale.clone(),
-             "offset": None if p.offset is None else p.offset.clone(),
-             "bias": None if p.bias is None else p.bias.clone(), "residual": p.residual.clone(),
-             "gamma": p.gamma.clone(), "y": torch.empty_like(p.residual),
-             "normOut": torch.empty_like(p.residual)}
-        sets.append(s)
-    ws_bytes = wq.matmul_add_rmsnorm_get_workspace(p.x1, w0, p.scale, p.offset, p.bias,
-                                                   p.residual, p.gamma, p.eps, p.group,
-                                                   kernel=kernel)
-    ws = torch.zeros(max(ws_bytes, 2048), dtype=torch.uint8, device=dev)  # header zeroed once
-    chosen = int(wq.select_kernel(p.x1, w0, p.scale, p.offset, p.bias, p.residual, p.gamma, p.eps,
-                                  p.group)) if kernel == 0 else kernel
-
-    def step(i):
-        s = sets[i % R]
-        wq.matmul_add_rmsnorm(s["x1"], s["w"], s["scale"], s["offset"], s["bias"], s["residual"],
-                              s["gamma"], p.eps, p.group, y=s["y"], normOut=s["normOut"],
-                              workspace=ws, kernel=kernel, stream=stream)
+    runner = Runner(wq, p, kernel, dev, stream)
+    w_src, w0, ab, R, sets = runner.w_src, runner.w0, runner.ab, runner.R, runner.sets
+    chosen = runner.chosen
+    step = runner.step
 
     for i in range(W):
         step(i)
     torch.cuda.synchronize(dev)
 
     # capture the K timed steps (in chunks so a graph stays small), replay once untimed
-    chunk = min(K, 1000)
-    graphs = []
-    done = 0
-    while done < K:
-        n = min(chunk, K - done)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(done, done + n):
-                step(i)
-        graphs.append(g)
-        done += n
+    graphs = capture_graphs(runner, K)
     for g in graphs:
         g.replay()
     torch.cuda.synchronize(dev)
@@ -375,6 +483,7 @@ def run_ours(args, world, rank, local):
     flops = 2.0 * p.M * p.K * p.N
     tflops = flops / (ms_step * 1e-3) / 1e12 * world
     w_gbs = ab["weight"] / (ms_step * 1e-3) / 1e9
+    del graphs
 
     # end-to-end: pinned host inputs -> device, call, outputs -> pinned host
     e2e = None
@@ -509,31 +618,21 @@ def run_ours(args, world, rank, local):
                 "bit_exact": bool(torch.equal(out, w0))}
 
     peaks, peak_src = load_peaks()
-    t_s = ms_step * 1e-3
-    bound_time_hbm = ab["total"] / (peaks["hbm_gbs"] * 1e9)
-    bound_time_tc = flops / (peaks["bf16_tflops"] * 1e12)
-    if bound_time_hbm >= bound_time_tc:
-        roof = {"bound": "hbm", "achieved": ab["total"] / t_s / 1e9, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s"}
-    else:
-        roof = {"bound": "tensor", "achieved": flops / t_s / 1e12, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof = roofline(p, ms_step, peaks)
+    # the dominant kernel's DRAM bytes per launch, from the committed ncu capture
+    kname = {3: "prefill_kernel", 2: "decode_kernel"}.get(chosen, "generic_gemm_kernel")
+    roof["traffic"] = traffic_record(kname, p.name)
+    roof["traffic_source"] = ("profiles/traffic.md (ncu dram__bytes_read.sum + "
+                              "dram__bytes_write.sum of one launch)"
+                              if roof["traffic"] is not None else
+                              "none: no capture of this kernel source on this workload")
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else \
         "fallback 6.4 TB/s / 1.8 PFLOP/s"
-    roof["kernel"] = ("the operator's launches of one step (matmul + epilogue), "
+    roof["kernel"] = (f"{kname}: achieved over the whole call (its pre-pass launches included), "
                       f"kernel choice {['auto', 'generic', 'decode', 'prefill'][chosen]}")
     roof["alg_bytes_per_launch"] = ab["total"]
     roof["flops_per_launch"] = flops
 
-    # our kernels per call: generic = matmul + epilogue; decode = one kernel;
-    # prefill = the tcgen05 kernel plus its row pre-pass (per-group scales, or
-    # an offset) and its scale pre-pass (per-group scales)
-    if chosen == 3:
-        kernels_per_call = 1 + (1 if (p.group or p.offset is not None) else 0) + (1 if p.group else 0)
-    else:
-        kernels_per_call = {1: 2, 2: 1}.get(chosen, 2)
     line = {
         "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -542,14 +641,13 @@ def run_ours(args, world, rank, local):
         "config": {"workload": p.name, "M": p.M, "K": p.K, "N": p.N, "wbits": p.wbits,
                    "group": p.group, "offset": p.offset is not None, "bias": p.bias is not None,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": (f"rotating {R} distinct input sets, {R * set_bytes / 1e6:.0f} MB > 2x L2"
-                          if R > 1 else f"one input set of {set_bytes / 1e6:.0f} MB > 2x L2"),
+                   "l2": runner.l2_note(),
                    "timing": "CUDA graph replay of the K steps, CUDA events on the launch stream",
                    "kernel": ["auto", "generic", "decode", "prefill"][chosen]},
         "weight_GBps": w_gbs,
         "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": K * kernels_per_call,
+        "gpu_launches": K * runner.kernels_per_call(),
         "pack": pack,
     }
     if rank == 0:
@@ -558,6 +656,17 @@ def run_ours(args, world, rank, local):
             line["cpu_baseline"] = cpu_baseline(p)
         elif not args.no_cpu_baseline:
             line["cpu_baseline"] = None
+    if not args.no_extra and world == 1:
+        del runner, sets, w0, p
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        extras = []
+        for cfg, n in EXTRA:
+            if cfg == args.config:
+                continue
+            extras.append(time_extra(wq, cfg, dev, stream, n, W, peaks))
+        line["workloads"] = extras
+    if rank == 0:
         print(json.dumps(line), flush=True)
 
 

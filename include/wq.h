@@ -206,9 +206,9 @@ int32_t wq_matmul_add_rmsnorm_select_kernel(
  *   - A problem whose workspace (as wq_matmul_add_rmsnorm_get_workspace
  *     reports it) exceeds WQ_NOALLOC_SCRATCH_BYTES is rejected with
  *     WQ_ERR_WORKSPACE before anything is enqueued.
- *   - The first call on each device looks up that device's address of the
- *     array (cudaGetSymbolAddress with the device current); make that first
- *     call before any stream capture.
+ *   - The first call in each CUDA context (in practice: on each device) looks
+ *     up that context's address of the array (cudaGetSymbolAddress with the
+ *     device current); make that first call before any stream capture.
  *   - All calls share the one array per device and it keeps the last call's
  *     contents (each call clears the part that must start at zero). Calls whose
  *     work overlaps on the GPU -- on different streams or from different host
@@ -220,6 +220,14 @@ int32_t wq_matmul_add_rmsnorm_noalloc(
     const wq_tensor *offset, const wq_tensor *bias, const wq_tensor *residual,
     const wq_tensor *gamma, double eps, int64_t group,
     const wq_tensor *y, const wq_tensor *normOut, void *stream);
+
+/* Device status word of the no-alloc scratch of the current device, as
+ * wq_read_device_status gives it for a workspace: synchronizes `stream`, copies
+ * the word to the host and stores it in *device_status (0 = no device-side
+ * error). Read it after a wq_matmul_add_rmsnorm_noalloc call and before the
+ * next one, which clears it. Returns WQ_ERR_NULL or WQ_ERR_CUDA on failure.
+ * (No counterpart on the pages, like the entry point it serves.) */
+int32_t wq_noalloc_read_device_status(void *stream, int32_t *device_status);
 
 /* ------------------------------------------------------------------ status */
 
@@ -246,6 +254,22 @@ int32_t wq_read_device_status(const void *ws, uint64_t ws_bytes, void *stream,
  * (ws_bytes < 2048) or WQ_ERR_CUDA. */
 #define WQ_WHERE_SELF_CHECK 31
 int32_t wq_check_device_timeout(void *ws, uint64_t ws_bytes, uint64_t budget_cycles, void *stream);
+
+/* Test hook of the device error channel (no counterpart on the pages). For
+ * every later launch in this process, the operator kernels' waits for other
+ * thread blocks -- the decode kernel's grid-wide counter (place
+ * WQ_WHERE_DECODE_GRID) and the prefill kernel's row-block counters (place
+ * WQ_WHERE_PREFILL_ROW_BLOCK) -- give up after `budget_cycles` SM clock cycles
+ * (in [1000, 4e9]) and wait for `extra_arrivals` (<= 2^20) more arrivals than
+ * the kernel makes. With extra_arrivals > 0 every such wait runs out: the
+ * kernel records WQ_ERR_DEVICE_TIMEOUT | place << 8 in the status word, writes
+ * no normOut, drains its copies and MMAs, frees its tensor memory and exits; the
+ * call itself returns WQ_OK. (0, 0) restores the defaults (about 2 s, no extra
+ * arrivals). Process-wide and not thread-safe with respect to calls in flight:
+ * for tests only. Returns WQ_ERR_SHAPE for values out of range. */
+#define WQ_WHERE_PREFILL_ROW_BLOCK 5
+#define WQ_WHERE_DECODE_GRID 15
+int32_t wq_test_set_wait_limits(uint64_t budget_cycles, uint32_t extra_arrivals);
 
 /* Static description of a status code ("WQ_OK", "WQ_ERR_SHAPE", ...). */
 const char *wq_status_string(int32_t status);

@@ -80,3 +80,24 @@ def compare(prob, y, no, ref, rows=None, tol=None):
                                f"worst {out[name]:.3e} at {tuple(bad[0])}: gpu {g[tuple(bad[0])]} "
                                f"ref {r[tuple(bad[0])]}")
     return out
+
+
+def compare_nonfinite(prob, y, no, ref, tol=None):
+    """Comparison for inputs that hold NaN or Inf (IEEE propagation). Where the
+    oracle's value is finite the GPU's must be finite and within the tolerance;
+    where the oracle's is NaN the GPU's must be NaN; where it is +-Inf the GPU's
+    must be the same infinity or NaN (the kernels add the dequantized weight's
+    terms in an exact but different order, which can turn an Inf into NaN)."""
+    tol = TOL[prob.dtype] if tol is None else tol
+    _, ry, rn = ref
+    for name, g, r in (("y", y, ry), ("normOut", no, rn)):
+        g = g.reshape(-1, prob.N).double().cpu().numpy()
+        fin_r, fin_g = np.isfinite(r), np.isfinite(g)
+        bad = np.argwhere(fin_r != fin_g)
+        assert bad.size == 0, (f"{prob.name} {name}: finiteness differs at {tuple(bad[0])}: gpu "
+                               f"{g[tuple(bad[0])]} ref {r[tuple(bad[0])]}")
+        assert np.isnan(g[np.isnan(r)]).all(), f"{prob.name} {name}: a NaN of the oracle is not NaN"
+        inf = np.isinf(r)
+        assert (np.isnan(g[inf]) | (g[inf] == r[inf])).all(), f"{prob.name} {name}: Inf differs"
+        err = np.abs(g[fin_r] - r[fin_r]) / (1.0 + np.abs(r[fin_r]))
+        assert err.size == 0 or err.max() <= tol, f"{prob.name} {name}: worst {err.max():.3e}"

@@ -21,11 +21,23 @@ pytestmark = pytest.mark.gpu
 GENERIC, DECODE, PREFILL = 1, 2, 3
 
 
+# Oracle results of the large named workloads, kept for the test session so
+# that each workload's oracle runs once for all the kernels checked on it.
+_ORACLE_CACHE = {}
+
+
 def _check(wq, prob, kernel, n_sample=None):
     y, no = run_gpu(wq, prob, kernel)
     rows = None if n_sample is None else sample_rows(prob.M, n_sample)
-    ref = run_oracle(prob, rows)
-    return compare(prob, y, no, ref, rows)
+    key = (prob.name, None if rows is None else tuple(int(r) for r in rows))
+    if key not in _ORACLE_CACHE:
+        _ORACLE_CACHE[key] = run_oracle(prob, rows)
+    return compare(prob, y, no, _ORACLE_CACHE[key], rows)
+
+
+# rows compared on the large workloads: a seeded sample of 512 plus the first
+# and the last row (rows are independent, so every sampled row is checked in full)
+N_SAMPLE = 512
 
 
 # ------------------------------------------------------------------ named workloads
@@ -55,21 +67,22 @@ def test_decode(wq, kernel):
 
 @pytest.mark.parametrize("kernel", [0, GENERIC, PREFILL])
 def test_w8a16(wq, kernel):
-    _check(wq, inputs.w8a16("cuda"), kernel, n_sample=48)
+    """Every element of the 2048 x 11008 output."""
+    _check(wq, inputs.w8a16("cuda"), kernel)
 
 
 @pytest.mark.parametrize("kernel", [0, PREFILL])
 def test_prefill_workload(wq, kernel):
-    _check(wq, inputs.prefill("cuda"), kernel, n_sample=48)
+    _check(wq, inputs.prefill("cuda"), kernel, n_sample=N_SAMPLE)
 
 
 @pytest.mark.parametrize("M", inputs.SWEEP_M)
 def test_sweep(wq, M):
-    _check(wq, inputs.sweep(M, device="cuda"), 0, n_sample=24)
+    _check(wq, inputs.sweep(M, device="cuda"), 0, n_sample=N_SAMPLE)
 
 
 def test_sweep_per_tensor(wq):
-    _check(wq, inputs.sweep(4096, per_tensor=True, device="cuda"), 0, n_sample=24)
+    _check(wq, inputs.sweep(4096, per_tensor=True, device="cuda"), 0, n_sample=N_SAMPLE)
 
 
 PREFILL_EDGE = [

@@ -11,7 +11,8 @@ _API = ("pack_int4", "pack_int4_get_workspace", "matmul_add_rmsnorm",
         "matmul_add_rmsnorm_get_workspace", "WQError", "Status", "Kernel", "lib",
         "read_device_status", "pack_int4_bytes", "select_kernel", "describe", "DType",
         "matmul_add_rmsnorm_noalloc", "NOALLOC_SCRATCH_BYTES", "check_device_timeout",
-        "WHERE_SELF_CHECK")
+        "WHERE_SELF_CHECK", "noalloc_read_device_status", "set_wait_limits_for_testing",
+        "WHERE_PREFILL_ROW_BLOCK", "WHERE_DECODE_GRID", "HEADER_BYTES")
 
 
 def __getattr__(name):

@@ -81,6 +81,8 @@ lib.wq_read_device_status.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c
                                       ctypes.POINTER(ctypes.c_int32)]
 lib.wq_check_device_timeout.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_uint64,
                                         ctypes.c_void_p]
+lib.wq_noalloc_read_device_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
+lib.wq_test_set_wait_limits.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
 lib.wq_status_string.argtypes = [ctypes.c_int32]
 lib.wq_status_string.restype = ctypes.c_char_p
 lib.wq_last_error.argtypes = []
@@ -89,7 +91,7 @@ for _f in ("wq_pack_int4_get_workspace", "wq_pack_int4", "wq_matmul_add_rmsnorm_
            "wq_matmul_add_rmsnorm", "wq_matmul_add_rmsnorm_get_workspace_ex",
            "wq_matmul_add_rmsnorm_ex", "wq_matmul_add_rmsnorm_select_kernel",
            "wq_read_device_status", "wq_version", "wq_matmul_add_rmsnorm_noalloc",
-           "wq_check_device_timeout"):
+           "wq_check_device_timeout", "wq_noalloc_read_device_status", "wq_test_set_wait_limits"):
     getattr(lib, _f).restype = ctypes.c_int32
 
 _TORCH2WQ = {torch.float16: DType.F16, torch.bfloat16: DType.BF16, torch.int8: DType.INT8,
@@ -186,13 +188,18 @@ def select_kernel(x1, x2, scale, offset, bias, residual, gamma, eps, group=0) ->
 def matmul_add_rmsnorm(x1, x2, scale, offset, bias, residual, gamma, eps: float, group: int = 0,
                        y: Optional[torch.Tensor] = None, normOut: Optional[torch.Tensor] = None,
                        workspace: Optional[torch.Tensor] = None, kernel: int = Kernel.AUTO,
-                       stream=None):
+                       stream=None, check_status: bool = False):
     """Fused ``y = x1 @ (x2*scale + offset) + bias + residual``,
     ``normOut = y / sqrt(mean(y^2) + eps) * gamma`` (``wq_matmul_add_rmsnorm``).
 
     Outputs and workspace are allocated with torch when not given (a given
     workspace must have had its first 2048 bytes zeroed once). Pass
     ``y=residual`` for the in-place variant. Returns ``(y, normOut)``.
+
+    ``check_status=True`` waits for the call and reads the workspace's device
+    status word: if a device-side wait gave up, the header is zeroed again (so
+    the workspace can serve the next call) and :class:`WQError` with
+    ``ERR_DEVICE_TIMEOUT`` is raised, naming the place that gave up.
     """
     if y is None:
         y = torch.empty_like(residual)
@@ -211,7 +218,17 @@ def matmul_add_rmsnorm(x1, x2, scale, offset, bias, residual, gamma, eps: float,
     _check(lib.wq_matmul_add_rmsnorm_ex(*refs[:7], float(eps), int(group), refs[7], refs[8],
                                         int(kernel), workspace.data_ptr(), workspace.numel(),
                                         _stream(stream)))
+    if check_status:
+        st = read_device_status(workspace, stream)
+        if st != 0:
+            workspace[:HEADER_BYTES].zero_()
+            torch.cuda.synchronize(workspace.device)
+            raise WQError(st & 0xFF, f"device status word 0x{st:x}: the bounded wait at place "
+                                     f"{st >> 8} gave up; y and normOut are incomplete")
     return y, normOut
+
+
+HEADER_BYTES = 2048  # the workspace header of include/wq.h
 
 
 def read_device_status(workspace: torch.Tensor, stream=None) -> int:
@@ -232,6 +249,23 @@ def check_device_timeout(workspace: torch.Tensor, budget_cycles: int, stream=Non
 
 
 NOALLOC_SCRATCH_BYTES = 8 << 20  # WQ_NOALLOC_SCRATCH_BYTES in include/wq.h
+WHERE_PREFILL_ROW_BLOCK = 5       # WQ_WHERE_PREFILL_ROW_BLOCK
+WHERE_DECODE_GRID = 15            # WQ_WHERE_DECODE_GRID
+
+
+def noalloc_read_device_status(stream=None) -> int:
+    """``wq_noalloc_read_device_status``: the no-alloc scratch's status word
+    (synchronizes the stream); read it before the next no-alloc call clears it."""
+    st = ctypes.c_int32(0)
+    _check(lib.wq_noalloc_read_device_status(_stream(stream), ctypes.byref(st)))
+    return st.value
+
+
+def set_wait_limits_for_testing(budget_cycles: int, extra_arrivals: int) -> None:
+    """``wq_test_set_wait_limits``: for tests of the device error channel only.
+    (0, 0) restores the defaults."""
+    _check(lib.wq_test_set_wait_limits(ctypes.c_uint64(budget_cycles),
+                                       ctypes.c_uint32(extra_arrivals)))
 
 
 def matmul_add_rmsnorm_noalloc(x1, x2, scale, offset, bias, residual, gamma, eps: float,

@@ -10,6 +10,7 @@
 // (ceil(k/group), n), offset shaped like scale, group in [32, k-1] and a
 // multiple of 32. The INT4 storage rule (last dimension even) is the one of
 // aclnnDynamicQuant, "Constraints".
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -19,11 +20,16 @@
 #include <vector>
 
 #include "wq_internal.h"
+#include "wq_sync.cuh"
 
 namespace wq {
 namespace {
 
 thread_local std::string g_last_error;
+
+// Wait limits of the operator kernels' cross-CTA waits (wq_test_set_wait_limits).
+std::atomic<long long> g_wait_budget{kWaitBudget};
+std::atomic<uint32_t> g_wait_extra{0};
 
 int32_t fail(int32_t code, const char *fmt, ...) {
   char buf[512];
@@ -275,6 +281,9 @@ int32_t cuda_fail(cudaError_t e, const char *what) {
 
 }  // namespace
 
+long long wait_budget() { return g_wait_budget.load(std::memory_order_relaxed); }
+uint32_t wait_extra_arrivals() { return g_wait_extra.load(std::memory_order_relaxed); }
+
 void set_last_error(int32_t code, const char *msg) {
   if (code == WQ_OK)
     g_last_error.clear();
@@ -480,6 +489,21 @@ int32_t wq_check_device_timeout(void *ws, uint64_t ws_bytes, uint64_t budget_cyc
   cudaError_t e = launch_timeout_check(static_cast<uint32_t *>(ws), (long long)b,
                                        (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "self-check kernel launch");
+  return ok();
+}
+
+int32_t wq_test_set_wait_limits(uint64_t budget_cycles, uint32_t extra_arrivals) {
+  if (budget_cycles == 0 && extra_arrivals == 0) {
+    g_wait_budget.store(kWaitBudget);
+    g_wait_extra.store(0);
+    return ok();
+  }
+  if (budget_cycles < 1000 || budget_cycles > (uint64_t)kWaitBudget)
+    return fail(WQ_ERR_SHAPE, "budget_cycles must lie in [1000, %lld]", (long long)kWaitBudget);
+  if (extra_arrivals > (1u << 20))
+    return fail(WQ_ERR_SHAPE, "extra_arrivals must be at most 2^20");
+  g_wait_budget.store((long long)budget_cycles);
+  g_wait_extra.store(extra_arrivals);
   return ok();
 }
 

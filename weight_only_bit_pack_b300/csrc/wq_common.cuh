@@ -69,4 +69,16 @@ __device__ __forceinline__ uint32_t sub2(uint32_t v, uint32_t c) {
   return r;
 }
 
+// 2^e as an fp32 for e in [-126, 127].
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// v * 2^e for e in [-252, 254], in two exact power-of-two steps (the result
+// rounds only where it leaves the fp32 normal range).
+__device__ __forceinline__ float scale_pow2(float v, int e) {
+  const int a = e < -126 ? -126 : (e > 127 ? 127 : e);
+  int b = e - a;
+  b = b < -126 ? -126 : (b > 127 ? 127 : b);
+  return v * exp2i(a) * exp2i(b);
+}
+
 }  // namespace wq

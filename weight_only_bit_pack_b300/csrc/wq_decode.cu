@@ -141,6 +141,8 @@ struct DecodeArgs {
   int M, K, N, group, Ns, so_rows;
   int nTiles, kst, U, per, G, SMAX, npf;
   float eps;
+  long long budget;   // cycles the grid barrier waits before it gives up
+  uint32_t extra;     // arrivals the grid barrier waits for beyond G (0; > 0 only in tests)
   int NS;                                      // ring depth
   uint32_t slot, off_x, off_s, off_o, off_red, off_misc, off_bar;  // shared-memory layout
 };
@@ -564,9 +566,9 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
   if (ctid == 0) {
     red_release_add(a.gbar, 1u);
     const long long t0 = clock64();
-    while (ld_acquire_u32(a.gbar) < (uint32_t)a.G) {
+    while (ld_acquire_u32(a.gbar) < (uint32_t)a.G + a.extra) {
       if (*abort_flag) break;
-      if (clock64() - t0 > kWaitBudget) {
+      if (clock64() - t0 > a.budget) {
         *abort_flag = 1;
         record_timeout(a.status, kDWhereGrid);
         break;
@@ -589,7 +591,8 @@ __global__ void __launch_bounds__(DCfg<MT>::THREADS, 1)
       atomicExch(a.gbar + 1, 0u);
     }
   }
-  for (int f = 0; f < nfin && f < 4; ++f) {
+  // a CTA whose wait gave up (or whose producers did) writes no normOut
+  for (int f = 0; f < nfin && f < 4 && !*abort_flag; ++f) {
     const int tile = fin_tiles[f];
     for (int q = ctid; q < MP * DNT / 4; q += CT) {
       const int m = q / (DNT / 4), col = 4 * (q - m * (DNT / 4));
@@ -776,6 +779,8 @@ static cudaError_t launch_decode_t(const Problem &p, const Plan &plan, void *ws,
   args.SMAX = gm.SMAX;
   args.npf = gm.per < 16 ? gm.per : 16;
   args.eps = p.eps;
+  args.budget = wait_budget();
+  args.extra = wait_extra_arrivals();
   args.NS = L.NS;
   args.slot = L.slot; args.off_x = L.off_x; args.off_s = L.off_s; args.off_o = L.off_o;
   args.off_red = L.off_red; args.off_misc = L.off_misc; args.off_bar = L.off_bar;

@@ -73,14 +73,19 @@ cudaError_t launch_generic(const Problem &p, const Plan &plan, void *ws, cudaStr
 cudaError_t launch_prefill(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
 cudaError_t launch_decode(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
 cudaError_t launch_timeout_check(uint32_t *status, long long budget, cudaStream_t s);
-cudaError_t launch_row_prep(const Problem &p, float *rowsum, int8_t *e_row, __half *x16,
+cudaError_t launch_row_prep(const Problem &p, float *rowsum, int16_t *e_row, __half *x16,
                             cudaStream_t s);
 // S16/O16 rows are ld words long (ld >= N; INT4 rows are padded to whole
 // 256-column tiles and stored in the dequant's interleaved column order).
-cudaError_t launch_so_prep(const Problem &p, int64_t ld, int8_t *e_col, uint32_t *S16,
+cudaError_t launch_so_prep(const Problem &p, int64_t ld, int16_t *e_col, uint32_t *S16,
                            uint32_t *O16, cudaStream_t s);
 cudaError_t launch_epilogue(const Problem &p, const Plan &plan, const void *ws, bool pdl,
                             cudaStream_t s);
+
+// Budget (clock cycles) and extra target of the kernels' waits for other
+// thread blocks: kWaitBudget and 0 unless wq_test_set_wait_limits changed them.
+long long wait_budget();
+uint32_t wait_extra_arrivals();
 
 // Sets the thread-local message that wq_last_error() returns.
 void set_last_error(int32_t code, const char *msg);

@@ -13,10 +13,17 @@
 // The array is a file-scope __device__ variable: every GPU that loads this
 // library holds WQ_NOALLOC_SCRATCH_BYTES for it until the process exits. In
 // host code its name is only a host-side stand-in, not a device address, so the
-// device address is looked up with cudaGetSymbolAddress once per device, with
-// that device current, on the first call made on it; that first call should
-// therefore come before any stream capture. No cudaMalloc, cudaFree or other
-// allocating routine is called.
+// device address is looked up with cudaGetSymbolAddress once per CUDA context
+// (in practice once per device), with that device current, on the first call
+// made in it; that first call should therefore come before any stream capture.
+// No cudaMalloc, cudaFree or other allocating routine is called.
+//
+// Device-side errors of these calls (a bounded wait that gave up) land in the
+// array's status word; wq_noalloc_read_device_status reads it. The next
+// no-alloc call on the device clears it again.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cstdio>
 #include <mutex>
 
@@ -28,42 +35,81 @@ constexpr uint64_t kScratchBytes = WQ_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-struct DeviceScratch {
-  int device;
+// The array's device address belongs to the module loaded in one CUDA
+// context: a device reset (or another context on the same device) loads the
+// module again, possibly elsewhere. The cache is therefore keyed by the
+// current context's unique id (cuCtxGetId), not by the device number.
+struct ContextScratch {
+  unsigned long long ctx_id;
   void *ptr;
 };
 
 std::mutex g_scratch_mu;
-DeviceScratch g_scratch_tab[256];
-int g_scratch_n = 0;
+constexpr int kCacheSlots = 64;
+ContextScratch g_scratch_tab[kCacheSlots];
+int g_scratch_n = 0, g_scratch_next = 0;
 
-// Device address of g_noalloc_scratch on the current device (set-up on first use).
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+template <typename Fn>
+Fn driver_fn(const char *name) {
+  void *p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<Fn>(p);
+  cudaGetLastError();
+  return nullptr;
+}
+
+// Unique id of the calling thread's current context, or 0 if there is none yet.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+int32_t cuda_error(cudaError_t e, const char *what) {
+  char msg[200];
+  snprintf(msg, sizeof(msg), "%s: %s", what, cudaGetErrorString(e));
+  wq::set_last_error(WQ_ERR_CUDA, msg);
+  return WQ_ERR_CUDA;
+}
+
+// Device address of g_noalloc_scratch in the current context. The first call
+// in a context looks it up (cudaGetSymbolAddress, which also loads the module
+// and, if needed, initialises the device's primary context).
 int32_t scratch_address(void **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    char msg[160];
-    snprintf(msg, sizeof(msg), "cudaGetDevice: %s", cudaGetErrorString(e));
-    wq::set_last_error(WQ_ERR_CUDA, msg);
-    return WQ_ERR_CUDA;
-  }
+  unsigned long long id = current_context_id();
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  for (int i = 0; i < g_scratch_n; ++i) {
-    if (g_scratch_tab[i].device == dev) {
-      *out = g_scratch_tab[i].ptr;
-      return WQ_OK;
-    }
+  if (id != 0) {
+    for (int i = 0; i < g_scratch_n; ++i)
+      if (g_scratch_tab[i].ctx_id == id) {
+        *out = g_scratch_tab[i].ptr;
+        return WQ_OK;
+      }
   }
   void *ptr = nullptr;
-  e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-  if (e != cudaSuccess || ptr == nullptr) {
-    char msg[160];
-    snprintf(msg, sizeof(msg), "cudaGetSymbolAddress of the static scratch on device %d: %s", dev,
-             cudaGetErrorString(e));
-    wq::set_last_error(WQ_ERR_CUDA, msg);
-    return WQ_ERR_CUDA;
+  cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+  if (e != cudaSuccess || ptr == nullptr)
+    return cuda_error(e, "cudaGetSymbolAddress of the static scratch");
+  if (id == 0) id = current_context_id();  // the lookup made a context current
+  if (id != 0) {
+    g_scratch_tab[g_scratch_next] = {id, ptr};
+    g_scratch_next = (g_scratch_next + 1) % kCacheSlots;
+    if (g_scratch_n < kCacheSlots) ++g_scratch_n;
   }
-  if (g_scratch_n < 256) g_scratch_tab[g_scratch_n++] = {dev, ptr};
   *out = ptr;
   return WQ_OK;
 }
@@ -93,12 +139,25 @@ extern "C" int32_t wq_matmul_add_rmsnorm_noalloc(
   // The shared array keeps whatever the previous call left; the status word
   // must start at zero for this call.
   cudaError_t e = cudaMemsetAsync(ws, 0, wq::kWsHeader, (cudaStream_t)stream);
-  if (e != cudaSuccess) {
-    char msg[160];
-    snprintf(msg, sizeof(msg), "clearing the static scratch header: %s", cudaGetErrorString(e));
-    wq::set_last_error(WQ_ERR_CUDA, msg);
-    return WQ_ERR_CUDA;
-  }
+  if (e != cudaSuccess) return cuda_error(e, "clearing the static scratch header");
   return wq_matmul_add_rmsnorm(x1, x2, scale, offset, bias, residual, gamma, eps, group, y,
                                normOut, ws, kScratchBytes, stream);
+}
+
+extern "C" int32_t wq_noalloc_read_device_status(void *stream, int32_t *device_status) {
+  if (!device_status) {
+    wq::set_last_error(WQ_ERR_NULL, "device_status is required");
+    return WQ_ERR_NULL;
+  }
+  void *ws = nullptr;
+  int32_t st = scratch_address(&ws);
+  if (st != WQ_OK) return st;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_error(e, "stream synchronize");
+  uint32_t word = 0;
+  e = cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_error(e, "status word copy");
+  *device_status = (int32_t)word;
+  wq::set_last_error(WQ_OK, "");
+  return WQ_OK;
 }

@@ -13,7 +13,7 @@
 //                the two halves of one) and tcgen05.mma issuer (M=128, N=256,
 //                K=16, kind::f16; one MMA per half).
 //   warps 4-11   dequant: packed weight -> B operand (W^T, 256 x 64, K-major,
-//                128-byte swizzle), in one of two exact forms (below).
+//                128-byte swizzle), in one of two forms (below).
 //   warps 12-15  epilogue (one per TMEM lane quarter): y = acc + bias +
 //                residual, written to HBM; per-row partial sum(y^2) (of the
 //                fp32 y) published to the workspace; the accumulator is handed
@@ -22,15 +22,17 @@
 //                published, sum the partials in a fixed order, and write
 //                normOut = y * rstd * gamma from the y this thread stored
 //                (still in L2: a row block of y is 128 x N x 2 bytes).
-// Operand modes (both keep the dequantized weight exact or within 2^-12):
+// Operand modes:
 //   RAWQ   per-tensor / per-channel scales: B holds the integer q itself (exact
 //          in fp16 and bf16), the MMA accumulates x1*q in fp32, and the epilogue
 //          applies mm = S[n]*acc + O[n]*rowsum(x1[m,:]) + bias.
-//   F16EMU bf16 per-group scales: A is an fp16 copy of x1 (exact; a per-row
-//          power of two e_m keeps it in range) and B = q*S16 + O16 in fp16,
-//          where S16/O16 are the scales times a per-column power of two e_n so
-//          that q*S16 is exact (8-bit significand x 3-bit q <= 11 bits); only
-//          the offset add rounds, at 2^-12. The epilogue multiplies by
+//   F16EMU bf16 per-group scales: A is an fp16 copy of x1 scaled by a per-row
+//          power of two 2^-e_m that puts the row maximum in [2^13, 2^14) (exact
+//          for every element within 2^27 of the row maximum) and B = q*S16 + O16
+//          in fp16, where S16/O16 are the scales times a per-column power of
+//          two 2^-e_n. For INT4, q*S16 is exact (8-bit significand x 3-bit q
+//          <= 11 bits) and only the offset add rounds, at 2^-12; for INT8 the
+//          weight rounds once, at 2^-11. The epilogue multiplies by
 //          2^(e_m + e_n). Rounding W to bf16 instead (2^-9) would put the
 //          result outside the operator's stated tolerance at these K.
 // Pipelines: NR raw stages (x1 + packed weight) and NB dequantized-weight
@@ -87,14 +89,16 @@ struct PrefillArgs {
   uint32_t *counters;
   float *rowpart;
   const float *rowsum;       // RAWQ with offset: sum_k x1[m, k]
-  const int8_t *e_row;       // F16EMU: row exponents
-  const int8_t *e_col;       // F16EMU: column exponents
+  const int16_t *e_row;      // F16EMU: row exponents
+  const int16_t *e_col;      // F16EMU: column exponents
   const uint32_t *S16, *O16; // F16EMU: scaled fp16 scale / offset pairs (G x N words)
   long long M;
   int K, N, group, Ns, nTilesN, kTiles;
   long long nTiles;
   float eps;
   uint32_t so_bytes;         // F16EMU: bytes of one scale/offset row box (rows x 256 x 4)
+  long long budget;          // cycles a row-block wait lasts before it gives up
+  uint32_t extra;            // arrivals a row-block wait needs beyond its own (0; > 0 only in tests)
 };
 
 template <int WBITS, int MH, int MODE>
@@ -473,13 +477,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
       // wait until every n-tile of this row block published its partial sums
       {
-        const uint32_t target = (uint32_t)(kEpiWarps * a.nTilesN);
+        const uint32_t target = (uint32_t)(kEpiWarps * a.nTilesN) + a.extra;
         const long long t0 = clock64();
         bool done = false;
         while (true) {
           done = ld_acquire_u32(a.counters + rb) >= target;
           if (done || *abort_flag) break;
-          if (clock64() - t0 > kWaitBudget) {
+          if (clock64() - t0 > a.budget) {
             *abort_flag = 1;
             record_timeout(a.status, kWhereRowBlock);
             break;
@@ -597,12 +601,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                   mmv[2 * i + 1] = fmaf(s2.y, __uint_as_float(r[8 * v + 2 * i + 1]), o2.y * rs);
                 }
               } else {
-                const uint2 ev = *reinterpret_cast<const uint2 *>(a.e_col + n);
-                const uint32_t ew[2] = {ev.x, ev.y};
+                const uint4 ev = *reinterpret_cast<const uint4 *>(a.e_col + n);
+                const uint32_t ew[4] = {ev.x, ev.y, ev.z, ev.w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                  const int en = (int)(int8_t)((ew[i >> 2] >> (8 * (i & 3))) & 0xFFu);
-                  mmv[i] = __uint_as_float(r[8 * v + i]) * __int_as_float((em + en + 127) << 23);
+                  const int en = (int)(int16_t)((ew[i >> 1] >> (16 * (i & 1))) & 0xFFFFu);
+                  mmv[i] = scale_pow2(__uint_as_float(r[8 * v + i]), em + en);
                 }
               }
               uint32_t bw[4] = {0u, 0u, 0u, 0u}, rw[4] = {0u, 0u, 0u, 0u};
@@ -747,9 +751,9 @@ bool plan_prefill(const Problem &p, Plan &plan) {
     }
   } else {
     plan.erow_off = off;
-    off += align256((uint64_t)p.M);
+    off += align256((uint64_t)p.M * sizeof(int16_t));
     plan.ecol_off = off;
-    off += align256((uint64_t)p.N);
+    off += align256((uint64_t)p.N * sizeof(int16_t));
     const uint64_t ld = (uint64_t)so_ld(p, plan);
     plan.s16_off = off;
     off += align256((uint64_t)p.G * ld * 4);
@@ -789,6 +793,8 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
   args.kTiles = (int)((p.K + BK - 1) / BK);
   args.nTiles = plan.n_tiles * plan.m_tiles;
   args.eps = p.eps;
+  args.budget = wait_budget();
+  args.extra = wait_extra_arrivals();
 
   // status word and row-block counters start at zero on every call
   cudaError_t e = cudaMemsetAsync(ws, 0, plan.rowpart_off, s);
@@ -805,8 +811,8 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
       args.rowsum = rowsum;
     }
   } else {
-    int8_t *e_row = reinterpret_cast<int8_t *>(wsb + plan.erow_off);
-    int8_t *e_col = reinterpret_cast<int8_t *>(wsb + plan.ecol_off);
+    int16_t *e_row = reinterpret_cast<int16_t *>(wsb + plan.erow_off);
+    int16_t *e_col = reinterpret_cast<int16_t *>(wsb + plan.ecol_off);
     uint32_t *S16 = reinterpret_cast<uint32_t *>(wsb + plan.s16_off);
     uint32_t *O16 = p.offset ? reinterpret_cast<uint32_t *>(wsb + plan.o16_off) : nullptr;
     __half *x16 = reinterpret_cast<__half *>(wsb + plan.x16_off);

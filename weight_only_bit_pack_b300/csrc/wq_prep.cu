@@ -3,14 +3,22 @@
 // row_prep: for each row m of x1, the fp32 row sum (the factor of the offset
 //   term when the offset is applied after the k-sum: sum_k x1[m,k]*O[n]) and,
 //   for the fp16-operand mode, a power-of-two exponent e_m and an fp16 copy
-//   x16[m,k] = x1[m,k] * 2^-e_m. bf16 -> fp16 is exact for every value in the
-//   fp16 normal range; e_m is nonzero only for rows whose magnitude would
-//   overflow fp16, and it is undone exactly in the epilogue.
+//   x16[m,k] = x1[m,k] * 2^-e_m. e_m puts the row's largest magnitude into
+//   [2^13, 2^14), scaling small rows up as well as large rows down, so every
+//   element within a factor 2^27 of the row maximum converts to fp16 exactly
+//   (bf16 has 8 significant bits, fp16 11 above 2^-14 and its subnormals reach
+//   2^-24). Elements further below the maximum round (or flush to zero): their
+//   share of any dot product is below 2^-27 of the largest term's. Rows that are
+//   all zero or hold an Inf get e_m = 0 (NaN and Inf then propagate). e_m is
+//   undone exactly in the epilogue.
 // so_prep: for the fp16-operand mode, a per-column exponent e_n and fp16
 //   copies S16 = S * 2^-e_n, O16 = O * 2^-e_n, chosen so that
-//   qmax*|S16| + |O16| lies in [2^12, 2^13): then q*S16 is an exact fp16 value
-//   for every 4-bit q (an 8-bit bf16 significand times a 3-bit integer fits the
-//   11-bit fp16 significand), and only the offset add rounds, at 2^-12.
+//   qmax*|S16| + |O16| lies in [2^12, 2^13): then for 4-bit q, q*S16 is an
+//   exact fp16 value (an 8-bit bf16 significand times a 3-bit integer fits the
+//   11-bit fp16 significand) as long as S16 stays in the fp16 normal range
+//   (scales within 2^25 of the column's largest), and only the offset add
+//   rounds, at 2^-12. For 8-bit q the product needs up to 15 bits and is rounded
+//   once to fp16 (relative error at most 2^-11 of the dequantized weight).
 //   Each value is stored twice, as the two halves of a 32-bit word (the form
 //   the packed fp16 arithmetic of the dequantization consumes). With `odd16`
 //   the scale of every odd column is stored divided by 16 (exact): the kernel
@@ -24,24 +32,23 @@
 namespace wq {
 namespace {
 
-__device__ __forceinline__ float exp2i(int e) {
-  // 2^e as an fp32 for e in [-126, 127]
-  return __int_as_float((e + 127) << 23);
+// floor(log2(v)) of a finite v > 0, subnormals included.
+__device__ __forceinline__ int ilog2f(float v) {
+  if (v < 1.17549435e-38f) return ((__float_as_int(v * 18446744073709551616.f) >> 23) & 0xFF) - 127 - 64;
+  return ((__float_as_int(v) >> 23) & 0xFF) - 127;
 }
 
-// Exponent e >= 0 such that amax * 2^-e < 2^14 (0 when it already is).
+// Exponent e with amax * 2^-e in [2^13, 2^14) for a finite amax > 0; 0 for a
+// zero row and for a row whose maximum is Inf or NaN.
 __device__ __forceinline__ int row_exponent(float amax) {
-  if (!(amax >= 16384.f)) return 0;  // also 0 for NaN
-  if (amax > FLT_MAX) return 0;       // inf: let it propagate
-  int e;
-  frexpf(amax, &e);                   // amax = f * 2^e, f in [0.5, 1)
-  return e - 14;                      // amax * 2^-(e-14) < 2^14
+  if (!(amax > 0.f) || amax > FLT_MAX) return 0;
+  return ilog2f(amax) - 13;
 }
 
 template <int DT>
 __global__ void __launch_bounds__(256)
     row_prep_kernel(const typename Elem<DT>::T *__restrict__ x1, int64_t M, int K,
-                    float *__restrict__ rowsum, int8_t *__restrict__ e_row, __half *__restrict__ x16) {
+                    float *__restrict__ rowsum, int16_t *__restrict__ e_row, __half *__restrict__ x16) {
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -69,8 +76,7 @@ __global__ void __launch_bounds__(256)
     if (rowsum && lane == 0) rowsum[m] = s;
     if (x16) {
       const int e = row_exponent(amax);
-      if (lane == 0) e_row[m] = (int8_t)e;
-      const float sc = exp2i(-e);
+      if (lane == 0) e_row[m] = (int16_t)e;
       __half *out = x16 + m * K;
 #pragma unroll 4
       for (int k = lane * 8; k < K; k += 256) {
@@ -80,7 +86,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float2 f = unpack2<DT>(w[i]);
-          o[i] = pack2<WQ_F16>(f.x * sc, f.y * sc);
+          o[i] = pack2<WQ_F16>(scale_pow2(f.x, -e), scale_pow2(f.y, -e));
         }
         *reinterpret_cast<uint4 *>(out + k) = make_uint4(o[0], o[1], o[2], o[3]);
       }
@@ -100,11 +106,11 @@ __device__ __forceinline__ uint32_t half_pair(float v) {
 template <int DT>
 __global__ void __launch_bounds__(256)
     so_prep_kernel(const typename Elem<DT>::T *__restrict__ S, const typename Elem<DT>::T *__restrict__ O,
-                   int G, int N, int ld, float qmax, int int4, int8_t *__restrict__ e_col,
+                   int G, int N, int ld, float qmax, int int4, int16_t *__restrict__ e_col,
                    uint32_t *__restrict__ S16, uint32_t *__restrict__ O16) {
   using E = Elem<DT>;
   __shared__ float s_max[8][32];
-  __shared__ float s_scale[32];
+  __shared__ int s_exp[32];
   const int cx = threadIdx.x & 31, gy = threadIdx.x >> 5;
   const int n = blockIdx.x * 32 + cx;
   float mx = 0.f;
@@ -122,16 +128,10 @@ __global__ void __launch_bounds__(256)
     float m = s_max[0][cx];
 #pragma unroll
     for (int i = 1; i < 8; ++i) m = fmaxf(m, s_max[i][cx]);
-    int e = 0;
-    if (m > 0.f && m <= FLT_MAX) {
-      int ex;
-      frexpf(m, &ex);  // m in [2^(ex-1), 2^ex)
-      e = ex - 13;     // m * 2^-e in [2^12, 2^13)
-      if (e < -100) e = -100;
-      if (e > 100) e = 100;
-    }
-    if (n < N) e_col[n] = (int8_t)e;
-    s_scale[cx] = exp2i(-e);
+    // m * 2^-e in [2^12, 2^13); 0 for an all-zero or non-finite column
+    const int e = (m > 0.f && m <= FLT_MAX) ? ilog2f(m) - 12 : 0;
+    if (n < N) e_col[n] = (int16_t)e;
+    s_exp[cx] = e;
   }
   __syncthreads();
   // Destination word of column n in a row of ld words. INT4: within each
@@ -145,20 +145,23 @@ __global__ void __launch_bounds__(256)
     dst = (n - c) + (i < 4 ? 4 * l + i : 128 + 4 * l + (i - 4));
   }
   if (n < ld) {
-    const float sc = s_scale[cx];
-    const float ssc = (int4 && (n & 1)) ? sc * 0.0625f : sc;  // exact power-of-two factors
+    const int e = s_exp[cx];
+    const int es = (int4 && (n & 1)) ? -e - 4 : -e;  // odd INT4 columns: scale / 16 (exact)
 #pragma unroll 4
     for (int g = gy; g < G; g += 8) {
       const bool live = n < N;
-      S16[(int64_t)g * ld + dst] = live ? half_pair(E::to_f(S[(int64_t)g * N + n]) * ssc) : 0u;
-      if (O) O16[(int64_t)g * ld + dst] = live ? half_pair(E::to_f(O[(int64_t)g * N + n]) * sc) : 0u;
+      S16[(int64_t)g * ld + dst] =
+          live ? half_pair(scale_pow2(E::to_f(S[(int64_t)g * N + n]), es)) : 0u;
+      if (O)
+        O16[(int64_t)g * ld + dst] =
+            live ? half_pair(scale_pow2(E::to_f(O[(int64_t)g * N + n]), -e)) : 0u;
     }
   }
 }
 
 }  // namespace
 
-cudaError_t launch_row_prep(const Problem &p, float *rowsum, int8_t *e_row, __half *x16,
+cudaError_t launch_row_prep(const Problem &p, float *rowsum, int16_t *e_row, __half *x16,
                             cudaStream_t s) {
   const int64_t warps_needed = p.M;
   int64_t blocks = (warps_needed * 32 + 255) / 256;
@@ -174,7 +177,7 @@ cudaError_t launch_row_prep(const Problem &p, float *rowsum, int8_t *e_row, __ha
   return cudaGetLastError();
 }
 
-cudaError_t launch_so_prep(const Problem &p, int64_t ld, int8_t *e_col, uint32_t *S16,
+cudaError_t launch_so_prep(const Problem &p, int64_t ld, int16_t *e_col, uint32_t *S16,
                            uint32_t *O16, cudaStream_t s) {
   const int N = (int)p.N;
   const int blocks = (int)((ld + 31) / 32);
