@@ -9,11 +9,13 @@ fp16-operand mode scales every row of x1 by a power of two that puts its
 maximum in [2^13, 2^14) and every scale column by another; the decode and
 generic kernels take the values as they are.
 
-Rows scaled by 2^s keep y exactly 2^s times the unscaled row's y (no bias), so
-besides the operator's tolerance |d| <= tol * (1 + |ref|), which is loose for
-tiny rows, y of those rows is also compared after multiplying both sides by
-2^-s. normOut does not depend on the row's scale when eps = 0, so its ordinary
-comparison is already a relative one.
+Rows scaled by 2^s (no bias) have y exactly 2^s times the unscaled row's y,
+and the stated tolerance |d| <= tol * (1 + |ref|) is read on the unscaled
+values: y of those rows is compared after multiplying both sides by 2^-s. (On
+the raw values its absolute floor would be unreachable for 2^15-scale rows even
+for exact weights: fp32 accumulation of K terms of that size errs by more than
+1e-2 where the sum cancels to about 1.) normOut does not depend on the row's
+scale, so it is compared as it is for every row.
 """
 import zlib
 
@@ -50,15 +52,19 @@ def _scaled_rows_problem(M, eps, seed):
 def test_rows_far_from_unit_scale(wq, M, kernel, eps):
     prob = _scaled_rows_problem(M, eps, seed=M + int(eps > 0))
     y, no = run_gpu(wq, prob, kernel)
-    ref = run_oracle(prob)
-    compare(prob, y, no, ref)
+    _, ry, rn = run_oracle(prob)
     tol = TOL[prob.dtype]
     yg = y.double().cpu().numpy()
+    ng = no.double().cpu().numpy()
+    scale = np.ones((M, 1))
     for (r0, r1), s in ROW_SCALES:
-        g = yg[r0:r1] * 2.0 ** -s
-        r = ref[1][r0:r1] * 2.0 ** -s
+        scale[r0:r1] = 2.0 ** -s
+    for name, g, r in (("y", yg * scale, ry * scale), ("normOut", ng, rn)):
         err = np.abs(g - r) / (1.0 + np.abs(r))
-        assert err.max() <= tol, f"rows {r0}..{r1 - 1} (x 2^{s}): y relative error {err.max():.3e}"
+        bad = np.argwhere(~(err <= tol))
+        assert bad.size == 0, (f"{prob.name} {name}: {len(bad)} elements exceed {tol}; worst "
+                               f"{err.max():.3e} at {tuple(bad[0])} (row scale 2^"
+                               f"{-np.log2(scale[bad[0][0], 0]):g})")
 
 
 @pytest.mark.parametrize("M,kernel", [(300, PREFILL), (300, GENERIC), (12, DECODE)])

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -61,7 +62,8 @@ struct Plan {
   // prefill: operand mode, counters, row partials and preparation buffers
   int mode = 0;
   uint64_t cnt_off = 0, rowpart_off = 0, rowsum_off = 0, erow_off = 0, ecol_off = 0, s16_off = 0,
-           o16_off = 0, x16_off = 0;
+           x16_off = 0, dext_off = 0, oext_off = 0;
+  int ldx = 0;       // prefill F16EMU with offset: columns of the offset-term operands (2G up to 64)
   int64_t n_tiles = 0, m_tiles = 0;
   int grid = 0;
   int m_halves = 1;  // prefill: 128-row MMA halves per output tile (1 or 2)
@@ -73,12 +75,16 @@ cudaError_t launch_generic(const Problem &p, const Plan &plan, void *ws, cudaStr
 cudaError_t launch_prefill(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
 cudaError_t launch_decode(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
 cudaError_t launch_timeout_check(uint32_t *status, long long budget, cudaStream_t s);
+// row_prep: row sums (RAWQ with offset) or the fp16 copy of x1 with its row
+// exponents, plus (F16EMU with offset, dext != nullptr) the per-group row sums
+// of that copy split into bf16 hi/lo, (M, ldx) row-major.
 cudaError_t launch_row_prep(const Problem &p, float *rowsum, int16_t *e_row, __half *x16,
-                            cudaStream_t s);
-// S16/O16 rows are ld words long (ld >= N; INT4 rows are padded to whole
-// 256-column tiles and stored in the dequant's interleaved column order).
+                            __nv_bfloat16 *dext, int ldx, cudaStream_t s);
+// S16 rows are ld words long (ld >= N; INT4 rows are padded to whole
+// 256-column tiles and stored in the dequant's interleaved column order);
+// Oext (offset only) is the (N, ldx) bf16 operand of the offset term.
 cudaError_t launch_so_prep(const Problem &p, int64_t ld, int16_t *e_col, uint32_t *S16,
-                           uint32_t *O16, cudaStream_t s);
+                           __nv_bfloat16 *Oext, int ldx, cudaStream_t s);
 cudaError_t launch_epilogue(const Problem &p, const Plan &plan, const void *ws, bool pdl,
                             cudaStream_t s);
 

@@ -28,12 +28,16 @@
 //          applies mm = S[n]*acc + O[n]*rowsum(x1[m,:]) + bias.
 //   F16EMU bf16 per-group scales: A is an fp16 copy of x1 scaled by a per-row
 //          power of two 2^-e_m that puts the row maximum in [2^13, 2^14) (exact
-//          for every element within 2^27 of the row maximum) and B = q*S16 + O16
-//          in fp16, where S16/O16 are the scales times a per-column power of
-//          two 2^-e_n. For INT4, q*S16 is exact (8-bit significand x 3-bit q
-//          <= 11 bits) and only the offset add rounds, at 2^-12; for INT8 the
-//          weight rounds once, at 2^-11. The epilogue multiplies by
-//          2^(e_m + e_n). Rounding W to bf16 instead (2^-9) would put the
+//          for every element within 2^27 of the row maximum) and B = q*S16 in
+//          fp16, where S16 is the scale times a per-column power of two 2^-e_n.
+//          For INT4, q*S16 is exact (8-bit significand x 3-bit q <= 11 bits);
+//          for INT8 it rounds once, at 2^-11. An offset is not added to B (that
+//          sum would round): its term sum_g O[g][n] * sum_{k in g} x1[m][k]
+//          runs as kTilesX extra k-steps of bf16 MMAs into the same
+//          accumulator, A = the per-group row sums of the fp16 copy split into
+//          bf16 hi + lo (to 2^-18), B = O * 2^-e_n in bf16 (exact), both loaded by
+//          TMA straight into the MMA's operand layout. The epilogue multiplies
+//          by 2^(e_m + e_n). Rounding W to bf16 instead (2^-9) would put the
 //          result outside the operator's stated tolerance at these K.
 // Pipelines: NR raw stages (x1 + packed weight) and NB dequantized-weight
 // stages, each guarded by full/empty mbarriers. With MH = 1 two accumulator
@@ -91,9 +95,10 @@ struct PrefillArgs {
   const float *rowsum;       // RAWQ with offset: sum_k x1[m, k]
   const int16_t *e_row;      // F16EMU: row exponents
   const int16_t *e_col;      // F16EMU: column exponents
-  const uint32_t *S16, *O16; // F16EMU: scaled fp16 scale / offset pairs (G x N words)
+  const uint32_t *S16;       // F16EMU: scaled fp16 scale pairs (G x ld words)
   long long M;
   int K, N, group, Ns, nTilesN, kTiles;
+  int kTilesX;               // F16EMU with offset: extra k-steps of the offset term (else 0)
   long long nTiles;
   float eps;
   uint32_t so_bytes;         // F16EMU: bytes of one scale/offset row box (rows x 256 x 4)
@@ -109,14 +114,13 @@ struct Layout {
   static constexpr uint32_t A_BYTES = MH * A_HALF;
   static constexpr uint32_t BQ_BYTES = BK * BN * WBITS / 8;   // 8 or 16 KB
   static constexpr uint32_t B_BYTES = BN * BK * 2;            // 32 KB
-  // F16EMU: rows of S16 / O16 pairs (3 KB); RAWQ reads scales in the epilogue
+  // F16EMU: rows of S16 pairs (3 KB); RAWQ reads scales in the epilogue
   static constexpr uint32_t SO_BYTES = MODE == kF16Emu ? SO_ROWS * BN * 4 : 0;
   static constexpr uint32_t A_OFF = 0;
   static constexpr uint32_t BQ_OFF = A_OFF + NR * A_BYTES;
   static constexpr uint32_t B_OFF = BQ_OFF + NR * BQ_BYTES;
   static constexpr uint32_t S_OFF = B_OFF + NB * B_BYTES;
-  static constexpr uint32_t O_OFF = S_OFF + NR * SO_BYTES;
-  static constexpr uint32_t BAR_OFF = O_OFF + NR * SO_BYTES;
+  static constexpr uint32_t BAR_OFF = S_OFF + NR * SO_BYTES;
   static constexpr int NBARS = 2 * NR + 2 * NB + 4 + 1;
   static constexpr uint32_t SMEM = BAR_OFF + 8 * NBARS + 16 + 1024;
 };
@@ -142,47 +146,30 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
   return v;
 }
 
-// Packed pair arithmetic in the activation dtype: (v - c) * s + o, one rounding
-// for the subtraction (exact here: small integers) and one for the fma.
-template <int DT>
-__device__ __forceinline__ uint32_t sub_fma2(uint32_t v, uint32_t c, uint32_t s, uint32_t o) {
+// Packed fp16 pair arithmetic: (v - c) * s, exact here (small integers times
+// a scale whose product fits the fp16 significand) or rounded once (INT8).
+__device__ __forceinline__ uint32_t sub_mul2_f16(uint32_t v, uint32_t c, uint32_t s) {
   uint32_t r;
-  if (DT == WQ_BF16) {
-    asm("{\n\t.reg .b32 t;\n\t"
-        "sub.rn.bf16x2 t, %1, %2;\n\t"
-        "fma.rn.bf16x2 %0, t, %3, %4;\n\t}"
-        : "=r"(r)
-        : "r"(v), "r"(c), "r"(s), "r"(o));
-  } else {
-    asm("{\n\t.reg .b32 t;\n\t"
-        "sub.rn.f16x2 t, %1, %2;\n\t"
-        "fma.rn.f16x2 %0, t, %3, %4;\n\t}"
-        : "=r"(r)
-        : "r"(v), "r"(c), "r"(s), "r"(o));
-  }
+  asm("{\n\t.reg .b32 t;\n\t"
+      "sub.rn.f16x2 t, %1, %2;\n\t"
+      "mul.rn.f16x2 %0, t, %3;\n\t}"
+      : "=r"(r)
+      : "r"(v), "r"(c), "r"(s));
   return r;
 }
 
-// Reads the S16/O16 pairs (both halves hold the value) of CNT columns in group
-// row `row` of the stage's scale/offset rows: four columns per 16-byte chunk,
-// chunk q at word w + QSTRIDE * q of the row. Rows past the last group were
-// zero-filled by the copy (callers skip k-rows past K, whose rows may be stale).
+// Reads the S16 pairs (both halves hold the value) of CNT columns in group
+// row `row` of the stage's scale rows: four columns per 16-byte chunk, chunk q
+// at word w + QSTRIDE * q of the row. Rows past the last group were zero-filled
+// by the copy (callers skip k-rows past K, whose rows may be stale).
 template <int CNT, int QSTRIDE>
-__device__ __forceinline__ void smem_so(uint32_t s_base, uint32_t o_base, bool has_o, int row, int w,
-                                        uint32_t (&s2)[CNT], uint32_t (&o2)[CNT]) {
+__device__ __forceinline__ void smem_s(uint32_t s_base, int row, int w, uint32_t (&s2)[CNT]) {
   const uint32_t off = (uint32_t)(row * BN + w) * 4u;
 #pragma unroll
-  for (int q = 0; q < CNT / 4; ++q) {
+  for (int q = 0; q < CNT / 4; ++q)
     asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(s2[4 * q]), "=r"(s2[4 * q + 1]), "=r"(s2[4 * q + 2]), "=r"(s2[4 * q + 3])
                  : "r"(s_base + off + 4u * QSTRIDE * q));
-    if (has_o)
-      asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                   : "=r"(o2[4 * q]), "=r"(o2[4 * q + 1]), "=r"(o2[4 * q + 2]), "=r"(o2[4 * q + 3])
-                   : "r"(o_base + off + 4u * QSTRIDE * q));
-    else
-      o2[4 * q] = o2[4 * q + 1] = o2[4 * q + 2] = o2[4 * q + 3] = 0u;
-  }
 }
 
 // Byte offset of the 16-byte chunk (row r, k-octet c) in a K-major 128-byte
@@ -194,8 +181,8 @@ __device__ __forceinline__ uint32_t sw128_chunk(int r, int c) {
 template <int DT, int WBITS, int MODE, int MH>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                   const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_o,
-                   const PrefillArgs a) {
+                   const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_dx,
+                   const __grid_constant__ CUtensorMap tm_ox, const PrefillArgs a) {
   using L = Layout<WBITS, MH, MODE>;
   constexpr int NACC = 2 / MH;   // accumulator buffers of MH x 256 TMEM columns
   constexpr int TM = BM * MH;    // output rows per tile
@@ -234,7 +221,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_w);
     if (MODE == kF16Emu) {
       prefetch_tmap(&tm_s);
-      if (a.offset) prefetch_tmap(&tm_o);
+      if (a.kTilesX) {
+        prefetch_tmap(&tm_dx);
+        prefetch_tmap(&tm_ox);
+      }
     }
   }
   if (warp == 1) {
@@ -251,15 +241,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     // packed weights are re-read by every row block: keep them in L2
     const uint64_t pol_w = policy_evict_last();
     long long it = 0;
+    const int kAll = a.kTiles + a.kTilesX;
     for (long long t = blockIdx.x; t < a.nTiles; t += gridDim.x) {
       const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
-      for (int ks = 0; ks < a.kTiles; ++ks, ++it) {
+      for (int ks = 0; ks < kAll; ++ks, ++it) {
         const int s = (int)(it % NR);
         const uint32_t ph = (uint32_t)((it / NR) & 1);
         if (!wait_bar_warp(BAR(RAWEMPTY(s)), ph ^ 1u, abort_flag, a.status, kWhereProducer)) goto pdone;
+        if (MODE == kF16Emu && ks >= a.kTiles) {
+          // offset-term k-step: A = row sums of the groups (bf16 parts), B = the
+          // offsets, both straight into the MMA's operand layout; the B slot is
+          // this stage's, once the MMA has released it
+          const int sb = (int)(it % NB);
+          if (!wait_bar_warp(BAR(BEMPTY(sb)), (uint32_t)(((it / NB) & 1) ^ 1), abort_flag, a.status,
+                             kWhereProducer))
+            goto pdone;
+          if (lane == 0) {
+            const int kx = (ks - a.kTiles) * BK;
+            mbar_arrive_expect_tx(BAR(FULL(s)), L::A_BYTES + L::B_BYTES);
+            tma_load_2d(sbase + L::A_OFF + s * L::A_BYTES, &tm_dx, kx, rb * TM, BAR(FULL(s)));
+            tma_load_2d(sbase + L::B_OFF + sb * L::B_BYTES, &tm_ox, kx, nt * BN, BAR(FULL(s)));
+          }
+          __syncwarp();
+          continue;
+        }
         if (lane == 0) {
           uint32_t bytes = L::A_BYTES + L::BQ_BYTES;
-          if (MODE == kF16Emu) bytes += (a.offset ? 2u : 1u) * a.so_bytes;
+          if (MODE == kF16Emu) bytes += a.so_bytes;
           mbar_arrive_expect_tx(BAR(FULL(s)), bytes);
           tma_load_2d(sbase + L::A_OFF + s * L::A_BYTES, &tm_x, ks * BK, rb * TM, BAR(FULL(s)));
           tma_load_2d_hint(sbase + L::BQ_OFF + s * L::BQ_BYTES, &tm_w, nt * (BN * WBITS / 8),
@@ -268,8 +276,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the group rows this k-stage touches: (ks*BK)/group .. +SO_ROWS-1
             const int r0 = (ks * BK) / a.group;
             tma_load_2d(sbase + L::S_OFF + s * L::SO_BYTES, &tm_s, nt * BN, r0, BAR(FULL(s)));
-            if (a.offset)
-              tma_load_2d(sbase + L::O_OFF + s * L::SO_BYTES, &tm_o, nt * BN, r0, BAR(FULL(s)));
           }
         }
         __syncwarp();
@@ -284,6 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- MMA issuer
     {
       const uint32_t idesc = idesc_f16(MDT == WQ_BF16 ? 1u : 0u, BM, BN);
+      const uint32_t idesc_x = idesc_f16(1u, BM, BN);  // offset-term k-steps: bf16 x bf16
+      const int kAll = a.kTiles + a.kTilesX;
       long long it = 0;
       int lt = 0;
       for (long long t = blockIdx.x; t < a.nTiles; t += gridDim.x, ++lt) {
@@ -293,8 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           goto mdone;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(buf * BN);  // half h at + h * BN
-        for (int ks = 0; ks < a.kTiles; ++ks, ++it) {
+        for (int ks = 0; ks < kAll; ++ks, ++it) {
           const int s = (int)(it % NR), sb = (int)(it % NB);
+          const bool xstep = ks >= a.kTiles;  // offset-term step: both operands came by TMA
           if (!wait_bar_warp(BAR(FULL(s)), (uint32_t)((it / NR) & 1), abort_flag, a.status, kWhereMma))
             goto mdone;
           if (!wait_bar_warp(BAR(BFULL(sb)), (uint32_t)((it / NB) & 1), abort_flag, a.status,
@@ -304,12 +313,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             const uint32_t aaddr = sbase + L::A_OFF + s * L::A_BYTES;
             const uint32_t baddr = sbase + L::B_OFF + sb * L::B_BYTES;
+            const uint32_t id = xstep ? idesc_x : idesc;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
 #pragma unroll
               for (int h = 0; h < MH; ++h)
                 mma_f16(d + (uint32_t)(h * BN), desc_kmajor_sw128(aaddr + h * L::A_HALF + kk * 32),
-                        desc_kmajor_sw128(baddr + kk * 32), idesc, (ks | kk) != 0 ? 1u : 0u);
+                        desc_kmajor_sw128(baddr + kk * 32), id, (ks | kk) != 0 ? 1u : 0u);
             mma_commit(BAR(BEMPTY(sb)));
             mma_commit(BAR(RAWEMPTY(s)));
           }
@@ -340,14 +350,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 128 + u (bf16) or 1024 + u (fp16); subtracting `magic` gives q exactly.
     const uint32_t magic4 = MDT == WQ_BF16 ? 0x43084308u : 0x64086408u;
     long long it = 0;
+    const int kAll = a.kTiles + a.kTilesX;
     for (long long t = blockIdx.x; t < a.nTiles; t += gridDim.x) {
-      for (int ks = 0; ks < a.kTiles; ++ks, ++it) {
+      for (int ks = 0; ks < kAll; ++ks, ++it) {
         const int s = (int)(it % NR), sb = (int)(it % NB);
         const int k = ks * BK + 8 * ko;
+        if (ks >= a.kTiles) {
+          // offset-term step: no weight to dequantize (the producer copied both
+          // operands). The warps still arrive on the raw slot's and the B slot's
+          // barriers, so that every barrier completes exactly once per step and
+          // the parity waits of later steps stay in step. They arrive only after
+          // the copies landed: the producer issued them after the B slot's
+          // previous use was released, so no arrival counts towards that use.
+          if (!wait_bar_warp(BAR(FULL(s)), (uint32_t)((it / NR) & 1), abort_flag, a.status,
+                             kWhereDequant))
+            goto ddone;
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(BAR(RAWEMPTY(s)));
+            mbar_arrive(BAR(BFULL(sb)));
+          }
+          continue;
+        }
         const uint32_t bq = sbase + L::BQ_OFF + s * L::BQ_BYTES;
         const uint32_t bst = sbase + L::B_OFF + sb * L::B_BYTES;
         if constexpr (WBITS == 4) {
-          uint32_t s2[8], o2[8];
+          uint32_t s2[8];
           if (!wait_bar_warp(BAR(FULL(s)), (uint32_t)((it / NR) & 1), abort_flag, a.status,
                              kWhereDequant))
             goto ddone;
@@ -357,12 +385,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (MODE == kF16Emu) {
             if (k < a.K) {
               // columns 8 lane .. 8 lane + 7, stored as words 4 lane .. and 128 + 4 lane ..
-              smem_so<8, 128>(sbase + L::S_OFF + s * L::SO_BYTES, sbase + L::O_OFF + s * L::SO_BYTES,
-                              a.offset != nullptr, (k / a.group - (ks * BK) / a.group), 4 * lane, s2,
-                              o2);
+              smem_s<8, 128>(sbase + L::S_OFF + s * L::SO_BYTES, (k / a.group - (ks * BK) / a.group),
+                             4 * lane, s2);
             } else {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) s2[j] = o2[j] = 0u;
+              for (int j = 0; j < 8; ++j) s2[j] = 0u;
             }
           }
           uint32_t wr[8], wsh[8];
@@ -387,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t x = __byte_perm(wr[2 * p], wr[2 * p + 1], sel);
                 const uint32_t mg = (j & 1) ? 0x64806480u : magic4;
                 const uint32_t v = (x & ((j & 1) ? 0x00F000F0u : 0x000F000Fu)) ^ mg;
-                c[p] = sub_fma2<WQ_F16>(v, mg, s2[j], o2[j]);
+                c[p] = sub_mul2_f16(v, mg, s2[j]);
               } else {
                 const uint32_t x = (j & 1) ? __byte_perm(wsh[2 * p], wsh[2 * p + 1], sel)
                                            : __byte_perm(wr[2 * p], wr[2 * p + 1], sel);
@@ -398,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             st_shared_v4(bst + sto[j], c[0], c[1], c[2], c[3]);
           }
         } else {
-          uint32_t s2a[4], o2a[4], s2b[4], o2b[4];
+          uint32_t s2a[4], s2b[4];
           if (!wait_bar_warp(BAR(FULL(s)), (uint32_t)((it / NR) & 1), abort_flag, a.status,
                              kWhereDequant))
             goto ddone;
@@ -409,12 +436,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (k < a.K) {
               const int rr = k / a.group - (ks * BK) / a.group;
               const uint32_t sa = sbase + L::S_OFF + s * L::SO_BYTES;
-              const uint32_t oa = sbase + L::O_OFF + s * L::SO_BYTES;
-              smem_so<4, 4>(sa, oa, a.offset != nullptr, rr, 4 * lane, s2a, o2a);
-              smem_so<4, 4>(sa, oa, a.offset != nullptr, rr, 4 * (lane + 32), s2b, o2b);
+              smem_s<4, 4>(sa, rr, 4 * lane, s2a);
+              smem_s<4, 4>(sa, rr, 4 * (lane + 32), s2b);
             } else {
 #pragma unroll
-              for (int j = 0; j < 4; ++j) s2a[j] = o2a[j] = s2b[j] = o2b[j] = 0u;
+              for (int j = 0; j < 4; ++j) s2a[j] = s2b[j] = 0u;
             }
           }
           uint32_t wa[8], wb[8];
@@ -440,8 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   // byte b, (b ^ 0x80) | 0x6400 is the fp16 value 1152 + q
                   const uint32_t v = (x & 0x00FF00FFu) ^ 0x64806480u;
                   if constexpr (MODE == kF16Emu)
-                    c[p] = sub_fma2<WQ_F16>(v, 0x64806480u, half ? s2b[j] : s2a[j],
-                                            half ? o2b[j] : o2a[j]);
+                    c[p] = sub_mul2_f16(v, 0x64806480u, half ? s2b[j] : s2a[j]);
                   else
                     c[p] = sub2<WQ_F16>(v, 0x64806480u);
                 } else {
@@ -757,12 +782,16 @@ bool plan_prefill(const Problem &p, Plan &plan) {
     const uint64_t ld = (uint64_t)so_ld(p, plan);
     plan.s16_off = off;
     off += align256((uint64_t)p.G * ld * 4);
-    if (p.offset) {
-      plan.o16_off = off;
-      off += align256((uint64_t)p.G * ld * 4);
-    }
     plan.x16_off = off;
     off += align256((uint64_t)p.M * p.K * 2);
+    if (p.offset) {
+      // offset term: (M, ldx) group row sums (hi | lo) and (N, ldx) offsets, bf16
+      plan.ldx = (int)((2 * p.G + BK - 1) / BK * BK);
+      plan.dext_off = off;
+      off += align256((uint64_t)p.M * plan.ldx * 2);
+      plan.oext_off = off;
+      off += align256((uint64_t)p.N * plan.ldx * 2);
+    }
   }
   plan.ws_bytes = off;
   return true;
@@ -771,6 +800,7 @@ bool plan_prefill(const Problem &p, Plan &plan) {
 template <int DT, int WBITS, int MODE, int MH>
 static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws, cudaStream_t s) {
   using L = Layout<WBITS, MH, MODE>;
+  constexpr int TMROWS = BM * MH;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
@@ -791,6 +821,7 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
   args.M = p.M; args.K = (int)p.K; args.N = (int)p.N; args.group = (int)p.group; args.Ns = (int)p.Ns;
   args.nTilesN = (int)plan.n_tiles;
   args.kTiles = (int)((p.K + BK - 1) / BK);
+  args.kTilesX = MODE == kF16Emu && p.offset ? plan.ldx / BK : 0;
   args.nTiles = plan.n_tiles * plan.m_tiles;
   args.eps = p.eps;
   args.budget = wait_budget();
@@ -801,12 +832,13 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
   if (e != cudaSuccess) return e;
 
   const void *a_src = p.x1;
+  const void *x_ext = nullptr, *o_ext = nullptr;  // offset-term operands (F16EMU with offset)
   CUtensorMapDataType a_type =
       DT == WQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   if constexpr (MODE == kRawQ) {
     if (p.offset) {
       float *rowsum = reinterpret_cast<float *>(wsb + plan.rowsum_off);
-      e = launch_row_prep(p, rowsum, nullptr, nullptr, s);
+      e = launch_row_prep(p, rowsum, nullptr, nullptr, nullptr, 0, s);
       if (e != cudaSuccess) return e;
       args.rowsum = rowsum;
     }
@@ -814,13 +846,16 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
     int16_t *e_row = reinterpret_cast<int16_t *>(wsb + plan.erow_off);
     int16_t *e_col = reinterpret_cast<int16_t *>(wsb + plan.ecol_off);
     uint32_t *S16 = reinterpret_cast<uint32_t *>(wsb + plan.s16_off);
-    uint32_t *O16 = p.offset ? reinterpret_cast<uint32_t *>(wsb + plan.o16_off) : nullptr;
     __half *x16 = reinterpret_cast<__half *>(wsb + plan.x16_off);
-    e = launch_row_prep(p, nullptr, e_row, x16, s);
+    __nv_bfloat16 *dext = p.offset ? reinterpret_cast<__nv_bfloat16 *>(wsb + plan.dext_off) : nullptr;
+    __nv_bfloat16 *oext = p.offset ? reinterpret_cast<__nv_bfloat16 *>(wsb + plan.oext_off) : nullptr;
+    e = launch_row_prep(p, nullptr, e_row, x16, dext, plan.ldx, s);
     if (e != cudaSuccess) return e;
-    e = launch_so_prep(p, so_ld(p, plan), e_col, S16, O16, s);
+    e = launch_so_prep(p, so_ld(p, plan), e_col, S16, oext, plan.ldx, s);
     if (e != cudaSuccess) return e;
-    args.e_row = e_row; args.e_col = e_col; args.S16 = S16; args.O16 = O16;
+    args.e_row = e_row; args.e_col = e_col; args.S16 = S16;
+    x_ext = dext;
+    o_ext = oext;
     a_src = x16;
     a_type = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   }
@@ -847,7 +882,7 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  CUtensorMap tm_s = tm_w, tm_o = tm_w;  // placeholders unless F16EMU
+  CUtensorMap tm_s = tm_w, tm_dx = tm_w, tm_ox = tm_w;  // placeholders unless F16EMU
   args.so_bytes = 0;
   if constexpr (MODE == kF16Emu) {
     const int64_t ld = so_ld(p, plan);
@@ -861,15 +896,27 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    if (p.offset) {
-      r = enc(&tm_o, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(args.O16), dims,
-              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+    if (args.kTilesX > 0) {
+      // A: (M, ldx) group row sums, 64 x (128 MH) boxes; B: (N, ldx) offsets,
+      // 64 x 256 boxes; both bf16, K-major with the 128-byte swizzle of the MMA
+      const cuuint64_t sx[1] = {(cuuint64_t)plan.ldx * 2};
+      const cuuint32_t estr1[2] = {1, 1};
+      const cuuint64_t dxd[2] = {(cuuint64_t)plan.ldx, (cuuint64_t)p.M};
+      const cuuint32_t dxb[2] = {BK, (cuuint32_t)TMROWS};
+      r = enc(&tm_dx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x_ext), dxd, sx, dxb,
+              estr1, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+      const cuuint64_t oxd[2] = {(cuuint64_t)plan.ldx, (cuuint64_t)p.N};
+      const cuuint32_t oxb[2] = {BK, BN};
+      r = enc(&tm_ox, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(o_ext), oxd, sx, oxb,
+              estr1, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
   }
   prefill_kernel<DT, WBITS, MODE, MH>
-      <<<plan.grid, kThreads, L::SMEM, s>>>(tm_x, tm_w, tm_s, tm_o, args);
+      <<<plan.grid, kThreads, L::SMEM, s>>>(tm_x, tm_w, tm_s, tm_dx, tm_ox, args);
   return cudaGetLastError();
 }
 

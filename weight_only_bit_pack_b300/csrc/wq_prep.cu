@@ -11,18 +11,25 @@
 //   share of any dot product is below 2^-27 of the largest term's. Rows that are
 //   all zero or hold an Inf get e_m = 0 (NaN and Inf then propagate). e_m is
 //   undone exactly in the epilogue.
+//   With an offset, row_prep also writes the operand of the offset term
+//   sum_g O[g][n] * d[m][g], d[m][g] = sum of x16[m][k] over group g (fp32, in
+//   ascending k): each d split into two bf16 parts hi + lo (together within
+//   2^-18 of d), stored as row m of an (M, ldx) bf16 array [hi | lo | zero
+//   padding], ldx = 2G rounded up to 64.
 // so_prep: for the fp16-operand mode, a per-column exponent e_n and fp16
-//   copies S16 = S * 2^-e_n, O16 = O * 2^-e_n, chosen so that
-//   qmax*|S16| + |O16| lies in [2^12, 2^13): then for 4-bit q, q*S16 is an
-//   exact fp16 value (an 8-bit bf16 significand times a 3-bit integer fits the
-//   11-bit fp16 significand) as long as S16 stays in the fp16 normal range
-//   (scales within 2^25 of the column's largest), and only the offset add
-//   rounds, at 2^-12. For 8-bit q the product needs up to 15 bits and is rounded
-//   once to fp16 (relative error at most 2^-11 of the dequantized weight).
-//   Each value is stored twice, as the two halves of a 32-bit word (the form
-//   the packed fp16 arithmetic of the dequantization consumes). With `odd16`
-//   the scale of every odd column is stored divided by 16 (exact): the kernel
-//   reads those columns' nibbles in place at bits 7:4, i.e. as 16 q.
+//   copies S16 = S * 2^-e_n chosen so that qmax*|S16| lies in [2^12, 2^13):
+//   then for 4-bit q, q*S16 is an exact fp16 value (an 8-bit bf16 significand
+//   times a 3-bit integer fits the 11-bit fp16 significand) as long as S16
+//   stays in the fp16 normal range (scales within 2^25 of the column's
+//   largest). For 8-bit q the product needs up to 15 bits and is rounded once
+//   to fp16 (relative error at most 2^-11 of q*S). Each value is stored twice,
+//   as the two halves of a 32-bit word (the form the packed fp16 arithmetic of
+//   the dequantization consumes). With `odd16` the scale of every odd column is
+//   stored divided by 16 (exact): the kernel reads those columns' nibbles in
+//   place at bits 7:4, i.e. as 16 q. With an offset, the offsets scaled by the
+//   same 2^-e_n (exact in bf16, which has fp32's exponent range) go to an
+//   (N, ldx) bf16 array whose row n is [O' | O' | zero padding], the K-major
+//   operand that multiplies the hi and lo parts of d.
 // Both passes are deterministic (fixed reduction order).
 #include <cfloat>
 
@@ -48,7 +55,8 @@ __device__ __forceinline__ int row_exponent(float amax) {
 template <int DT>
 __global__ void __launch_bounds__(256)
     row_prep_kernel(const typename Elem<DT>::T *__restrict__ x1, int64_t M, int K,
-                    float *__restrict__ rowsum, int16_t *__restrict__ e_row, __half *__restrict__ x16) {
+                    float *__restrict__ rowsum, int16_t *__restrict__ e_row, __half *__restrict__ x16,
+                    __nv_bfloat16 *__restrict__ dext, int group, int G, int ldx) {
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -90,6 +98,32 @@ __global__ void __launch_bounds__(256)
         }
         *reinterpret_cast<uint4 *>(out + k) = make_uint4(o[0], o[1], o[2], o[3]);
       }
+      if (dext) {
+        // per-group sums of the fp16 row just written (the warp's own stores:
+        // __syncwarp orders them before the loads of the other lanes)
+        __syncwarp();
+        __nv_bfloat16 *drow = dext + m * ldx;
+        for (int gi = lane; gi < G; gi += 32) {
+          const int k0 = gi * group, k1 = k0 + group < K ? k0 + group : K;
+          float d = 0.f;
+          for (int k = k0; k < k1; k += 8) {  // group % 32 == 0 and K % 8 == 0
+            const uint4 v = *reinterpret_cast<const uint4 *>(out + k);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = unpack2<WQ_F16>(w[i]);
+              d += f.x;
+              d += f.y;
+            }
+          }
+          // d = hi + lo to 2^-18, each bf16 (the difference d - hi is exact in fp32)
+          const __nv_bfloat16 hi = __float2bfloat16_rn(d);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(d - __bfloat162float(hi));
+          drow[gi] = hi;
+          drow[G + gi] = lo;
+        }
+        for (int j = 2 * G + lane; j < ldx; j += 32) drow[j] = __float2bfloat16_rn(0.f);
+      }
     }
   }
 }
@@ -107,7 +141,7 @@ template <int DT>
 __global__ void __launch_bounds__(256)
     so_prep_kernel(const typename Elem<DT>::T *__restrict__ S, const typename Elem<DT>::T *__restrict__ O,
                    int G, int N, int ld, float qmax, int int4, int16_t *__restrict__ e_col,
-                   uint32_t *__restrict__ S16, uint32_t *__restrict__ O16) {
+                   uint32_t *__restrict__ S16, __nv_bfloat16 *__restrict__ Oext, int ldx) {
   using E = Elem<DT>;
   __shared__ float s_max[8][32];
   __shared__ int s_exp[32];
@@ -117,9 +151,7 @@ __global__ void __launch_bounds__(256)
   if (n < N) {
 #pragma unroll 4
     for (int g = gy; g < G; g += 8) {
-      const float sv = fabsf(E::to_f(S[(int64_t)g * N + n]));
-      const float ov = O ? fabsf(E::to_f(O[(int64_t)g * N + n])) : 0.f;
-      mx = fmaxf(mx, fmaf(qmax, sv, ov));
+      mx = fmaxf(mx, qmax * fabsf(E::to_f(S[(int64_t)g * N + n])));
     }
   }
   s_max[gy][cx] = mx;
@@ -152,33 +184,42 @@ __global__ void __launch_bounds__(256)
       const bool live = n < N;
       S16[(int64_t)g * ld + dst] =
           live ? half_pair(scale_pow2(E::to_f(S[(int64_t)g * N + n]), es)) : 0u;
-      if (O)
-        O16[(int64_t)g * ld + dst] =
-            live ? half_pair(scale_pow2(E::to_f(O[(int64_t)g * N + n]), -e)) : 0u;
     }
+  }
+  if (O && n < N) {
+    __nv_bfloat16 *orow = Oext + (int64_t)n * ldx;
+    for (int g = gy; g < G; g += 8) {
+      const __nv_bfloat16 o = __float2bfloat16_rn(scale_pow2(E::to_f(O[(int64_t)g * N + n]), -s_exp[cx]));
+      orow[g] = o;
+      orow[G + g] = o;
+    }
+    for (int j = 2 * G + gy; j < ldx; j += 8) orow[j] = __float2bfloat16_rn(0.f);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_row_prep(const Problem &p, float *rowsum, int16_t *e_row, __half *x16,
-                            cudaStream_t s) {
+                            __nv_bfloat16 *dext, int ldx, cudaStream_t s) {
   const int64_t warps_needed = p.M;
   int64_t blocks = (warps_needed * 32 + 255) / 256;
   const int64_t cap = (int64_t)device_info().sms * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  const int group = (int)p.group, G = (int)p.G;
   if (p.dtype == WQ_BF16)
     row_prep_kernel<WQ_BF16><<<(unsigned)blocks, 256, 0, s>>>(
-        static_cast<const __nv_bfloat16 *>(p.x1), p.M, (int)p.K, rowsum, e_row, x16);
+        static_cast<const __nv_bfloat16 *>(p.x1), p.M, (int)p.K, rowsum, e_row, x16, dext, group,
+        G, ldx);
   else
     row_prep_kernel<WQ_F16><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const __half *>(p.x1), p.M,
-                                                             (int)p.K, rowsum, e_row, x16);
+                                                             (int)p.K, rowsum, e_row, x16, dext,
+                                                             group, G, ldx);
   return cudaGetLastError();
 }
 
 cudaError_t launch_so_prep(const Problem &p, int64_t ld, int16_t *e_col, uint32_t *S16,
-                           uint32_t *O16, cudaStream_t s) {
+                           __nv_bfloat16 *Oext, int ldx, cudaStream_t s) {
   const int N = (int)p.N;
   const int blocks = (int)((ld + 31) / 32);
   const float qmax = p.wbits == 4 ? 8.f : 128.f;
@@ -186,11 +227,12 @@ cudaError_t launch_so_prep(const Problem &p, int64_t ld, int16_t *e_col, uint32_
   if (p.dtype == WQ_BF16)
     so_prep_kernel<WQ_BF16><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(p.scale),
                                                    static_cast<const __nv_bfloat16 *>(p.offset),
-                                                   (int)p.G, N, (int)ld, qmax, int4, e_col, S16, O16);
+                                                   (int)p.G, N, (int)ld, qmax, int4, e_col, S16,
+                                                   Oext, ldx);
   else
     so_prep_kernel<WQ_F16><<<blocks, 256, 0, s>>>(static_cast<const __half *>(p.scale),
                                                   static_cast<const __half *>(p.offset), (int)p.G,
-                                                  N, (int)ld, qmax, int4, e_col, S16, O16);
+                                                  N, (int)ld, qmax, int4, e_col, S16, Oext, ldx);
   return cudaGetLastError();
 }
 
