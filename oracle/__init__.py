@@ -8,7 +8,9 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
 reference leg may use it.
 
 Pages followed (Ascend CANN operator docs): ``aclnnConvertWeightToINT4Pack``
-(function description: sparse INT32 -> dense INT4), ``aclnnDynamicQuant``
+(function description: sparse INT32 -> dense INT4, and its option of a
+matrix-unit tiled output, for which the library defines its own tiled
+layout), ``aclnnDynamicQuant``
 (constraints: INT4 packs along the last dimension), and
 ``aclnnWeightQuantMatmulAllReduceAddRmsNorm`` (function description: formula;
 constraints: scale/offset shapes, group size). Every function is pinned by
@@ -51,8 +53,12 @@ def _load(path=None):
         lib.wqo_dequant.argtypes = [P, I, I, P, P, I, I, I, P]
         lib.wqo_matmul_add_rmsnorm.argtypes = [P, I, I, P, I, P, P, I, I, I, P, P, P,
                                                ctypes.c_double, P, P, P]
+        lib.wqo_tiled_bytes.argtypes = [I, I]
+        lib.wqo_tiled_bytes.restype = I
+        lib.wqo_pack_int4_tiled.argtypes = [P, I, I, P]
+        lib.wqo_unpack_int4_tiled.argtypes = [P, I, I, P]
         for f in (lib.wqo_pack_int4, lib.wqo_unpack_int4, lib.wqo_dequant,
-                  lib.wqo_matmul_add_rmsnorm):
+                  lib.wqo_matmul_add_rmsnorm, lib.wqo_pack_int4_tiled, lib.wqo_unpack_int4_tiled):
             f.restype = ctypes.c_int
         if path is not None:
             return lib
@@ -120,6 +126,30 @@ def unpack_int4(b, N: int) -> np.ndarray:
     rc = _load().wqo_unpack_int4(_p(b), K, N, _p(out))
     if rc:
         raise ValueError("wqo_unpack_int4 rejected its shape")
+    return out
+
+
+def pack_int4_tiled(v) -> np.ndarray:
+    """(K, N) int32 -> the kernel-native tiled INT4 bytes (N % 16 == 0; K padded to 64
+    with zero nibbles), as defined in wq_oracle.c."""
+    v = _i32(v)
+    K, N = v.shape
+    out = np.empty(int(_load().wqo_tiled_bytes(K, N)), dtype=np.uint8)
+    rc = _load().wqo_pack_int4_tiled(_p(v), K, N, _p(out))
+    if rc:
+        raise ValueError(f"wqo_pack_int4_tiled rejected shape {v.shape}")
+    return out
+
+
+def unpack_int4_tiled(b, K: int, N: int) -> np.ndarray:
+    """Tiled INT4 bytes -> (K, N) int32 in [-8, 7]."""
+    if hasattr(b, "detach"):
+        b = b.detach().to("cpu").numpy()
+    b = np.ascontiguousarray(np.asarray(b, dtype=np.uint8).reshape(-1))
+    out = np.empty((K, N), dtype=np.int32)
+    rc = _load().wqo_unpack_int4_tiled(_p(b), K, N, _p(out))
+    if rc:
+        raise ValueError("wqo_unpack_int4_tiled rejected its shape")
     return out
 
 

@@ -175,3 +175,64 @@ int wqo_matmul_add_rmsnorm(const double *x1, int64_t M, int64_t K,
     free(acc);
     return WQO_OK;
 }
+
+/* Kernel-native tiled INT4 layout (the library's analogue of the pack page's
+ * FRACTAL_NZ output option, aclnnConvertWeightToINT4Pack "Function
+ * description": the same pack, re-tiled for the matrix unit; the pages do not
+ * fix a tiled layout, so this is the library's own definition).
+ *
+ * A (K, N) weight, N % 16 == 0, is cut into tiles of 64 k-rows x 16 columns;
+ * tile (s, c) (k-rows 64s.., columns 16c..) takes the 512 bytes at
+ * (s * N/16 + c) * 512, tiles of one 64-row slab in column order. K is padded
+ * with zero nibbles up to a multiple of 64. Inside a tile, element (kk, cc) =
+ * (k - 64s, n - 16c) goes to
+ *     h = kk / 32, t = (kk % 32) / 8, jl = (kk % 8) / 4, e = kk % 4,
+ *     g = cc % 8, upper = cc / 8,
+ *     lane = 4g + t, word j = 2h + jl,
+ *     nibble p = (e < 2 ? 0 : 2) + upper + 4 * (e % 2),
+ *     byte lane*16 + j*4 + p/2, bits 4*(p%2)+3 : 4*(p%2)
+ * and holds the low four bits of the value (reading c3), like the ND pack. */
+static int64_t tiled_offset(int64_t k, int64_t n, int64_t N, int *shift)
+{
+    int64_t s = k / 64, c = n / 16, kk = k % 64, cc = n % 16;
+    int64_t h = kk / 32, t = (kk % 32) / 8, jl = (kk % 8) / 4, e = kk % 4;
+    int64_t g = cc % 8, upper = cc / 8;
+    int64_t lane = 4 * g + t, j = 2 * h + jl;
+    int64_t p = (e < 2 ? 0 : 2) + upper + 4 * (e % 2);
+    *shift = (int)(4 * (p % 2));
+    return (s * (N / 16) + c) * 512 + lane * 16 + j * 4 + p / 2;
+}
+
+/* Bytes of the tiled layout of a (K, N) weight: ceil(K/64) * 64 * N / 2. */
+int64_t wqo_tiled_bytes(int64_t K, int64_t N)
+{
+    return (K + 63) / 64 * 64 * N / 2;
+}
+
+/* Pack v (K, N) int32 into the tiled layout; out holds wqo_tiled_bytes bytes. */
+int wqo_pack_int4_tiled(const int32_t *v, int64_t K, int64_t N, uint8_t *out)
+{
+    if (K < 0 || N < 0 || (N % 16) != 0) return WQO_EINVAL;
+    memset(out, 0, (size_t)wqo_tiled_bytes(K, N));
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t n = 0; n < N; ++n) {
+            int shift;
+            int64_t b = tiled_offset(k, n, N, &shift);
+            out[b] |= (uint8_t)(((uint32_t)v[k * N + n] & 0xFu) << shift);
+        }
+    return WQO_OK;
+}
+
+/* Inverse: tiled bytes -> (K, N) int32 values in [-8, 7]. */
+int wqo_unpack_int4_tiled(const uint8_t *b, int64_t K, int64_t N, int32_t *out)
+{
+    if (K < 0 || N < 0 || (N % 16) != 0) return WQO_EINVAL;
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t n = 0; n < N; ++n) {
+            int shift;
+            int64_t o = tiled_offset(k, n, N, &shift);
+            int32_t nib = (b[o] >> shift) & 0xF;
+            out[k * N + n] = nib >= 8 ? nib - 16 : nib;
+        }
+    return WQO_OK;
+}

@@ -71,6 +71,83 @@ def test_pack_roundtrip_random_and_int32_view():
             np.testing.assert_array_equal(nib, expect)
 
 
+def _read_tiled_literals():
+    rows = []
+    with open(os.path.join(GOLDEN, "tiled_literals.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            lhs, rhs = line.split("->")
+            K, N, k, n, v = (int(x) for x in lhs.split())
+            bi, bv = rhs.split()
+            rows.append((K, N, k, n, v, int(bi), int(bv, 16)))
+    return rows
+
+
+@pytest.mark.parametrize("K,N,k,n,v,byte,value", _read_tiled_literals())
+def test_tiled_pack_literals(K, N, k, n, v, byte, value):
+    w = np.zeros((K, N), dtype=np.int32)
+    w[k, n] = v
+    b = oracle.pack_int4_tiled(w)
+    assert b.size == (K + 63) // 64 * 64 * N // 2
+    assert np.nonzero(b)[0].tolist() == [byte]
+    assert int(b[byte]) == value
+
+
+def test_tiled_roundtrip_and_same_nibbles_as_nd():
+    rng = np.random.default_rng(11)
+    for K, N in ((64, 16), (100, 48), (130, 32), (1, 16)):
+        v = rng.integers(-8, 8, size=(K, N), dtype=np.int32)
+        t = oracle.pack_int4_tiled(v)
+        np.testing.assert_array_equal(oracle.unpack_int4_tiled(t, K, N), v)
+        # a permutation of the ND pack's nibbles, padded with zero nibbles
+        nd = oracle.pack_int4(v).reshape(-1)
+        nib = lambda b: np.sort(np.concatenate([b & 0xF, b >> 4]))
+        pad = t.size * 2 - nd.size * 2
+        np.testing.assert_array_equal(nib(t), np.sort(np.concatenate([nib(nd), np.zeros(pad, np.uint8)])))
+
+
+def test_tiled_layout_feeds_the_m16n8k16_fragments():
+    """What the layout is for: lane l's word j of a tile is the A fragment
+    (A = W^T, 16 columns x 16 k) of the tile's MMA j, in the PTX ISA's m16n8k16
+    register map -- a0 = A[g][2t..2t+1], a1 = A[g+8][2t..], a2 = A[g][2t+8..],
+    a3 = A[g+8][2t+8..], register i holding nibble i (low half) and nibble i+4
+    (high half) -- when MMA j's k index kk maps to k-row 32(j/2) + 4(j%2) + 8t +
+    e with e = kk % 2 (kk < 8) or 2 + kk % 2 (kk >= 8). Summing the four MMAs of
+    a tile must then give W_tile^T @ x for any x."""
+    rng = np.random.default_rng(5)
+    K, N = 64, 32
+    v = rng.integers(-8, 8, size=(K, N), dtype=np.int32)
+    x = rng.standard_normal((K, 8))
+    tb = oracle.pack_int4_tiled(v)
+    for c in range(N // 16):
+        tile = tb[c * 512:(c + 1) * 512].reshape(32, 4, 4)  # lane, word, byte
+        out = np.zeros((16, 8))
+        for j in range(4):
+            A = np.zeros((16, 16))
+            Bm = np.zeros((16, 8))
+            for lane in range(32):
+                g, t = lane // 4, lane % 4
+                w = int.from_bytes(bytes(tile[lane, j]), "little")
+                nib = [(w >> (4 * i)) & 0xF for i in range(8)]
+                sv = [q - 16 if q >= 8 else q for q in nib]
+                A[g, 2 * t], A[g, 2 * t + 1] = sv[0], sv[4]
+                A[g + 8, 2 * t], A[g + 8, 2 * t + 1] = sv[1], sv[5]
+                A[g, 2 * t + 8], A[g, 2 * t + 9] = sv[2], sv[6]
+                A[g + 8, 2 * t + 8], A[g + 8, 2 * t + 9] = sv[3], sv[7]
+                base = 32 * (j // 2) + 4 * (j % 2) + 8 * t
+                for e, kk in ((0, 2 * t), (1, 2 * t + 1), (2, 2 * t + 8), (3, 2 * t + 9)):
+                    Bm[kk] = x[base + e]
+            out += A @ Bm
+        np.testing.assert_allclose(out, v[:, 16 * c:16 * c + 16].T.astype(float) @ x, atol=1e-9)
+
+
+def test_tiled_rejects_n_not_multiple_of_16():
+    with pytest.raises(ValueError):
+        oracle.pack_int4_tiled(np.zeros((64, 24), np.int32))
+
+
 def test_pack_rejects_odd_n():
     with pytest.raises(ValueError):
         oracle.pack_int4(np.zeros((2, 3), np.int32))

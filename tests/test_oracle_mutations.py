@@ -29,6 +29,11 @@ MUTATIONS = {
     "gamma_reversed": ("yv / rms * gamma[n]", "yv / rms * gamma[N - 1 - n]"),
     "x_reversed_k": ("double xk = x1[m * K + k];", "double xk = x1[m * K + (K - 1 - k)];"),
     "weight_row_shifted": ("double wk = (double)q[k * N + n]", "double wk = (double)q[((k + 1) % K) * N + n]"),
+    "tiled_t_and_jl_swapped": ("int64_t h = kk / 32, t = (kk % 32) / 8, jl = (kk % 8) / 4, e = kk % 4;",
+                               "int64_t h = kk / 32, jl = (kk % 32) / 16, t = (kk % 16) / 4, e = kk % 4;"),
+    "tiled_upper_nibble_pairs": ("int64_t p = (e < 2 ? 0 : 2) + upper + 4 * (e % 2);",
+                                 "int64_t p = (e < 2 ? 0 : 4) + upper + 2 * (e % 2);"),
+    "tiled_word_major_in_tile": ("* 512 + lane * 16 + j * 4 + p / 2;", "* 512 + j * 128 + lane * 4 + p / 2;"),
 }
 
 
