@@ -231,8 +231,8 @@ int wqo_unpack_int4_tiled(const uint8_t *b, int64_t K, int64_t N, int32_t *out)
         for (int64_t n = 0; n < N; ++n) {
             int shift;
             int64_t o = tiled_offset(k, n, N, &shift);
-            int32_t nib = (b[o] >> shift) & 0xF;
-            out[k * N + n] = nib >= 8 ? nib - 16 : nib;
+            int32_t u = (b[o] >> shift) & 0xF;
+            out[k * N + n] = u < 8 ? u : u - 16;
         }
     return WQO_OK;
 }
