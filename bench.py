@@ -75,6 +75,7 @@ def parse_args():
 
 def make_problem(config: str, device):
     from weight_only_bit_pack_b300 import inputs
+    config = config.split("@")[0]  # "@tiled": same workload, weight in the tiled layout
     if config in inputs.CONFIGS:
         return inputs.CONFIGS[config](device)
     if config.startswith("sweep_pt:"):
@@ -304,10 +305,13 @@ class Runner:
     """R distinct input sets of one workload on the device (weights packed once,
     then copied), a zeroed workspace, and step(i) = one C-ABI call on set i % R."""
 
-    def __init__(self, wq, p, kernel, dev, stream):
-        self.p, self.kernel, self.stream = p, kernel, stream
+    def __init__(self, wq, p, kernel, dev, stream, tiled=False):
+        self.p, self.kernel, self.stream, self.tiled = p, kernel, stream, tiled
         self.w_src = p.x2
-        self.w0 = wq.pack_int4(p.x2) if p.wbits == 4 else p.x2.contiguous()
+        if tiled:
+            self.w0 = wq.pack_int4_tiled(p.x2)
+        else:
+            self.w0 = wq.pack_int4(p.x2) if p.wbits == 4 else p.x2.contiguous()
         self.ab = alg_bytes(p)
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         self.set_bytes = self.ab["total"]
@@ -315,7 +319,9 @@ class Runner:
         self.R = max(1, min(R, 64))
         self.sets = []
         for i in range(self.R):
-            s = {"x1": p.x1.clone(), "w": self.w0.clone(), "scale": p.scale.clone(),
+            w = (wq.TiledInt4(self.w0.data.clone(), self.w0.K, self.w0.N) if tiled
+                 else self.w0.clone())
+            s = {"x1": p.x1.clone(), "w": w, "scale": p.scale.clone(),
                  "offset": None if p.offset is None else p.offset.clone(),
                  "bias": None if p.bias is None else p.bias.clone(),
                  "residual": p.residual.clone(), "gamma": p.gamma.clone(),
@@ -383,7 +389,7 @@ def time_extra(wq, config, dev, stream, steps, warmup, peaks):
     """Device time of one named workload (graph replay, CUDA events), for the
     line's "workloads" key."""
     p = make_problem(config, dev)
-    r = Runner(wq, p, 0, dev, stream)
+    r = Runner(wq, p, 0, dev, stream, tiled=config.endswith("@tiled"))
     for i in range(warmup):
         r.step(i)
     graphs = capture_graphs(r, steps)
@@ -399,7 +405,8 @@ def time_extra(wq, config, dev, stream, steps, warmup, peaks):
     torch.cuda.synchronize(dev)
     ms = ev0.elapsed_time(ev1) / steps
     roof = roofline(p, ms, peaks)
-    out = {"workload": p.name, "M": p.M, "K": p.K, "N": p.N, "kernel":
+    out = {"workload": p.name + ("_tiled" if r.tiled else ""), "M": p.M, "K": p.K, "N": p.N,
+           "kernel":
            ["auto", "generic", "decode", "prefill"][r.chosen], "steps": steps, "ms_per_step": ms,
            "TFLOP/s": 2.0 * p.M * p.K * p.N / (ms * 1e-3) / 1e12,
            "weight_GBps": r.ab["weight"] / (ms * 1e-3) / 1e9,
@@ -410,7 +417,8 @@ def time_extra(wq, config, dev, stream, steps, warmup, peaks):
     return out
 
 
-EXTRA = (("decode", 2000), ("sweep:1", 1000), ("sweep:16", 1000), ("w8a16", 50), ("prefill", 20))
+EXTRA = (("decode", 2000), ("decode@tiled", 2000), ("sweep:1", 1000), ("sweep:1@tiled", 1000),
+         ("sweep:16", 1000), ("sweep:16@tiled", 1000), ("w8a16", 50), ("prefill", 20))
 
 
 def traffic_record(kernel_name, workload):
@@ -451,7 +459,7 @@ def run_ours(args, world, rank, local):
 
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.set_stream(stream)
-    runner = Runner(wq, p, kernel, dev, stream)
+    runner = Runner(wq, p, kernel, dev, stream, tiled=args.config.endswith("@tiled"))
     w_src, w0, ab, R, sets = runner.w_src, runner.w0, runner.ab, runner.R, runner.sets
     chosen = runner.chosen
     step = runner.step
@@ -600,22 +608,29 @@ def run_ours(args, world, rank, local):
     # INT32 -> INT4 pack of this workload's weight (once per weight in deployment)
     pack = None
     if not args.no_pack and p.wbits == 4:
-        out = torch.empty_like(w0)
+        if runner.tiled:
+            out = wq.TiledInt4(torch.empty_like(w0.data), w0.K, w0.N)
+            pack_fn = lambda: wq.pack_int4_tiled(w_src, out=out, stream=stream)  # noqa: E731
+        else:
+            out = torch.empty_like(w0)
+            pack_fn = lambda: wq.pack_int4(w_src, out=out, stream=stream)  # noqa: E731
         for _ in range(3):
-            wq.pack_int4(w_src, out=out, stream=stream)
+            pack_fn()
         torch.cuda.synchronize(dev)
         reps = 20
         ev0.record(stream)
         for _ in range(reps):
-            wq.pack_int4(w_src, out=out, stream=stream)
+            pack_fn()
         ev1.record(stream)
         torch.cuda.synchronize(dev)
         tp = ev0.elapsed_time(ev1) / reps
-        pbytes = w_src.numel() * 4 + out.numel()
+        ob = out.data if runner.tiled else out
+        pbytes = w_src.numel() * 4 + ob.numel()
         peaks, _src = load_peaks()
-        pack = {"ms": tp, "GB/s": pbytes / (tp * 1e-3) / 1e9, "bytes": pbytes,
+        pack = {"layout": "tiled" if runner.tiled else "dense", "ms": tp,
+                "GB/s": pbytes / (tp * 1e-3) / 1e9, "bytes": pbytes,
                 "frac_of_measured_hbm": pbytes / (tp * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                "bit_exact": bool(torch.equal(out, w0))}
+                "bit_exact": bool(torch.equal(ob, w0.data if runner.tiled else w0))}
 
     peaks, peak_src = load_peaks()
     roof = roofline(p, ms_step, peaks)

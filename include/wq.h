@@ -50,13 +50,28 @@ extern "C" {
  * per row; the element in even column 2j sits in bits 3:0 of byte j and the
  * element in column 2j+1 in bits 7:4 (the pages do not fix this order; this is
  * the library's reading). Read as little-endian int32 words, element 8i+t of a
- * row sits in bits 4t+3:4t of word i. */
+ * row sits in bits 4t+3:4t of word i.
+ *
+ * WQ_INT4_TILED is the same 4-bit values of a 2-D (K, N) weight, N % 16 == 0,
+ * in the library's kernel-native tiled layout (the analogue of the pack page's
+ * matrix-unit output format, aclnnConvertWeightToINT4Pack "Function
+ * description"; the pages fix no layout for this GPU). The weight is cut into
+ * tiles of 64 k-rows x 16 columns; tile (s, c) -- k-rows 64s.., columns 16c.. --
+ * takes the 512 bytes at (s * N/16 + c) * 512, and K is padded with zero
+ * nibbles to a multiple of 64 (ceil(K/64) * 64 * N / 2 bytes in all). Inside a
+ * tile, element (kk, cc) = (k - 64s, n - 16c) takes nibble p of 32-bit word j of
+ * 16-byte lane l: l = 4 (cc % 8) + (kk % 32) / 8, j = 2 (kk / 32) + (kk % 8) / 4,
+ * p = (e < 2 ? 0 : 2) + cc / 8 + 4 (e % 2) with e = kk % 4, i.e. byte
+ * l*16 + j*4 + p/2, bits 4(p%2)+3 : 4(p%2). Lane l's 16 bytes are then exactly
+ * its A-operand registers (A = W^T) of four m16n8k16 MMAs. Tiled tensors must be
+ * 16-byte aligned. */
 typedef enum wq_dtype {
     WQ_F16 = 1,
     WQ_BF16 = 2,
     WQ_INT8 = 3,
     WQ_INT4 = 4,
-    WQ_INT32 = 5
+    WQ_INT32 = 5,
+    WQ_INT4_TILED = 6
 } wq_dtype;
 
 /* Tensor descriptor (the analogue of aclTensor): pointer, element type, rank
@@ -97,7 +112,8 @@ typedef enum wq_kernel {
  *   weight       WQ_INT32, 2-D (K, N), N even, K >= 0, N >= 0. Values should lie
  *                in [-8, 7]; any other value keeps its low four bits (two's
  *                complement truncation).
- *   weight_int4  WQ_INT4, 2-D, logical shape (K, N), i.e. K*N/2 bytes.
+ *   weight_int4  WQ_INT4, 2-D, logical shape (K, N), i.e. K*N/2 bytes; or
+ *                WQ_INT4_TILED (N % 16 == 0, 16-byte aligned), the tiled layout.
  *   ws_bytes     out: workspace bytes the second phase needs (always 0).
  * Errors: WQ_ERR_NULL, WQ_ERR_DTYPE, WQ_ERR_SHAPE. Touches no device memory. */
 int32_t wq_pack_int4_get_workspace(const wq_tensor *weight, const wq_tensor *weight_int4,
@@ -109,13 +125,26 @@ int32_t wq_pack_int4_get_workspace(const wq_tensor *weight, const wq_tensor *wei
 int32_t wq_pack_int4(const wq_tensor *weight, const wq_tensor *weight_int4,
                      void *ws, uint64_t ws_bytes, void *stream);
 
+/* Converts a 2-D (K, N) INT4 weight between the dense layout (WQ_INT4) and the
+ * tiled layout (WQ_INT4_TILED), in the direction the two dtypes give; both
+ * descriptors carry the logical shape, N % 16 == 0, the tiled one 16-byte
+ * aligned. The padding nibbles of a tiled output are zero. Bit-exact,
+ * asynchronous on `stream`, no workspace. Errors: WQ_ERR_NULL, WQ_ERR_DTYPE,
+ * WQ_ERR_SHAPE, WQ_ERR_UNSUPPORTED (alignment), WQ_ERR_ALIAS, WQ_ERR_CUDA.
+ * (aclnnConvertWeightToINT4Pack, "Function description": the ND to tiled
+ * conversion of the pack's output format; the tiled to ND direction serves
+ * checking and re-use of the weight elsewhere.) */
+int32_t wq_convert_int4_layout(const wq_tensor *src, const wq_tensor *dst, void *stream);
+
 /* ------------------------------------------------------------------ matmul */
 
 /* First phase of the fused operator (aclnnWeightQuantMatmulAllReduceAddRmsNorm).
  *   x1        WQ_F16 or WQ_BF16, (M, K) or (b, s, K) with M = b*s; 0 <= M < 2^31,
  *             1 <= K <= 65535. Not transposed.
- *   x2        WQ_INT8 (K, N) or WQ_INT4 (K, N) packed as described above (N even);
- *             0 <= N <= 65535. Not transposed.
+ *   x2        WQ_INT8 (K, N) or WQ_INT4 (K, N) packed as described above (N even),
+ *             or WQ_INT4_TILED (K, N) (N % 16 == 0, 16-byte aligned);
+ *             0 <= N <= 65535. Not transposed. A tiled weight runs on the tiled
+ *             decode kernel for M <= 16 and on the generic kernel otherwise.
  *   scale     antiquantScale, x1's dtype: (1) per-tensor, (N) or (1, N)
  *             per-channel, (ceil(K/group), N) per-group.
  *   offset    antiquantOffset or NULL; if given, the scale's shape and dtype.

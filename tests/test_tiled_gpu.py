@@ -1,0 +1,142 @@
+"""Kernel-native tiled INT4 layout on the GPU: the pack into it and the layout
+conversions (bit-exact against the oracle's restatement of the layout), and the
+tiled decode kernel (against the fp64 oracle, like every other kernel).
+
+The layout is the library's analogue of the pack's matrix-unit output
+(aclnnConvertWeightToINT4Pack, "Function description"), defined in
+include/wq.h; the operator it feeds is the one of
+aclnnWeightQuantMatmulAllReduceAddRmsNorm.
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from weight_only_bit_pack_b300 import inputs
+from parity_util import compare, run_oracle, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+AUTO, GENERIC, DECODE, PREFILL = 0, 1, 2, 3
+
+
+@pytest.mark.parametrize("K,N", [(64, 16), (100, 48), (256, 128), (4096, 4096), (8192, 28672),
+                                 (33, 4112)])
+def test_pack_tiled_bit_exact_and_conversions(wq, K, N):
+    g = torch.Generator().manual_seed(K * 7 + N)
+    v = torch.randint(-8, 8, (K, N), generator=g, dtype=torch.int32)
+    if K * N < 1 << 20:  # out-of-range int32 keep their low four bits, as in the ND pack
+        v[0, :4] = torch.tensor([100, -100, 2 ** 30, -(2 ** 31)], dtype=torch.int32)
+    vd = v.cuda()
+    t = wq.pack_int4_tiled(vd)
+    ref = oracle.pack_int4_tiled(v)
+    assert np.array_equal(t.data.cpu().numpy(), ref)
+    nd = wq.pack_int4(vd)
+    assert torch.equal(wq.int4_to_tiled(nd).data, t.data)          # ND -> tiled
+    assert torch.equal(wq.tiled_to_int4(t), nd)                    # tiled -> ND
+    torch.cuda.synchronize()
+
+
+def _tiled_problem(prob):
+    return prob, wq_tiled(prob)
+
+
+def wq_tiled(prob):
+    import weight_only_bit_pack_b300 as wq
+    return wq.pack_int4_tiled(prob.x2.to("cuda").contiguous())
+
+
+def _run(wq, prob, w, kernel, **kw):
+    y, no = wq.matmul_add_rmsnorm(prob.x1, w, prob.scale, prob.offset, prob.bias, prob.residual,
+                                  prob.gamma, prob.eps, prob.group, kernel=kernel, **kw)
+    torch.cuda.synchronize()
+    return y, no
+
+
+@pytest.mark.parametrize("cfg", ["tiny", "decode", "sweep1", "sweep16"])
+def test_named_workloads_tiled(wq, cfg):
+    if cfg == "tiny":
+        from parity_util import to_device
+        prob = to_device(inputs.tiny())
+    elif cfg == "decode":
+        prob = inputs.decode("cuda")
+    else:
+        prob = inputs.sweep(int(cfg[5:]), device="cuda")
+    w = wq_tiled(prob)
+    assert wq.select_kernel(prob.x1, w, prob.scale, prob.offset, prob.bias, prob.residual,
+                            prob.gamma, prob.eps, prob.group) == wq.Kernel.DECODE
+    y, no = _run(wq, prob, w, AUTO)
+    compare(prob, y, no, run_oracle(prob))
+
+
+CASES = [
+    ("m1_channel", dict(M_shape=(1,), K=512, N=256, dtype=torch.bfloat16, mode="channel")),
+    ("m3_tensor_offset", dict(M_shape=(3,), K=192, N=48, dtype=torch.float16, mode="tensor")),
+    ("m5_group32_ragged_k", dict(M_shape=(5,), K=200, N=96, dtype=torch.bfloat16, mode="group",
+                                 group=32)),
+    ("m7_group96", dict(M_shape=(7,), K=960, N=320, dtype=torch.bfloat16, mode="group",
+                        group=96)),
+    ("m8_group64_nooffset", dict(M_shape=(8,), K=1024, N=1024, dtype=torch.bfloat16,
+                                 mode="group", group=64, offset=False)),
+    ("m9_fp16_group128", dict(M_shape=(9,), K=2048, N=512, dtype=torch.float16, mode="group",
+                              group=128)),
+    ("m12_channel2d_nobias", dict(M_shape=(3, 4), K=1024, N=2064, dtype=torch.bfloat16,
+                                  mode="channel2d", bias=False)),
+    ("m16_group32", dict(M_shape=(2, 8), K=4096, N=768, dtype=torch.bfloat16, mode="group",
+                         group=32)),
+    ("k8_single_rows", dict(M_shape=(4,), K=8, N=16, dtype=torch.float16, mode="channel")),
+    ("wide_n_20000", dict(M_shape=(6,), K=256, N=20000, dtype=torch.float16, mode="channel")),
+    ("long_k_65528", dict(M_shape=(2,), K=65528, N=64, dtype=torch.bfloat16, mode="group",
+                          group=256, offset=False)),
+    ("max_n_65520", dict(M_shape=(1,), K=64, N=65520, dtype=torch.bfloat16, mode="group",
+                         group=32)),
+]
+
+
+@pytest.mark.parametrize("name,kw", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("kernel", [DECODE, GENERIC])
+def test_tiled_kernels_vs_oracle(wq, name, kw, kernel):
+    prob = inputs.make_problem(**kw, wbits=4, seed=zlib.crc32(name.encode()) % 1000,
+                               device="cuda", name=name)
+    w = wq_tiled(prob)
+    y, no = _run(wq, prob, w, kernel)
+    compare(prob, y, no, run_oracle(prob))
+
+
+def test_tiled_auto_above_16_rows_runs_generic(wq):
+    prob = inputs.make_problem(M_shape=(40,), K=256, N=128, dtype=torch.bfloat16, wbits=4,
+                               mode="group", group=64, seed=3, device="cuda", name="tiled_m40")
+    w = wq_tiled(prob)
+    assert wq.select_kernel(prob.x1, w, prob.scale, prob.offset, prob.bias, prob.residual,
+                            prob.gamma, prob.eps, prob.group) == wq.Kernel.GENERIC
+    y, no = _run(wq, prob, w, AUTO)
+    compare(prob, y, no, run_oracle(prob))
+
+
+def test_tiled_decode_deterministic_and_reusable_workspace(wq):
+    prob = inputs.sweep(16, device="cuda")
+    w = wq_tiled(prob)
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    a = _run(wq, prob, w, AUTO, workspace=ws)
+    b = _run(wq, prob, w, AUTO, workspace=ws)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    assert wq.read_device_status(ws) == 0
+    assert int(ws[:2048].sum()) == 0  # grid counters back at zero
+
+
+def test_tiled_decode_timeout_path(wq):
+    prob = inputs.decode("cuda")
+    w = wq_tiled(prob)
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    wq.set_wait_limits_for_testing(2_000_000, 1)
+    try:
+        _run(wq, prob, w, AUTO, workspace=ws)
+        st = wq.read_device_status(ws)
+    finally:
+        wq.set_wait_limits_for_testing(0, 0)
+    assert st & 0xFF == 8 and st >> 8 == wq.WHERE_DECODE_GRID, hex(st)
+    ws[:2048].zero_()
+    y, no = _run(wq, prob, w, AUTO, workspace=ws, check_status=True)
+    compare(prob, y, no, run_oracle(prob))

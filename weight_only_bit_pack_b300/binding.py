@@ -7,7 +7,9 @@ is no fallback: if the library cannot be loaded, importing this module raises.
 
 Tensor conventions: fp16/bf16 tensors map to WQ_F16/WQ_BF16, ``torch.int8`` to
 WQ_INT8, ``torch.int32`` to WQ_INT32, and a ``torch.uint8`` tensor of shape
-(K, N/2) is read as packed WQ_INT4 of logical shape (K, N).
+(K, N/2) is read as packed WQ_INT4 of logical shape (K, N). A weight in the
+kernel-native tiled layout is a :class:`TiledInt4` (its bytes plus the logical
+(K, N)), described as WQ_INT4_TILED.
 """
 from __future__ import annotations
 
@@ -52,6 +54,7 @@ class DType(enum.IntEnum):
     INT8 = 3
     INT4 = 4
     INT32 = 5
+    INT4_TILED = 6
 
 
 class WQError(RuntimeError):
@@ -65,10 +68,29 @@ class WqTensor(ctypes.Structure):
                 ("shape", ctypes.c_int64 * 3)]
 
 
+class TiledInt4:
+    """A (K, N) INT4 weight in the kernel-native tiled layout: ``data`` holds its
+    ceil(K/64) * 64 * N / 2 bytes (uint8, 16-byte aligned)."""
+
+    def __init__(self, data: torch.Tensor, K: int, N: int):
+        if data.dtype != torch.uint8 or data.numel() != tiled_bytes(K, N):
+            raise ValueError(f"a tiled ({K}, {N}) INT4 weight holds {tiled_bytes(K, N)} uint8 bytes")
+        self.data, self.K, self.N = data, int(K), int(N)
+
+    @property
+    def device(self):
+        return self.data.device
+
+
+def tiled_bytes(K: int, N: int) -> int:
+    return (K + 63) // 64 * 64 * N // 2
+
+
 _P = ctypes.POINTER(WqTensor)
 _T = [_P] * 7 + [ctypes.c_double, ctypes.c_int64, _P, _P]
 lib.wq_pack_int4_get_workspace.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint64)]
 lib.wq_pack_int4.argtypes = [_P, _P, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
+lib.wq_convert_int4_layout.argtypes = [_P, _P, ctypes.c_void_p]
 lib.wq_matmul_add_rmsnorm_get_workspace.argtypes = _T + [ctypes.POINTER(ctypes.c_uint64)]
 lib.wq_matmul_add_rmsnorm.argtypes = _T + [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
 lib.wq_matmul_add_rmsnorm_get_workspace_ex.argtypes = _T + [ctypes.c_int32,
@@ -91,7 +113,8 @@ for _f in ("wq_pack_int4_get_workspace", "wq_pack_int4", "wq_matmul_add_rmsnorm_
            "wq_matmul_add_rmsnorm", "wq_matmul_add_rmsnorm_get_workspace_ex",
            "wq_matmul_add_rmsnorm_ex", "wq_matmul_add_rmsnorm_select_kernel",
            "wq_read_device_status", "wq_version", "wq_matmul_add_rmsnorm_noalloc",
-           "wq_check_device_timeout", "wq_noalloc_read_device_status", "wq_test_set_wait_limits"):
+           "wq_check_device_timeout", "wq_noalloc_read_device_status", "wq_test_set_wait_limits",
+           "wq_convert_int4_layout"):
     getattr(lib, _f).restype = ctypes.c_int32
 
 _TORCH2WQ = {torch.float16: DType.F16, torch.bfloat16: DType.BF16, torch.int8: DType.INT8,
@@ -107,6 +130,13 @@ def describe(t: Optional[torch.Tensor], dtype: Optional[int] = None, shape=None)
     """wq_tensor for a contiguous torch tensor (None -> NULL)."""
     if t is None:
         return None
+    if isinstance(t, TiledInt4):
+        d = WqTensor()
+        d.data = t.data.data_ptr()
+        d.dtype = int(DType.INT4_TILED)
+        d.ndim = 2
+        d.shape[0], d.shape[1] = t.K, t.N
+        return d
     if not t.is_contiguous():
         raise ValueError("wq tensors must be contiguous")
     d = WqTensor()
@@ -147,6 +177,36 @@ def pack_int4(weight: torch.Tensor, out: Optional[torch.Tensor] = None, stream=N
     ws = ctypes.c_uint64(0)
     _check(lib.wq_pack_int4_get_workspace(_ref(wd), _ref(od), ctypes.byref(ws)))
     _check(lib.wq_pack_int4(_ref(wd), _ref(od), None, 0, _stream(stream)))
+    return out
+
+
+def pack_int4_tiled(weight: torch.Tensor, out: Optional[TiledInt4] = None,
+                    stream=None) -> TiledInt4:
+    """(K, N) int32 -> the kernel-native tiled INT4 layout, on the GPU (``wq_pack_int4``
+    with a WQ_INT4_TILED output; N % 16 == 0)."""
+    K, N = weight.shape
+    if out is None:
+        out = TiledInt4(torch.empty(tiled_bytes(K, N), dtype=torch.uint8, device=weight.device),
+                        K, N)
+    wd, od = describe(weight), describe(out)
+    ws = ctypes.c_uint64(0)
+    _check(lib.wq_pack_int4_get_workspace(_ref(wd), _ref(od), ctypes.byref(ws)))
+    _check(lib.wq_pack_int4(_ref(wd), _ref(od), None, 0, _stream(stream)))
+    return out
+
+
+def int4_to_tiled(w4: torch.Tensor, stream=None) -> TiledInt4:
+    """Dense packed INT4 (K, N/2) uint8 -> tiled layout (``wq_convert_int4_layout``)."""
+    K, N = w4.shape[0], w4.shape[1] * 2
+    out = TiledInt4(torch.empty(tiled_bytes(K, N), dtype=torch.uint8, device=w4.device), K, N)
+    _check(lib.wq_convert_int4_layout(_ref(describe(w4)), _ref(describe(out)), _stream(stream)))
+    return out
+
+
+def tiled_to_int4(t: TiledInt4, stream=None) -> torch.Tensor:
+    """Tiled layout -> dense packed INT4 (K, N/2) uint8 (``wq_convert_int4_layout``)."""
+    out = torch.empty((t.K, t.N // 2), dtype=torch.uint8, device=t.device)
+    _check(lib.wq_convert_int4_layout(_ref(describe(t)), _ref(describe(out)), _stream(stream)))
     return out
 
 

@@ -56,13 +56,17 @@ int64_t elem_bits(int dt) {
   switch (dt) {
     case WQ_F16: case WQ_BF16: return 16;
     case WQ_INT8: return 8;
-    case WQ_INT4: return 4;
+    case WQ_INT4: case WQ_INT4_TILED: return 4;
     case WQ_INT32: return 32;
     default: return 0;
   }
 }
 
-uint64_t nbytes(const wq_tensor *t) { return (uint64_t)((numel(t) * elem_bits(t->dtype) + 7) / 8); }
+uint64_t nbytes(const wq_tensor *t) {
+  if (t->dtype == WQ_INT4_TILED && t->ndim == 2)  // K padded to a multiple of 64
+    return tiled_int4_bytes(t->shape[0], t->shape[1]);
+  return (uint64_t)((numel(t) * elem_bits(t->dtype) + 7) / 8);
+}
 
 bool valid_rank(const wq_tensor *t) {
   if (t->ndim < 1 || t->ndim > 3) return false;
@@ -89,7 +93,8 @@ bool same_shape(const wq_tensor *a, const wq_tensor *b) {
 const char *dtname(int dt) {
   switch (dt) {
     case WQ_F16: return "F16"; case WQ_BF16: return "BF16"; case WQ_INT8: return "INT8";
-    case WQ_INT4: return "INT4"; case WQ_INT32: return "INT32"; default: return "?";
+    case WQ_INT4: return "INT4"; case WQ_INT32: return "INT32";
+    case WQ_INT4_TILED: return "INT4_TILED"; default: return "?";
   }
 }
 
@@ -113,8 +118,8 @@ int32_t validate(const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scal
   const int dt = x1->dtype;
   if (dt != WQ_F16 && dt != WQ_BF16)
     return fail(WQ_ERR_DTYPE, "x1 must be F16 or BF16, got %s", dtname(dt));
-  if (x2->dtype != WQ_INT8 && x2->dtype != WQ_INT4)
-    return fail(WQ_ERR_DTYPE, "x2 must be INT8 or INT4, got %s", dtname(x2->dtype));
+  if (x2->dtype != WQ_INT8 && x2->dtype != WQ_INT4 && x2->dtype != WQ_INT4_TILED)
+    return fail(WQ_ERR_DTYPE, "x2 must be INT8, INT4 or INT4_TILED, got %s", dtname(x2->dtype));
   const wq_tensor *same[] = {scale, offset, bias, residual, gamma, y, normOut};
   const char *snames[] = {"scale", "offset", "bias", "residual", "gamma", "y", "normOut"};
   for (int i = 0; i < 7; ++i)
@@ -143,6 +148,10 @@ int32_t validate(const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scal
   if (N > kMaxKN) return fail(WQ_ERR_SHAPE, "n = %lld exceeds 65535", (long long)N);
   if (x2->dtype == WQ_INT4 && (N % 2) != 0)
     return fail(WQ_ERR_SHAPE, "INT4 x2 needs an even last dimension, got n = %lld", (long long)N);
+  if (x2->dtype == WQ_INT4_TILED && (N % 16) != 0)
+    return fail(WQ_ERR_SHAPE, "INT4_TILED x2 needs n %% 16 == 0, got n = %lld", (long long)N);
+  if (x2->dtype == WQ_INT4_TILED && ((uintptr_t)x2->data % 16) != 0)
+    return fail(WQ_ERR_UNSUPPORTED, "INT4_TILED x2 must be 16-byte aligned");
 
   // scale / group
   int smode;
@@ -223,7 +232,8 @@ int32_t validate(const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scal
   p = Problem();
   p.M = M; p.K = K; p.N = N;
   p.dtype = dt;
-  p.wbits = x2->dtype == WQ_INT4 ? 4 : 8;
+  p.wbits = x2->dtype == WQ_INT8 ? 8 : 4;
+  p.tiled = x2->dtype == WQ_INT4_TILED;
   p.smode = smode; p.group = smode == kPerGroup ? group : 0; p.G = G; p.Ns = Ns;
   p.eps = (float)eps;
   p.x1 = x1->data; p.x2 = x2->data; p.scale = scale->data;
@@ -246,6 +256,21 @@ int32_t make_plan(const Problem &p, int32_t kernel, Plan &plan) {
     return WQ_OK;
   }
   int chosen = kernel;
+  if (p.tiled) {
+    // the tiled layout: the tiled decode kernel for small M, else the generic kernel
+    if (chosen == WQ_KERNEL_AUTO)
+      chosen = (p.M <= 16 && decode_tiled_applicable(p)) ? WQ_KERNEL_DECODE : WQ_KERNEL_GENERIC;
+    if (chosen == WQ_KERNEL_DECODE) {
+      if (!plan_decode_tiled(p, plan))
+        return fail(WQ_ERR_UNSUPPORTED,
+                    "the tiled decode kernel needs 1 <= m <= 16, k %% 8 == 0, 16-byte aligned x1, "
+                    "scale, offset, bias, residual and gamma, 4-byte aligned y and normOut, and at "
+                    "most 32 column groups of 16 per CTA");
+      return WQ_OK;
+    }
+    if (chosen == WQ_KERNEL_PREFILL)
+      return fail(WQ_ERR_UNSUPPORTED, "the prefill kernel does not read the INT4_TILED layout");
+  }
   if (chosen == WQ_KERNEL_AUTO) {
     if (p.M <= 16 && decode_applicable(p))
       chosen = WQ_KERNEL_DECODE;
@@ -346,11 +371,16 @@ const char *wq_last_error(void) { return g_last_error.c_str(); }
 static int32_t validate_pack(const wq_tensor *w, const wq_tensor *o) {
   if (!w || !o) return fail(WQ_ERR_NULL, "weight and weight_int4 are required");
   if (w->dtype != WQ_INT32) return fail(WQ_ERR_DTYPE, "weight must be INT32, got %s", dtname(w->dtype));
-  if (o->dtype != WQ_INT4) return fail(WQ_ERR_DTYPE, "weight_int4 must be INT4, got %s", dtname(o->dtype));
+  if (o->dtype != WQ_INT4 && o->dtype != WQ_INT4_TILED)
+    return fail(WQ_ERR_DTYPE, "weight_int4 must be INT4 or INT4_TILED, got %s", dtname(o->dtype));
   if (!valid_rank(w) || !valid_rank(o) || w->ndim != 2 || o->ndim != 2)
     return fail(WQ_ERR_SHAPE, "weight and weight_int4 must be 2-D");
   if (!same_shape(w, o)) return fail(WQ_ERR_SHAPE, "weight_int4 must have weight's logical shape");
   if (w->shape[1] % 2 != 0) return fail(WQ_ERR_SHAPE, "the last dimension must be even for INT4");
+  if (o->dtype == WQ_INT4_TILED && w->shape[1] % 16 != 0)
+    return fail(WQ_ERR_SHAPE, "the INT4_TILED layout needs the last dimension divisible by 16");
+  if (o->dtype == WQ_INT4_TILED && ((uintptr_t)o->data % 16) != 0)
+    return fail(WQ_ERR_UNSUPPORTED, "an INT4_TILED tensor must be 16-byte aligned");
   if (numel(w) > 0 && (!w->data || !o->data))
     return fail(WQ_ERR_NULL, "non-empty tensors need data pointers");
   if (overlap(w, o)) return fail(WQ_ERR_ALIAS, "weight_int4 overlaps weight");
@@ -371,9 +401,41 @@ int32_t wq_pack_int4(const wq_tensor *w, const wq_tensor *o, void *ws, uint64_t 
   int32_t st = validate_pack(w, o);
   if (st) return st;
   if (numel(w) == 0) return ok();
-  cudaError_t e = launch_pack_int4((const int32_t *)w->data, (uint8_t *)o->data, w->shape[0],
-                                   w->shape[1], (cudaStream_t)stream);
+  cudaError_t e = o->dtype == WQ_INT4_TILED
+                      ? launch_pack_int4_tiled((const int32_t *)w->data, (uint8_t *)o->data,
+                                               w->shape[0], w->shape[1], (cudaStream_t)stream)
+                      : launch_pack_int4((const int32_t *)w->data, (uint8_t *)o->data, w->shape[0],
+                                         w->shape[1], (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "pack kernel launch");
+  return ok();
+}
+
+int32_t wq_convert_int4_layout(const wq_tensor *src, const wq_tensor *dst, void *stream) {
+  if (!src || !dst) return fail(WQ_ERR_NULL, "src and dst are required");
+  const bool to_tiled = src->dtype == WQ_INT4 && dst->dtype == WQ_INT4_TILED;
+  const bool to_nd = src->dtype == WQ_INT4_TILED && dst->dtype == WQ_INT4;
+  if (!to_tiled && !to_nd)
+    return fail(WQ_ERR_DTYPE, "converts INT4 <-> INT4_TILED, got %s -> %s", dtname(src->dtype),
+                dtname(dst->dtype));
+  if (!valid_rank(src) || !valid_rank(dst) || src->ndim != 2 || dst->ndim != 2)
+    return fail(WQ_ERR_SHAPE, "src and dst must be 2-D");
+  if (!same_shape(src, dst)) return fail(WQ_ERR_SHAPE, "src and dst must have one logical shape");
+  if (src->shape[1] % 16 != 0)
+    return fail(WQ_ERR_SHAPE, "the INT4_TILED layout needs the last dimension divisible by 16");
+  const wq_tensor *tl = to_tiled ? dst : src;
+  if (numel(src) > 0 && (!src->data || !dst->data))
+    return fail(WQ_ERR_NULL, "non-empty tensors need data pointers");
+  if (numel(src) > 0 && ((uintptr_t)tl->data % 16) != 0)
+    return fail(WQ_ERR_UNSUPPORTED, "an INT4_TILED tensor must be 16-byte aligned");
+  if (overlap(src, dst)) return fail(WQ_ERR_ALIAS, "dst overlaps src");
+  if (numel(src) == 0) return ok();
+  const int64_t K = src->shape[0], N = src->shape[1];
+  cudaError_t e = to_tiled
+                      ? launch_int4_nd_to_tiled((const uint8_t *)src->data, (uint8_t *)dst->data, K, N,
+                                                (cudaStream_t)stream)
+                      : launch_int4_tiled_to_nd((const uint8_t *)src->data, (uint8_t *)dst->data, K, N,
+                                                (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "layout conversion launch");
   return ok();
 }
 
@@ -448,7 +510,7 @@ int32_t wq_matmul_add_rmsnorm_ex(
       if (e != cudaSuccess) return cuda_fail(e, "prefill kernel launch");
       break;
     case WQ_KERNEL_DECODE:
-      e = launch_decode(p, plan, ws, s);
+      e = p.tiled ? launch_decode_tiled(p, plan, ws, s) : launch_decode(p, plan, ws, s);
       if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
       break;
     default:

@@ -69,6 +69,19 @@ __device__ __forceinline__ uint32_t sub2(uint32_t v, uint32_t c) {
   return r;
 }
 
+// 4-bit value (0..15, two's complement nibble) of element (k, n) of a weight in
+// the kernel-native tiled INT4 layout (64 k x 16 column tiles, 512 bytes each,
+// tiles of a 64-row slab in column order; see wq_tiled.cu for the map).
+__device__ __forceinline__ uint32_t tiled_nibble(const uint8_t *w, int64_t k, int64_t n, int64_t N) {
+  const int64_t s = k >> 6, c = n >> 4;
+  const int kk = (int)(k & 63), cc = (int)(n & 15);
+  const int t = (kk >> 3) & 3, j = 2 * (kk >> 5) + ((kk >> 2) & 1), e = kk & 3;
+  const int lane = 4 * (cc & 7) + t;
+  const int p = (e < 2 ? 0 : 2) + (cc >> 3) + 4 * (e & 1);
+  const uint32_t b = w[(s * (N >> 4) + c) * 512 + lane * 16 + j * 4 + (p >> 1)];
+  return (b >> (4 * (p & 1))) & 0xFu;
+}
+
 // 2^e as an fp32 for e in [-126, 127].
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
 

@@ -7,7 +7,8 @@
 // W[k][n] = q[k][n] * S[r(k)][c(n)] + O[r(k)][c(n)] is formed in fp32 (q*S is
 // exact in fp32; adding O rounds once), r(k) = floor(k/group) or 0, c(n) = n or
 // 0. One thread owns one column n and eight rows; each block covers 128
-// columns, one split of k, and a grid-stride range of 8-row blocks.
+// columns, one split of k, and a grid-stride range of 8-row blocks. The weight
+// is INT8, dense INT4 or INT4 in the kernel-native tiled layout (LAYOUT 8, 4, 6).
 #include "wq_internal.h"
 #include "wq_common.cuh"
 
@@ -17,7 +18,7 @@ namespace {
 constexpr int kGenThreads = 128;
 constexpr int kGenRows = 8;
 
-template <int DT, int WBITS>
+template <int DT, int LAYOUT>
 __global__ void __launch_bounds__(kGenThreads)
     generic_gemm_kernel(const typename Elem<DT>::T *__restrict__ x1, const uint8_t *__restrict__ x2,
                         const typename Elem<DT>::T *__restrict__ S,
@@ -36,9 +37,12 @@ __global__ void __launch_bounds__(kGenThreads)
     for (int i = 0; i < kGenRows; ++i) acc[i] = 0.f;
     for (int64_t k = k0; k < k1; ++k) {
       int q;
-      if (WBITS == 4) {
+      if (LAYOUT == 4) {
         const uint32_t b = x2[k * (N / 2) + (n >> 1)];
         const int nib = (n & 1) ? (int)(b >> 4) : (int)(b & 0xFu);
+        q = nib >= 8 ? nib - 16 : nib;
+      } else if (LAYOUT == 6) {
+        const int nib = (int)tiled_nibble(x2, k, n, N);
         q = nib >= 8 ? nib - 16 : nib;
       } else {
         q = (int)reinterpret_cast<const int8_t *>(x2)[k * N + n];
@@ -86,14 +90,19 @@ cudaError_t launch_generic(const Problem &p, const Plan &plan, void *ws, cudaStr
   dim3 grid((unsigned)nb, (unsigned)plan.parts, (unsigned)mb);
   float *part = reinterpret_cast<float *>(static_cast<char *>(ws) + plan.part_off);
   const uint8_t *x2 = static_cast<const uint8_t *>(p.x2);
-#define WQ_GEN_LAUNCH(DT, WB)                                                                     \
-  generic_gemm_kernel<DT, WB><<<grid, kGenThreads, 0, s>>>(                                       \
+#define WQ_GEN_LAUNCH(DT, LAYOUT)                                                                 \
+  generic_gemm_kernel<DT, LAYOUT><<<grid, kGenThreads, 0, s>>>(                                   \
       static_cast<const Elem<DT>::T *>(p.x1), x2, static_cast<const Elem<DT>::T *>(p.scale),      \
       static_cast<const Elem<DT>::T *>(p.offset), p.M, p.K, p.N, p.group, p.Ns, plan.ksplit, part)
+  const int layout = p.wbits == 8 ? 8 : (p.tiled ? 6 : 4);
   if (p.dtype == WQ_BF16) {
-    if (p.wbits == 4) WQ_GEN_LAUNCH(WQ_BF16, 4); else WQ_GEN_LAUNCH(WQ_BF16, 8);
+    if (layout == 4) WQ_GEN_LAUNCH(WQ_BF16, 4);
+    else if (layout == 6) WQ_GEN_LAUNCH(WQ_BF16, 6);
+    else WQ_GEN_LAUNCH(WQ_BF16, 8);
   } else {
-    if (p.wbits == 4) WQ_GEN_LAUNCH(WQ_F16, 4); else WQ_GEN_LAUNCH(WQ_F16, 8);
+    if (layout == 4) WQ_GEN_LAUNCH(WQ_F16, 4);
+    else if (layout == 6) WQ_GEN_LAUNCH(WQ_F16, 6);
+    else WQ_GEN_LAUNCH(WQ_F16, 8);
   }
 #undef WQ_GEN_LAUNCH
   return cudaGetLastError();

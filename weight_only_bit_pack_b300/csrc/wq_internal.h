@@ -18,6 +18,7 @@ struct Problem {
   int64_t M = 0, K = 0, N = 0;
   int dtype = WQ_BF16;     // WQ_F16 or WQ_BF16 (x1, scale, offset, bias, residual, gamma, y, normOut)
   int wbits = 4;           // 4 (packed, two per byte along N) or 8
+  bool tiled = false;      // INT4 in the kernel-native tiled layout (wq_tiled.cu)
   int smode = kPerTensor;  // ScaleMode
   int64_t group = 0;       // > 0 only for kPerGroup
   int64_t G = 1;           // scale rows: ceil(K/group) for kPerGroup, else 1
@@ -71,6 +72,16 @@ struct Plan {
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_pack_int4(const int32_t *in, uint8_t *out, int64_t K, int64_t N, cudaStream_t s);
+// Kernel-native tiled INT4 layout: its byte count, the pack into it and the
+// conversions between it and the dense layout (wq_tiled.cu).
+uint64_t tiled_int4_bytes(int64_t K, int64_t N);
+cudaError_t launch_pack_int4_tiled(const int32_t *in, uint8_t *out, int64_t K, int64_t N,
+                                   cudaStream_t s);
+cudaError_t launch_int4_nd_to_tiled(const uint8_t *in, uint8_t *out, int64_t K, int64_t N,
+                                    cudaStream_t s);
+cudaError_t launch_int4_tiled_to_nd(const uint8_t *in, uint8_t *out, int64_t K, int64_t N,
+                                    cudaStream_t s);
+cudaError_t launch_decode_tiled(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
 cudaError_t launch_generic(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
 cudaError_t launch_prefill(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
 cudaError_t launch_decode(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
@@ -101,6 +112,8 @@ bool plan_generic(const Problem &p, Plan &plan);
 bool prefill_applicable(const Problem &p);
 bool plan_prefill(const Problem &p, Plan &plan);
 bool decode_applicable(const Problem &p);
+bool decode_tiled_applicable(const Problem &p);
+bool plan_decode_tiled(const Problem &p, Plan &plan);
 bool plan_decode(const Problem &p, Plan &plan);
 void plan_epilogue(const Problem &p, Plan &plan);
 
