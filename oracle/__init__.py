@@ -53,6 +53,8 @@ def _load(path=None):
         lib.wqo_dequant.argtypes = [P, I, I, P, P, I, I, I, P]
         lib.wqo_matmul_add_rmsnorm.argtypes = [P, I, I, P, I, P, P, I, I, I, P, P, P,
                                                ctypes.c_double, P, P, P]
+        lib.wqo_dynamic_quant.argtypes = [P, I, I, P, ctypes.c_int, P, P]
+        lib.wqo_dynamic_quant.restype = ctypes.c_int
         lib.wqo_tiled_bytes.argtypes = [I, I]
         lib.wqo_tiled_bytes.restype = I
         lib.wqo_pack_int4_tiled.argtypes = [P, I, I, P]
@@ -151,6 +153,28 @@ def unpack_int4_tiled(b, K: int, N: int) -> np.ndarray:
     if rc:
         raise ValueError("wqo_unpack_int4_tiled rejected its shape")
     return out
+
+
+def dynamic_quant(x, smooth=None, bits: int = 8):
+    """Per-token symmetric quantization of x (..., K) in fp32 arithmetic.
+    Returns (codes int8 with x's shape, scale float32 with x's leading shape);
+    INT4 codes lie in [-7, 7] (pack them with ``pack_int4``)."""
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").float().numpy()
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    lead, K = x.shape[:-1], x.shape[-1]
+    M = int(np.prod(lead)) if lead else 1
+    sm = None
+    if smooth is not None:
+        if hasattr(smooth, "detach"):
+            smooth = smooth.detach().to("cpu").float().numpy()
+        sm = np.ascontiguousarray(np.asarray(smooth, dtype=np.float32))
+    q = np.empty((M, K), dtype=np.int8)
+    s = np.empty(M, dtype=np.float32)
+    rc = _load().wqo_dynamic_quant(_p(x), M, K, _p(sm), 127 if bits == 8 else 7, _p(q), _p(s))
+    if rc:
+        raise ValueError("wqo_dynamic_quant rejected its arguments")
+    return q.reshape(x.shape), s.reshape(lead)
 
 
 def _so_shape(S, N):

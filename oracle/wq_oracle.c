@@ -236,3 +236,49 @@ int wqo_unpack_int4_tiled(const uint8_t *b, int64_t K, int64_t N, int32_t *out)
         }
     return WQO_OK;
 }
+
+/* Per-token symmetric dynamic quantization (aclnnDynamicQuant, "Function
+ * description", formula): for each row of x (M rows of K),
+ *     input    = x                      (or x * smoothScales, per column)
+ *     scaleOut = row_max(|input|) / dtypeMax
+ *     yOut     = round(input / scaleOut)
+ * with dtypeMax = 127 (INT8) or 7 (INT4). Readings where the page is silent:
+ * the arithmetic is fp32 (x * smooth, the maximum, the division by dtypeMax
+ * and the division by scaleOut are each one IEEE fp32 operation, as the GPU
+ * does them, because the rounding decides an integer); round() is round half
+ * to even; a row whose maximum is 0 gets scaleOut = 0 and codes 0; a NaN code
+ * becomes 0 and codes are clamped to [-dtypeMax, dtypeMax]. x and smooth hold
+ * fp16/bf16 values (exact in fp32). q receives int8 codes (M, K). */
+int wqo_dynamic_quant(const float *x, int64_t M, int64_t K, const float *smooth,
+                      int qmax, int8_t *q, float *scale)
+{
+    if (M < 0 || K < 1 || (qmax != 127 && qmax != 7)) return WQO_EINVAL;
+    float *row = (float *)malloc((size_t)K * sizeof(float));
+    if (!row) return WQO_ENOMEM;
+    for (int64_t m = 0; m < M; ++m) {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            volatile float v = x[m * K + k];
+            if (smooth) v = v * smooth[k];
+            row[k] = v;
+            float a = fabsf(v);
+            if (a > amax) amax = a;   /* a NaN element never wins the comparison */
+        }
+        volatile float s = amax / (float)qmax;
+        scale[m] = s;
+        for (int64_t k = 0; k < K; ++k) {
+            int32_t c = 0;
+            if (s != 0.0f) {
+                volatile float r = row[k] / s;
+                float rr = rintf(r);      /* current rounding mode: to nearest, ties to even */
+                if (rr != rr) c = 0;
+                else if (rr > (float)qmax) c = qmax;
+                else if (rr < (float)-qmax) c = -qmax;
+                else c = (int32_t)rr;
+            }
+            q[m * K + k] = (int8_t)c;
+        }
+    }
+    free(row);
+    return WQO_OK;
+}

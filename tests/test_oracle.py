@@ -148,6 +148,50 @@ def test_tiled_rejects_n_not_multiple_of_16():
         oracle.pack_int4_tiled(np.zeros((64, 24), np.int32))
 
 
+def _read_dq_literals():
+    rows = []
+    with open(os.path.join(GOLDEN, "dynamic_quant_literals.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            bits, xs, qs, frac = (part.strip() for part in line.split("|"))
+            num, den = frac.split("/")
+            rows.append((int(bits), [float(v) for v in xs.split()], [int(v) for v in qs.split()],
+                         float(np.float32(float(num)) / np.float32(float(den)))))
+    return rows
+
+
+@pytest.mark.parametrize("bits,xs,qs,scale", _read_dq_literals())
+def test_dynamic_quant_literals(bits, xs, qs, scale):
+    q, s = oracle.dynamic_quant(np.array([xs], np.float32), bits=bits)
+    assert q[0].tolist() == qs
+    assert s[0] == np.float32(scale)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_dynamic_quant_properties(bits):
+    """Codes within [-qmax, qmax]; the row maximum maps to +-qmax; every element
+    is reconstructed within half a step; scaling a row by 2^k leaves the codes and
+    multiplies the scale by 2^k (exact in fp32); smooth scales act per column."""
+    qmax = 127 if bits == 8 else 7
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal((64, 200)) * rng.uniform(0.01, 100, (64, 1))).astype(np.float16)
+    xf = x.astype(np.float32)
+    q, s = oracle.dynamic_quant(x, bits=bits)
+    assert np.abs(q).max() <= qmax
+    amax_idx = np.abs(xf).argmax(axis=1)
+    assert np.all(np.abs(q[np.arange(64), amax_idx]) == qmax)
+    err = np.abs(q.astype(np.float64) * s[:, None] - xf)
+    assert np.all(err <= s[:, None] * (0.5 + 1e-5))
+    q2, s2 = oracle.dynamic_quant(xf * 2.0 ** 7, bits=bits)
+    assert np.array_equal(q2, q) and np.array_equal(s2, s * np.float32(2.0 ** 7))
+    sm = rng.uniform(0.5, 2.0, 200).astype(np.float32)
+    q3, s3 = oracle.dynamic_quant(x, smooth=sm, bits=bits)
+    q4, s4 = oracle.dynamic_quant(xf * sm[None, :], bits=bits)
+    assert np.array_equal(q3, q4) and np.array_equal(s3, s4)
+
+
 def test_pack_rejects_odd_n():
     with pytest.raises(ValueError):
         oracle.pack_int4(np.zeros((2, 3), np.int32))

@@ -33,6 +33,10 @@ MUTATIONS = {
                                "int64_t h = kk / 32, jl = (kk % 32) / 16, t = (kk % 16) / 4, e = kk % 4;"),
     "tiled_upper_nibble_pairs": ("int64_t p = (e < 2 ? 0 : 2) + upper + 4 * (e % 2);",
                                  "int64_t p = (e < 2 ? 0 : 4) + upper + 2 * (e % 2);"),
+    "dq_round_half_away": ("float rr = rintf(r);", "float rr = roundf(r);"),
+    "dq_scale_off_by_one": ("volatile float s = amax / (float)qmax;", "volatile float s = amax / (float)(qmax + 1);"),
+    "dq_smooth_ignored": ("if (smooth) v = v * smooth[k];", "(void)smooth;"),
+    "dq_max_not_abs": ("float a = fabsf(v);", "float a = v;"),
     "tiled_word_major_in_tile": ("* 512 + lane * 16 + j * 4 + p / 2;", "* 512 + j * 128 + lane * 4 + p / 2;"),
 }
 
