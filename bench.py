@@ -417,6 +417,40 @@ def time_extra(wq, config, dev, stream, steps, warmup, peaks):
     return out
 
 
+def time_dynamic_quant(wq, dev, stream, bits, steps, warmup, peaks, M=8192, K=8192):
+    """Device time of the per-token dynamic quantization of a bf16 (M, K) activation."""
+    g = torch.Generator(device=dev).manual_seed(6)
+    R = 3  # distinct inputs, 3 x 134 MB > 2x L2
+    xs = [torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16) for _ in range(R)]
+    ys = [torch.empty((M, K if bits == 8 else K // 2), dtype=torch.int8 if bits == 8 else torch.uint8,
+                      device=dev) for _ in range(R)]
+    ss = [torch.empty(M, dtype=torch.float32, device=dev) for _ in range(R)]
+    for i in range(warmup):
+        wq.dynamic_quant(xs[i % R], None, bits, y=ys[i % R], scale=ss[i % R], stream=stream)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        for i in range(steps):
+            wq.dynamic_quant(xs[i % R], None, bits, y=ys[i % R], scale=ss[i % R], stream=stream)
+    gr.replay()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    gr.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = ev0.elapsed_time(ev1) / steps
+    nbytes = M * K * 2 + M * K * bits // 8 + M * 4
+    out = {"workload": f"dynamic_quant_bf16_int{bits}_M{M}_K{K}", "kernel": "dynamic_quant",
+           "steps": steps, "ms_per_step": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9,
+           "roofline_bound": "hbm", "roofline_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+           "l2": f"rotating {R} distinct inputs, {R * M * K * 2 / 1e6:.0f} MB > 2x L2"}
+    del gr, xs, ys, ss
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return out
+
+
 EXTRA = (("decode", 2000), ("decode@tiled", 2000), ("sweep:1", 1000), ("sweep:1@tiled", 1000),
          ("sweep:16", 1000), ("sweep:16@tiled", 1000), ("w8a16", 50), ("prefill", 20))
 
@@ -680,6 +714,8 @@ def run_ours(args, world, rank, local):
             if cfg == args.config:
                 continue
             extras.append(time_extra(wq, cfg, dev, stream, n, W, peaks))
+        for bits in (8, 4):
+            extras.append(time_dynamic_quant(wq, dev, stream, bits, 50, W, peaks))
         line["workloads"] = extras
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -71,7 +71,8 @@ typedef enum wq_dtype {
     WQ_INT8 = 3,
     WQ_INT4 = 4,
     WQ_INT32 = 5,
-    WQ_INT4_TILED = 6
+    WQ_INT4_TILED = 6,
+    WQ_F32 = 7
 } wq_dtype;
 
 /* Tensor descriptor (the analogue of aclTensor): pointer, element type, rank
@@ -217,6 +218,35 @@ int32_t wq_matmul_add_rmsnorm_select_kernel(
     const wq_tensor *offset, const wq_tensor *bias, const wq_tensor *residual,
     const wq_tensor *gamma, double eps, int64_t group,
     const wq_tensor *y, const wq_tensor *normOut);
+
+/* ------------------------------------------------------------------ dynamic quantization */
+
+/* First phase of the per-token symmetric dynamic quantization
+ * (aclnnDynamicQuant, "Function description": scaleOut = row_max(|input|) /
+ * dtypeMax, yOut = round(input / scaleOut), input = x or x * smoothScales).
+ *   x              WQ_F16 or WQ_BF16, 1-D (K), 2-D (M, K) or 3-D (b, s, K);
+ *                  1 <= K <= 65535. Rows are the leading dimensions.
+ *   smooth_scales  NULL or (K), x's dtype: multiplies column k before the
+ *                  maximum is taken.
+ *   y              out: WQ_INT8 with x's shape (dtypeMax 127), or WQ_INT4 with
+ *                  x's logical shape, K even, packed two per byte along the row
+ *                  like the weight pack (dtypeMax 7); read as little-endian int32
+ *                  words it is the page's INT32 output (8 codes per word).
+ *   scale          out: WQ_F32 with x's leading shape ((1) for a 1-D x).
+ *   ws_bytes       out: 0.
+ * Every step is one IEEE fp32 operation (x * smooth, the maximum, max /
+ * dtypeMax, x / scale), round() is round half to even, a code is clamped to
+ * [-dtypeMax, dtypeMax] and a NaN quotient gives 0, and a row whose maximum is
+ * 0 gets scale 0 and codes 0 (readings where the page is silent). Errors:
+ * WQ_ERR_NULL, WQ_ERR_DTYPE, WQ_ERR_SHAPE, WQ_ERR_ALIAS. Touches no device memory. */
+int32_t wq_dynamic_quant_get_workspace(const wq_tensor *x, const wq_tensor *smooth_scales,
+                                       const wq_tensor *y, const wq_tensor *scale,
+                                       uint64_t *ws_bytes);
+
+/* Second phase: enqueue the quantization on `stream`. Bit-exact and
+ * deterministic (the maximum is order-independent); M = 0 enqueues nothing. */
+int32_t wq_dynamic_quant(const wq_tensor *x, const wq_tensor *smooth_scales, const wq_tensor *y,
+                         const wq_tensor *scale, void *ws, uint64_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------ no-alloc variant */
 

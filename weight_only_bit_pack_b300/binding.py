@@ -55,6 +55,7 @@ class DType(enum.IntEnum):
     INT4 = 4
     INT32 = 5
     INT4_TILED = 6
+    F32 = 7
 
 
 class WQError(RuntimeError):
@@ -91,6 +92,8 @@ _T = [_P] * 7 + [ctypes.c_double, ctypes.c_int64, _P, _P]
 lib.wq_pack_int4_get_workspace.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint64)]
 lib.wq_pack_int4.argtypes = [_P, _P, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
 lib.wq_convert_int4_layout.argtypes = [_P, _P, ctypes.c_void_p]
+lib.wq_dynamic_quant_get_workspace.argtypes = [_P, _P, _P, _P, ctypes.POINTER(ctypes.c_uint64)]
+lib.wq_dynamic_quant.argtypes = [_P, _P, _P, _P, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
 lib.wq_matmul_add_rmsnorm_get_workspace.argtypes = _T + [ctypes.POINTER(ctypes.c_uint64)]
 lib.wq_matmul_add_rmsnorm.argtypes = _T + [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
 lib.wq_matmul_add_rmsnorm_get_workspace_ex.argtypes = _T + [ctypes.c_int32,
@@ -114,11 +117,11 @@ for _f in ("wq_pack_int4_get_workspace", "wq_pack_int4", "wq_matmul_add_rmsnorm_
            "wq_matmul_add_rmsnorm_ex", "wq_matmul_add_rmsnorm_select_kernel",
            "wq_read_device_status", "wq_version", "wq_matmul_add_rmsnorm_noalloc",
            "wq_check_device_timeout", "wq_noalloc_read_device_status", "wq_test_set_wait_limits",
-           "wq_convert_int4_layout"):
+           "wq_convert_int4_layout", "wq_dynamic_quant_get_workspace", "wq_dynamic_quant"):
     getattr(lib, _f).restype = ctypes.c_int32
 
 _TORCH2WQ = {torch.float16: DType.F16, torch.bfloat16: DType.BF16, torch.int8: DType.INT8,
-             torch.uint8: DType.INT4, torch.int32: DType.INT32}
+             torch.uint8: DType.INT4, torch.int32: DType.INT32, torch.float32: DType.F32}
 
 
 def _check(status: int):
@@ -208,6 +211,26 @@ def tiled_to_int4(t: TiledInt4, stream=None) -> torch.Tensor:
     out = torch.empty((t.K, t.N // 2), dtype=torch.uint8, device=t.device)
     _check(lib.wq_convert_int4_layout(_ref(describe(t)), _ref(describe(out)), _stream(stream)))
     return out
+
+
+def dynamic_quant(x: torch.Tensor, smooth_scales: Optional[torch.Tensor] = None, bits: int = 8,
+                  y: Optional[torch.Tensor] = None, scale: Optional[torch.Tensor] = None,
+                  stream=None):
+    """Per-token symmetric quantization (``wq_dynamic_quant``). Returns ``(y, scale)``:
+    y int8 with x's shape (bits 8), or uint8 (..., K/2) packed INT4 codes (bits 4);
+    scale float32 with x's leading shape."""
+    lead = tuple(x.shape[:-1])
+    if y is None:
+        shp = lead + ((x.shape[-1],) if bits == 8 else (x.shape[-1] // 2,))
+        y = torch.empty(shp, dtype=torch.int8 if bits == 8 else torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty(lead if lead else (1,), dtype=torch.float32, device=x.device)
+    yd = describe(y)
+    d = [describe(x), describe(smooth_scales), yd, describe(scale)]
+    ws = ctypes.c_uint64(0)
+    _check(lib.wq_dynamic_quant_get_workspace(*[_ref(v) for v in d], ctypes.byref(ws)))
+    _check(lib.wq_dynamic_quant(*[_ref(v) for v in d], None, 0, _stream(stream)))
+    return y, scale
 
 
 def pack_int4_bytes(n_logical: int, data: torch.Tensor) -> WqTensor:

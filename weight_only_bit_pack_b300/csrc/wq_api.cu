@@ -57,7 +57,7 @@ int64_t elem_bits(int dt) {
     case WQ_F16: case WQ_BF16: return 16;
     case WQ_INT8: return 8;
     case WQ_INT4: case WQ_INT4_TILED: return 4;
-    case WQ_INT32: return 32;
+    case WQ_INT32: case WQ_F32: return 32;
     default: return 0;
   }
 }
@@ -94,7 +94,7 @@ const char *dtname(int dt) {
   switch (dt) {
     case WQ_F16: return "F16"; case WQ_BF16: return "BF16"; case WQ_INT8: return "INT8";
     case WQ_INT4: return "INT4"; case WQ_INT32: return "INT32";
-    case WQ_INT4_TILED: return "INT4_TILED"; default: return "?";
+    case WQ_INT4_TILED: return "INT4_TILED"; case WQ_F32: return "F32"; default: return "?";
   }
 }
 
@@ -436,6 +436,67 @@ int32_t wq_convert_int4_layout(const wq_tensor *src, const wq_tensor *dst, void 
                       : launch_int4_tiled_to_nd((const uint8_t *)src->data, (uint8_t *)dst->data, K, N,
                                                 (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "layout conversion launch");
+  return ok();
+}
+
+// ------------------------------------------------------------------ dynamic quantization
+
+static int32_t validate_dq(const wq_tensor *x, const wq_tensor *sm, const wq_tensor *y,
+                           const wq_tensor *sc, int64_t &M, int64_t &K, int &bits) {
+  if (!x || !y || !sc) return fail(WQ_ERR_NULL, "x, y and scale are required");
+  const wq_tensor *all[] = {x, sm, y, sc};
+  for (const wq_tensor *t : all)
+    if (t && !valid_rank(t)) return fail(WQ_ERR_SHAPE, "ranks must be 1..3 with non-negative dims");
+  if (x->dtype != WQ_F16 && x->dtype != WQ_BF16)
+    return fail(WQ_ERR_DTYPE, "x must be F16 or BF16, got %s", dtname(x->dtype));
+  if (sm && sm->dtype != x->dtype) return fail(WQ_ERR_DTYPE, "smooth_scales must have x's dtype");
+  if (y->dtype != WQ_INT8 && y->dtype != WQ_INT4)
+    return fail(WQ_ERR_DTYPE, "y must be INT8 or INT4, got %s", dtname(y->dtype));
+  if (sc->dtype != WQ_F32) return fail(WQ_ERR_DTYPE, "scale must be F32, got %s", dtname(sc->dtype));
+  K = x->shape[x->ndim - 1];
+  M = 1;
+  for (int i = 0; i < x->ndim - 1; ++i) M *= x->shape[i];
+  if (K < 1 || K > kMaxKN) return fail(WQ_ERR_SHAPE, "the last dimension must lie in [1, 65535]");
+  if (M > kMaxRows) return fail(WQ_ERR_SHAPE, "more than 2^31-1 rows");
+  if (sm && (sm->ndim != 1 || sm->shape[0] != K))
+    return fail(WQ_ERR_SHAPE, "smooth_scales must be 1-D (k = %lld)", (long long)K);
+  if (!same_shape(x, y)) return fail(WQ_ERR_SHAPE, "y must have x's (logical) shape");
+  bits = y->dtype == WQ_INT8 ? 8 : 4;
+  if (bits == 4 && K % 2 != 0) return fail(WQ_ERR_SHAPE, "INT4 output needs an even last dimension");
+  if (numel(sc) != M || (x->ndim > 1 && (sc->ndim != x->ndim - 1 ||
+                                         [&] { for (int i = 0; i < sc->ndim; ++i)
+                                                 if (sc->shape[i] != x->shape[i]) return true;
+                                               return false; }())))
+    return fail(WQ_ERR_SHAPE, "scale must have x's leading shape");
+  for (const wq_tensor *t : all)
+    if (t && numel(t) > 0 && !t->data) return fail(WQ_ERR_NULL, "a non-empty tensor has no data");
+  if (overlap(y, x) || overlap(y, sm) || overlap(y, sc) || overlap(sc, x) || overlap(sc, sm))
+    return fail(WQ_ERR_ALIAS, "the outputs must not overlap the inputs or each other");
+  return WQ_OK;
+}
+
+int32_t wq_dynamic_quant_get_workspace(const wq_tensor *x, const wq_tensor *sm, const wq_tensor *y,
+                                       const wq_tensor *sc, uint64_t *ws_bytes) {
+  if (!ws_bytes) return fail(WQ_ERR_NULL, "ws_bytes is required");
+  int64_t M, K;
+  int bits;
+  int32_t st = validate_dq(x, sm, y, sc, M, K, bits);
+  if (st) return st;
+  *ws_bytes = 0;
+  return ok();
+}
+
+int32_t wq_dynamic_quant(const wq_tensor *x, const wq_tensor *sm, const wq_tensor *y,
+                         const wq_tensor *sc, void *ws, uint64_t ws_bytes, void *stream) {
+  (void)ws; (void)ws_bytes;
+  int64_t M, K;
+  int bits;
+  int32_t st = validate_dq(x, sm, y, sc, M, K, bits);
+  if (st) return st;
+  if (M == 0) return ok();
+  cudaError_t e = launch_dynamic_quant(x->data, sm ? sm->data : nullptr, x->dtype, M, K, bits,
+                                       y->data, static_cast<float *>(sc->data), (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "dynamic quantization launch");
   return ok();
 }
 

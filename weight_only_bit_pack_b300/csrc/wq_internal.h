@@ -82,6 +82,9 @@ cudaError_t launch_int4_nd_to_tiled(const uint8_t *in, uint8_t *out, int64_t K, 
 cudaError_t launch_int4_tiled_to_nd(const uint8_t *in, uint8_t *out, int64_t K, int64_t N,
                                     cudaStream_t s);
 cudaError_t launch_decode_tiled(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
+// Per-token symmetric dynamic quantization (wq_dynquant.cu); bits 8 or 4.
+cudaError_t launch_dynamic_quant(const void *x, const void *smooth, int dtype, int64_t M, int64_t K,
+                                 int bits, void *y, float *scale, cudaStream_t s);
 cudaError_t launch_generic(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
 cudaError_t launch_prefill(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
 cudaError_t launch_decode(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
