@@ -64,7 +64,13 @@ extern "C" {
  * p = (e < 2 ? 0 : 2) + cc / 8 + 4 (e % 2) with e = kk % 4, i.e. byte
  * l*16 + j*4 + p/2, bits 4(p%2)+3 : 4(p%2). Lane l's 16 bytes are then exactly
  * its A-operand registers (A = W^T) of four m16n8k16 MMAs. Tiled tensors must be
- * 16-byte aligned. */
+ * 16-byte aligned.
+ *
+ * WQ_INT8_T and WQ_INT4_T hold a weight transposed (aclnnWeightQuantMatmul-
+ * AllReduceAddRmsNorm, "Constraints": x2 may be transposed): a (K, N) weight
+ * stored as its (N, K) transpose, row-major with K contiguous; the descriptor
+ * gives the stored shape (N, K). INT4_T packs two values per byte along K (k
+ * even in bits 3:0), i.e. it is the WQ_INT4 packing of the (N, K) array. */
 typedef enum wq_dtype {
     WQ_F16 = 1,
     WQ_BF16 = 2,
@@ -72,7 +78,9 @@ typedef enum wq_dtype {
     WQ_INT4 = 4,
     WQ_INT32 = 5,
     WQ_INT4_TILED = 6,
-    WQ_F32 = 7
+    WQ_F32 = 7,
+    WQ_INT8_T = 8,
+    WQ_INT4_T = 9
 } wq_dtype;
 
 /* Tensor descriptor (the analogue of aclTensor): pointer, element type, rank
@@ -114,7 +122,9 @@ typedef enum wq_kernel {
  *                in [-8, 7]; any other value keeps its low four bits (two's
  *                complement truncation).
  *   weight_int4  WQ_INT4, 2-D, logical shape (K, N), i.e. K*N/2 bytes; or
- *                WQ_INT4_TILED (N % 16 == 0, 16-byte aligned), the tiled layout.
+ *                WQ_INT4_TILED (N % 16 == 0, 16-byte aligned), the tiled layout;
+ *                or WQ_INT4_T: the same bytes as WQ_INT4, for a `weight` that is
+ *                already the transposed (N, K) array.
  *   ws_bytes     out: workspace bytes the second phase needs (always 0).
  * Errors: WQ_ERR_NULL, WQ_ERR_DTYPE, WQ_ERR_SHAPE. Touches no device memory. */
 int32_t wq_pack_int4_get_workspace(const wq_tensor *weight, const wq_tensor *weight_int4,
@@ -126,12 +136,13 @@ int32_t wq_pack_int4_get_workspace(const wq_tensor *weight, const wq_tensor *wei
 int32_t wq_pack_int4(const wq_tensor *weight, const wq_tensor *weight_int4,
                      void *ws, uint64_t ws_bytes, void *stream);
 
-/* Converts a 2-D (K, N) INT4 weight between the dense layout (WQ_INT4) and the
- * tiled layout (WQ_INT4_TILED), in the direction the two dtypes give; both
- * descriptors carry the logical shape, N % 16 == 0, the tiled one 16-byte
- * aligned. The padding nibbles of a tiled output are zero. Bit-exact,
- * asynchronous on `stream`, no workspace. Errors: WQ_ERR_NULL, WQ_ERR_DTYPE,
- * WQ_ERR_SHAPE, WQ_ERR_UNSUPPORTED (alignment), WQ_ERR_ALIAS, WQ_ERR_CUDA.
+/* Converts a (K, N) INT4 weight between any two of its layouts: dense
+ * (WQ_INT4, shape (K, N)), tiled (WQ_INT4_TILED, shape (K, N), N % 16 == 0,
+ * 16-byte aligned) and transposed (WQ_INT4_T, shape (N, K), K even), in the
+ * direction the two dtypes give. The padding nibbles of a tiled output are zero.
+ * Bit-exact, asynchronous on `stream`, no workspace. Errors: WQ_ERR_NULL,
+ * WQ_ERR_DTYPE, WQ_ERR_SHAPE, WQ_ERR_UNSUPPORTED (alignment), WQ_ERR_ALIAS,
+ * WQ_ERR_CUDA.
  * (aclnnConvertWeightToINT4Pack, "Function description": the ND to tiled
  * conversion of the pack's output format; the tiled to ND direction serves
  * checking and re-use of the weight elsewhere.) */
@@ -143,9 +154,12 @@ int32_t wq_convert_int4_layout(const wq_tensor *src, const wq_tensor *dst, void 
  *   x1        WQ_F16 or WQ_BF16, (M, K) or (b, s, K) with M = b*s; 0 <= M < 2^31,
  *             1 <= K <= 65535. Not transposed.
  *   x2        WQ_INT8 (K, N) or WQ_INT4 (K, N) packed as described above (N even),
- *             or WQ_INT4_TILED (K, N) (N % 16 == 0, 16-byte aligned);
- *             0 <= N <= 65535. Not transposed. A tiled weight runs on the tiled
- *             decode kernel for M <= 16 and on the generic kernel otherwise.
+ *             WQ_INT4_TILED (K, N) (N % 16 == 0, 16-byte aligned), or transposed:
+ *             WQ_INT8_T / WQ_INT4_T given as (N, K) (K even for INT4_T);
+ *             0 <= N <= 65535. A tiled weight runs on the tiled decode kernel for
+ *             M <= 16 and on the generic kernel otherwise; a transposed weight
+ *             runs on the generic kernel (wq_convert_int4_layout turns an INT4_T
+ *             weight into the dense or tiled layout once, for the fast kernels).
  *   scale     antiquantScale, x1's dtype: (1) per-tensor, (N) or (1, N)
  *             per-channel, (ceil(K/group), N) per-group.
  *   offset    antiquantOffset or NULL; if given, the scale's shape and dtype.

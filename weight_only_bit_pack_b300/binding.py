@@ -56,6 +56,8 @@ class DType(enum.IntEnum):
     INT32 = 5
     INT4_TILED = 6
     F32 = 7
+    INT8_T = 8
+    INT4_T = 9
 
 
 class WQError(RuntimeError):
@@ -77,6 +79,22 @@ class TiledInt4:
         if data.dtype != torch.uint8 or data.numel() != tiled_bytes(K, N):
             raise ValueError(f"a tiled ({K}, {N}) INT4 weight holds {tiled_bytes(K, N)} uint8 bytes")
         self.data, self.K, self.N = data, int(K), int(N)
+
+    @property
+    def device(self):
+        return self.data.device
+
+
+class TransposedWeight:
+    """A (K, N) weight stored transposed: ``data`` is the (N, K) int8 array
+    (``bits=8``) or its INT4 packing along K, an (N, K/2) uint8 array (``bits=4``)."""
+
+    def __init__(self, data: torch.Tensor, bits: int):
+        if bits not in (4, 8) or data.dim() != 2:
+            raise ValueError("a transposed weight is a 2-D int8 (N, K) or uint8 (N, K/2) array")
+        self.data, self.bits = data, bits
+        self.N = data.shape[0]
+        self.K = data.shape[1] * (2 if bits == 4 else 1)
 
     @property
     def device(self):
@@ -133,6 +151,15 @@ def describe(t: Optional[torch.Tensor], dtype: Optional[int] = None, shape=None)
     """wq_tensor for a contiguous torch tensor (None -> NULL)."""
     if t is None:
         return None
+    if isinstance(t, TransposedWeight):
+        if not t.data.is_contiguous():
+            raise ValueError("wq tensors must be contiguous")
+        d = WqTensor()
+        d.data = t.data.data_ptr()
+        d.dtype = int(DType.INT4_T if t.bits == 4 else DType.INT8_T)
+        d.ndim = 2
+        d.shape[0], d.shape[1] = t.N, t.K
+        return d
     if isinstance(t, TiledInt4):
         d = WqTensor()
         d.data = t.data.data_ptr()
@@ -203,6 +230,29 @@ def int4_to_tiled(w4: torch.Tensor, stream=None) -> TiledInt4:
     K, N = w4.shape[0], w4.shape[1] * 2
     out = TiledInt4(torch.empty(tiled_bytes(K, N), dtype=torch.uint8, device=w4.device), K, N)
     _check(lib.wq_convert_int4_layout(_ref(describe(w4)), _ref(describe(out)), _stream(stream)))
+    return out
+
+
+def convert_int4(src, layout: str, stream=None):
+    """Any INT4 layout of a weight into another (``wq_convert_int4_layout``):
+    ``src`` is a (K, N/2) uint8 dense tensor, a :class:`TiledInt4` or a 4-bit
+    :class:`TransposedWeight`; ``layout`` is "dense", "tiled" or "transposed"."""
+    if isinstance(src, TiledInt4):
+        K, N = src.K, src.N
+    elif isinstance(src, TransposedWeight):
+        K, N = src.K, src.N
+    else:
+        K, N = src.shape[0], src.shape[1] * 2
+    dev = src.device
+    if layout == "dense":
+        out = torch.empty((K, N // 2), dtype=torch.uint8, device=dev)
+    elif layout == "tiled":
+        out = TiledInt4(torch.empty(tiled_bytes(K, N), dtype=torch.uint8, device=dev), K, N)
+    elif layout == "transposed":
+        out = TransposedWeight(torch.empty((N, K // 2), dtype=torch.uint8, device=dev), 4)
+    else:
+        raise ValueError(layout)
+    _check(lib.wq_convert_int4_layout(_ref(describe(src)), _ref(describe(out)), _stream(stream)))
     return out
 
 

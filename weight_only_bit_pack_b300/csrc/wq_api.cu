@@ -55,8 +55,8 @@ int64_t numel(const wq_tensor *t) {
 int64_t elem_bits(int dt) {
   switch (dt) {
     case WQ_F16: case WQ_BF16: return 16;
-    case WQ_INT8: return 8;
-    case WQ_INT4: case WQ_INT4_TILED: return 4;
+    case WQ_INT8: case WQ_INT8_T: return 8;
+    case WQ_INT4: case WQ_INT4_TILED: case WQ_INT4_T: return 4;
     case WQ_INT32: case WQ_F32: return 32;
     default: return 0;
   }
@@ -94,7 +94,8 @@ const char *dtname(int dt) {
   switch (dt) {
     case WQ_F16: return "F16"; case WQ_BF16: return "BF16"; case WQ_INT8: return "INT8";
     case WQ_INT4: return "INT4"; case WQ_INT32: return "INT32";
-    case WQ_INT4_TILED: return "INT4_TILED"; case WQ_F32: return "F32"; default: return "?";
+    case WQ_INT4_TILED: return "INT4_TILED"; case WQ_F32: return "F32";
+    case WQ_INT8_T: return "INT8_T"; case WQ_INT4_T: return "INT4_T"; default: return "?";
   }
 }
 
@@ -118,8 +119,11 @@ int32_t validate(const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scal
   const int dt = x1->dtype;
   if (dt != WQ_F16 && dt != WQ_BF16)
     return fail(WQ_ERR_DTYPE, "x1 must be F16 or BF16, got %s", dtname(dt));
-  if (x2->dtype != WQ_INT8 && x2->dtype != WQ_INT4 && x2->dtype != WQ_INT4_TILED)
-    return fail(WQ_ERR_DTYPE, "x2 must be INT8, INT4 or INT4_TILED, got %s", dtname(x2->dtype));
+  if (x2->dtype != WQ_INT8 && x2->dtype != WQ_INT4 && x2->dtype != WQ_INT4_TILED &&
+      x2->dtype != WQ_INT8_T && x2->dtype != WQ_INT4_T)
+    return fail(WQ_ERR_DTYPE, "x2 must be INT8, INT4, INT4_TILED, INT8_T or INT4_T, got %s",
+                dtname(x2->dtype));
+  const bool x2t = x2->dtype == WQ_INT8_T || x2->dtype == WQ_INT4_T;  // stored (n, k)
   const wq_tensor *same[] = {scale, offset, bias, residual, gamma, y, normOut};
   const char *snames[] = {"scale", "offset", "bias", "residual", "gamma", "y", "normOut"};
   for (int i = 0; i < 7; ++i)
@@ -139,12 +143,15 @@ int32_t validate(const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scal
   if (K < 1) return fail(WQ_ERR_SHAPE, "k must be >= 1 (empty k is not supported)");
   if (K > kMaxKN) return fail(WQ_ERR_SHAPE, "k = %lld exceeds 65535", (long long)K);
 
-  // x2: (k, n)
-  if (x2->ndim != 2) return fail(WQ_ERR_SHAPE, "x2 must be 2-D (k, n)");
-  if (x2->shape[0] != K)
-    return fail(WQ_ERR_SHAPE, "x2 has k = %lld, x1 has k = %lld", (long long)x2->shape[0],
+  // x2: (k, n), or (n, k) when transposed
+  if (x2->ndim != 2) return fail(WQ_ERR_SHAPE, "x2 must be 2-D (k, n), or (n, k) when transposed");
+  if (x2->shape[x2t ? 1 : 0] != K)
+    return fail(WQ_ERR_SHAPE, "x2 has k = %lld, x1 has k = %lld", (long long)x2->shape[x2t ? 1 : 0],
                 (long long)K);
-  const int64_t N = x2->shape[1];
+  const int64_t N = x2->shape[x2t ? 0 : 1];
+  if (x2->dtype == WQ_INT4_T && (K % 2) != 0)
+    return fail(WQ_ERR_SHAPE, "INT4_T x2 packs along k, which must be even, got k = %lld",
+                (long long)K);
   if (N > kMaxKN) return fail(WQ_ERR_SHAPE, "n = %lld exceeds 65535", (long long)N);
   if (x2->dtype == WQ_INT4 && (N % 2) != 0)
     return fail(WQ_ERR_SHAPE, "INT4 x2 needs an even last dimension, got n = %lld", (long long)N);
@@ -232,8 +239,9 @@ int32_t validate(const wq_tensor *x1, const wq_tensor *x2, const wq_tensor *scal
   p = Problem();
   p.M = M; p.K = K; p.N = N;
   p.dtype = dt;
-  p.wbits = x2->dtype == WQ_INT8 ? 8 : 4;
+  p.wbits = (x2->dtype == WQ_INT8 || x2->dtype == WQ_INT8_T) ? 8 : 4;
   p.tiled = x2->dtype == WQ_INT4_TILED;
+  p.transposed = x2t;
   p.smode = smode; p.group = smode == kPerGroup ? group : 0; p.G = G; p.Ns = Ns;
   p.eps = (float)eps;
   p.x1 = x1->data; p.x2 = x2->data; p.scale = scale->data;
@@ -256,6 +264,12 @@ int32_t make_plan(const Problem &p, int32_t kernel, Plan &plan) {
     return WQ_OK;
   }
   int chosen = kernel;
+  if (p.transposed) {  // a transposed weight: the generic kernel reads it in place
+    if (chosen == WQ_KERNEL_DECODE || chosen == WQ_KERNEL_PREFILL)
+      return fail(WQ_ERR_UNSUPPORTED, "the decode and prefill kernels do not read a transposed x2 "
+                                      "(convert an INT4_T weight with wq_convert_int4_layout)");
+    chosen = WQ_KERNEL_GENERIC;
+  }
   if (p.tiled) {
     // the tiled layout: the tiled decode kernel for small M, else the generic kernel
     if (chosen == WQ_KERNEL_AUTO)
@@ -371,8 +385,9 @@ const char *wq_last_error(void) { return g_last_error.c_str(); }
 static int32_t validate_pack(const wq_tensor *w, const wq_tensor *o) {
   if (!w || !o) return fail(WQ_ERR_NULL, "weight and weight_int4 are required");
   if (w->dtype != WQ_INT32) return fail(WQ_ERR_DTYPE, "weight must be INT32, got %s", dtname(w->dtype));
-  if (o->dtype != WQ_INT4 && o->dtype != WQ_INT4_TILED)
-    return fail(WQ_ERR_DTYPE, "weight_int4 must be INT4 or INT4_TILED, got %s", dtname(o->dtype));
+  if (o->dtype != WQ_INT4 && o->dtype != WQ_INT4_TILED && o->dtype != WQ_INT4_T)
+    return fail(WQ_ERR_DTYPE, "weight_int4 must be INT4, INT4_TILED or INT4_T, got %s",
+                dtname(o->dtype));
   if (!valid_rank(w) || !valid_rank(o) || w->ndim != 2 || o->ndim != 2)
     return fail(WQ_ERR_SHAPE, "weight and weight_int4 must be 2-D");
   if (!same_shape(w, o)) return fail(WQ_ERR_SHAPE, "weight_int4 must have weight's logical shape");
@@ -412,29 +427,47 @@ int32_t wq_pack_int4(const wq_tensor *w, const wq_tensor *o, void *ws, uint64_t 
 
 int32_t wq_convert_int4_layout(const wq_tensor *src, const wq_tensor *dst, void *stream) {
   if (!src || !dst) return fail(WQ_ERR_NULL, "src and dst are required");
-  const bool to_tiled = src->dtype == WQ_INT4 && dst->dtype == WQ_INT4_TILED;
-  const bool to_nd = src->dtype == WQ_INT4_TILED && dst->dtype == WQ_INT4;
-  if (!to_tiled && !to_nd)
-    return fail(WQ_ERR_DTYPE, "converts INT4 <-> INT4_TILED, got %s -> %s", dtname(src->dtype),
-                dtname(dst->dtype));
+  auto is4 = [](int d) { return d == WQ_INT4 || d == WQ_INT4_TILED || d == WQ_INT4_T; };
+  if (!is4(src->dtype) || !is4(dst->dtype) || src->dtype == dst->dtype)
+    return fail(WQ_ERR_DTYPE, "converts between two of INT4, INT4_TILED and INT4_T, got %s -> %s",
+                dtname(src->dtype), dtname(dst->dtype));
   if (!valid_rank(src) || !valid_rank(dst) || src->ndim != 2 || dst->ndim != 2)
     return fail(WQ_ERR_SHAPE, "src and dst must be 2-D");
-  if (!same_shape(src, dst)) return fail(WQ_ERR_SHAPE, "src and dst must have one logical shape");
-  if (src->shape[1] % 16 != 0)
-    return fail(WQ_ERR_SHAPE, "the INT4_TILED layout needs the last dimension divisible by 16");
-  const wq_tensor *tl = to_tiled ? dst : src;
-  if (numel(src) > 0 && (!src->data || !dst->data))
+  // logical (K, N) of each side (INT4_T is given as its stored (N, K))
+  auto kn = [](const wq_tensor *t, int64_t &K, int64_t &N) {
+    K = t->shape[t->dtype == WQ_INT4_T ? 1 : 0];
+    N = t->shape[t->dtype == WQ_INT4_T ? 0 : 1];
+  };
+  int64_t K, N, K2, N2;
+  kn(src, K, N);
+  kn(dst, K2, N2);
+  if (K != K2 || N != N2) return fail(WQ_ERR_SHAPE, "src and dst must hold one (k, n) weight");
+  const bool tiled = src->dtype == WQ_INT4_TILED || dst->dtype == WQ_INT4_TILED;
+  if (tiled && N % 16 != 0)
+    return fail(WQ_ERR_SHAPE, "the INT4_TILED layout needs n divisible by 16");
+  if (src->dtype == WQ_INT4_T || dst->dtype == WQ_INT4_T ? K % 2 != 0 : false)
+    return fail(WQ_ERR_SHAPE, "the INT4_T layout packs along k, which must be even");
+  if (src->dtype == WQ_INT4 || dst->dtype == WQ_INT4 ? N % 2 != 0 : false)
+    return fail(WQ_ERR_SHAPE, "the INT4 layout packs along n, which must be even");
+  if (K * N > 0 && (!src->data || !dst->data))
     return fail(WQ_ERR_NULL, "non-empty tensors need data pointers");
-  if (numel(src) > 0 && ((uintptr_t)tl->data % 16) != 0)
-    return fail(WQ_ERR_UNSUPPORTED, "an INT4_TILED tensor must be 16-byte aligned");
+  if (K * N > 0 && tiled) {
+    const wq_tensor *tl = src->dtype == WQ_INT4_TILED ? src : dst;
+    if (((uintptr_t)tl->data % 16) != 0)
+      return fail(WQ_ERR_UNSUPPORTED, "an INT4_TILED tensor must be 16-byte aligned");
+  }
   if (overlap(src, dst)) return fail(WQ_ERR_ALIAS, "dst overlaps src");
-  if (numel(src) == 0) return ok();
-  const int64_t K = src->shape[0], N = src->shape[1];
-  cudaError_t e = to_tiled
-                      ? launch_int4_nd_to_tiled((const uint8_t *)src->data, (uint8_t *)dst->data, K, N,
-                                                (cudaStream_t)stream)
-                      : launch_int4_tiled_to_nd((const uint8_t *)src->data, (uint8_t *)dst->data, K, N,
-                                                (cudaStream_t)stream);
+  if (K * N == 0) return ok();
+  cudaStream_t s = (cudaStream_t)stream;
+  const uint8_t *in = (const uint8_t *)src->data;
+  uint8_t *out = (uint8_t *)dst->data;
+  cudaError_t e;
+  if (src->dtype == WQ_INT4 && dst->dtype == WQ_INT4_TILED)
+    e = launch_int4_nd_to_tiled(in, out, K, N, s);
+  else if (src->dtype == WQ_INT4_TILED && dst->dtype == WQ_INT4)
+    e = launch_int4_tiled_to_nd(in, out, K, N, s);
+  else
+    e = launch_int4_remap(in, src->dtype, out, dst->dtype, K, N, s);
   if (e != cudaSuccess) return cuda_fail(e, "layout conversion launch");
   return ok();
 }

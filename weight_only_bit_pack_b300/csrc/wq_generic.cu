@@ -8,7 +8,9 @@
 // exact in fp32; adding O rounds once), r(k) = floor(k/group) or 0, c(n) = n or
 // 0. One thread owns one column n and eight rows; each block covers 128
 // columns, one split of k, and a grid-stride range of 8-row blocks. The weight
-// is INT8, dense INT4 or INT4 in the kernel-native tiled layout (LAYOUT 8, 4, 6).
+// is INT8, dense INT4 or INT4 in the kernel-native tiled layout (LAYOUT 8, 4, 6),
+// or transposed -- stored (N, K), K contiguous -- as INT8 (LAYOUT 10) or INT4
+// packed along K (LAYOUT 9).
 #include "wq_internal.h"
 #include "wq_common.cuh"
 
@@ -44,6 +46,12 @@ __global__ void __launch_bounds__(kGenThreads)
       } else if (LAYOUT == 6) {
         const int nib = (int)tiled_nibble(x2, k, n, N);
         q = nib >= 8 ? nib - 16 : nib;
+      } else if (LAYOUT == 9) {
+        const uint32_t b = x2[n * (K / 2) + (k >> 1)];
+        const int nib = (k & 1) ? (int)(b >> 4) : (int)(b & 0xFu);
+        q = nib >= 8 ? nib - 16 : nib;
+      } else if (LAYOUT == 10) {
+        q = (int)reinterpret_cast<const int8_t *>(x2)[n * K + k];
       } else {
         q = (int)reinterpret_cast<const int8_t *>(x2)[k * N + n];
       }
@@ -94,16 +102,22 @@ cudaError_t launch_generic(const Problem &p, const Plan &plan, void *ws, cudaStr
   generic_gemm_kernel<DT, LAYOUT><<<grid, kGenThreads, 0, s>>>(                                   \
       static_cast<const Elem<DT>::T *>(p.x1), x2, static_cast<const Elem<DT>::T *>(p.scale),      \
       static_cast<const Elem<DT>::T *>(p.offset), p.M, p.K, p.N, p.group, p.Ns, plan.ksplit, part)
-  const int layout = p.wbits == 8 ? 8 : (p.tiled ? 6 : 4);
-  if (p.dtype == WQ_BF16) {
-    if (layout == 4) WQ_GEN_LAUNCH(WQ_BF16, 4);
-    else if (layout == 6) WQ_GEN_LAUNCH(WQ_BF16, 6);
-    else WQ_GEN_LAUNCH(WQ_BF16, 8);
-  } else {
-    if (layout == 4) WQ_GEN_LAUNCH(WQ_F16, 4);
-    else if (layout == 6) WQ_GEN_LAUNCH(WQ_F16, 6);
-    else WQ_GEN_LAUNCH(WQ_F16, 8);
+  const int layout = p.transposed ? (p.wbits == 8 ? 10 : 9)
+                                  : (p.wbits == 8 ? 8 : (p.tiled ? 6 : 4));
+#define WQ_GEN_LAYOUTS(DT)                                       \
+  switch (layout) {                                              \
+    case 4: WQ_GEN_LAUNCH(DT, 4); break;                         \
+    case 6: WQ_GEN_LAUNCH(DT, 6); break;                         \
+    case 9: WQ_GEN_LAUNCH(DT, 9); break;                         \
+    case 10: WQ_GEN_LAUNCH(DT, 10); break;                       \
+    default: WQ_GEN_LAUNCH(DT, 8); break;                        \
   }
+  if (p.dtype == WQ_BF16) {
+    WQ_GEN_LAYOUTS(WQ_BF16)
+  } else {
+    WQ_GEN_LAYOUTS(WQ_F16)
+  }
+#undef WQ_GEN_LAYOUTS
 #undef WQ_GEN_LAUNCH
   return cudaGetLastError();
 }

@@ -19,6 +19,7 @@ struct Problem {
   int dtype = WQ_BF16;     // WQ_F16 or WQ_BF16 (x1, scale, offset, bias, residual, gamma, y, normOut)
   int wbits = 4;           // 4 (packed, two per byte along N) or 8
   bool tiled = false;      // INT4 in the kernel-native tiled layout (wq_tiled.cu)
+  bool transposed = false; // x2 stored as its (N, K) transpose, K contiguous
   int smode = kPerTensor;  // ScaleMode
   int64_t group = 0;       // > 0 only for kPerGroup
   int64_t G = 1;           // scale rows: ceil(K/group) for kPerGroup, else 1
@@ -81,6 +82,9 @@ cudaError_t launch_int4_nd_to_tiled(const uint8_t *in, uint8_t *out, int64_t K, 
                                     cudaStream_t s);
 cudaError_t launch_int4_tiled_to_nd(const uint8_t *in, uint8_t *out, int64_t K, int64_t N,
                                     cudaStream_t s);
+// Any layout of a (K, N) INT4 weight (WQ_INT4, WQ_INT4_T, WQ_INT4_TILED) into another.
+cudaError_t launch_int4_remap(const uint8_t *in, int in_layout, uint8_t *out, int out_layout,
+                              int64_t K, int64_t N, cudaStream_t s);
 cudaError_t launch_decode_tiled(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
 // Per-token symmetric dynamic quantization (wq_dynquant.cu); bits 8 or 4.
 cudaError_t launch_dynamic_quant(const void *x, const void *smooth, int dtype, int64_t M, int64_t K,

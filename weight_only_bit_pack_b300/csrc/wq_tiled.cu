@@ -1,5 +1,5 @@
 // Kernel-native tiled INT4 layout: the pack into it and the conversions between
-// it and the dense row-major INT4 layout.
+// the INT4 layouts of a weight (dense, transposed, tiled).
 //
 // aclnnConvertWeightToINT4Pack, "Function description": besides the dense ND
 // output, the pack can emit the same 4-bit values in a layout tiled for the
@@ -25,7 +25,9 @@
 //
 // The pack reads a 64 x 128 block of int32 through shared memory (coalesced
 // loads, conflict-free column reads with a 129-word pitch) and writes whole
-// 512-byte tiles; the conversions use the same block shape.
+// 512-byte tiles; the dense <-> tiled conversions use the same block shape, and
+// a plain one-byte-per-thread remap covers the pairs with the transposed layout
+// (an offline, once-per-weight step).
 #include "wq_common.cuh"
 #include "wq_internal.h"
 
@@ -117,6 +119,53 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Nibble of logical element (k, n) of a (K, N) weight in layout `lay`.
+__device__ __forceinline__ uint32_t nibble_at(const uint8_t *w, int lay, int64_t k, int64_t n,
+                                              int64_t K, int64_t N) {
+  if (lay == WQ_INT4_TILED) return tiled_nibble(w, k, n, N);
+  const uint32_t b = lay == WQ_INT4 ? w[k * (N / 2) + n / 2] : w[n * (K / 2) + k / 2];
+  const int odd = lay == WQ_INT4 ? (int)(n & 1) : (int)(k & 1);
+  return odd ? (b >> 4) : (b & 0xFu);
+}
+
+// Logical element (k, n) held by nibble h (0 = bits 3:0) of byte i of a
+// (K, N) weight in layout `lay`; false for a padding nibble of the tiled layout.
+__device__ __forceinline__ bool element_of(int lay, int64_t i, int h, int64_t K, int64_t N,
+                                           int64_t &k, int64_t &n) {
+  if (lay == WQ_INT4) {
+    k = i / (N / 2);
+    n = 2 * (i % (N / 2)) + h;
+  } else if (lay == WQ_INT4_T) {
+    n = i / (K / 2);
+    k = 2 * (i % (K / 2)) + h;
+  } else {
+    const int64_t tile = i / kTileBytes, r = i % kTileBytes;
+    const int lane = (int)(r / 16), j = (int)((r % 16) / 4), p = 2 * (int)(r % 4) + h;
+    int kk, cc;
+    tiled_element(lane >> 2, lane & 3, j, p, kk, cc);
+    k = (tile / (N / kTC)) * kTK + kk;
+    n = (tile % (N / kTC)) * kTC + cc;
+  }
+  return k < K;
+}
+
+// One thread per output byte: each of its two nibbles is fetched from the
+// source layout (any pair of WQ_INT4, WQ_INT4_T, WQ_INT4_TILED).
+__global__ void __launch_bounds__(256)
+    remap_kernel(const uint8_t *__restrict__ in, int in_lay, uint8_t *__restrict__ out,
+                 int out_lay, int64_t K, int64_t N, int64_t nbytes) {
+  for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < nbytes;
+       i += (int64_t)gridDim.x * 256) {
+    uint32_t byte = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      int64_t k, n;
+      if (element_of(out_lay, i, h, K, N, k, n)) byte |= nibble_at(in, in_lay, k, n, K, N) << (4 * h);
+    }
+    out[i] = (uint8_t)byte;
+  }
+}
+
 dim3 tiled_grid(int64_t K, int64_t N) {
   return dim3((unsigned)((N + kBlockCols - 1) / kBlockCols), (unsigned)((K + kTK - 1) / kTK), 1);
 }
@@ -142,6 +191,16 @@ cudaError_t launch_int4_nd_to_tiled(const uint8_t *in, uint8_t *out, int64_t K, 
 cudaError_t launch_int4_tiled_to_nd(const uint8_t *in, uint8_t *out, int64_t K, int64_t N,
                                     cudaStream_t s) {
   to_nd_kernel<<<tiled_grid(K, N), 256, 0, s>>>(in, out, K, N);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_int4_remap(const uint8_t *in, int in_layout, uint8_t *out, int out_layout,
+                              int64_t K, int64_t N, cudaStream_t s) {
+  const int64_t nbytes = out_layout == WQ_INT4_TILED ? (int64_t)tiled_int4_bytes(K, N) : K * N / 2;
+  int64_t blocks = (nbytes + 255) / 256;
+  const int64_t cap = (int64_t)device_info().sms * 16;
+  if (blocks > cap) blocks = cap;
+  remap_kernel<<<(unsigned)blocks, 256, 0, s>>>(in, in_layout, out, out_layout, K, N, nbytes);
   return cudaGetLastError();
 }
 
