@@ -670,7 +670,8 @@ def run_ours(args, world, rank, local):
     roof = roofline(p, ms_step, peaks)
     # the dominant kernel's DRAM bytes per launch, from the committed ncu capture
     kname = {3: "prefill_kernel", 2: "decode_kernel"}.get(chosen, "generic_gemm_kernel")
-    roof["traffic"] = traffic_record(kname, p.name)
+    wname = p.name + ("_tiled" if runner.tiled else "")
+    roof["traffic"] = traffic_record(kname, wname)
     roof["traffic_source"] = ("profiles/traffic.md (ncu dram__bytes_read.sum + "
                               "dram__bytes_write.sum of one launch)"
                               if roof["traffic"] is not None else
@@ -687,7 +688,7 @@ def run_ours(args, world, rank, local):
         "warmup": W, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": {torch.bfloat16: "bf16", torch.float16: "f16"}[p.dtype],
         "data": "synthetic (seeded; weights random INT4/INT8, activations N(0,1))",
-        "config": {"workload": p.name, "M": p.M, "K": p.K, "N": p.N, "wbits": p.wbits,
+        "config": {"workload": wname, "M": p.M, "K": p.K, "N": p.N, "wbits": p.wbits,
                    "group": p.group, "offset": p.offset is not None, "bias": p.bias is not None,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": runner.l2_note(),
