@@ -53,6 +53,10 @@ def _load(path=None):
         lib.wqo_dequant.argtypes = [P, I, I, P, P, I, I, I, P]
         lib.wqo_matmul_add_rmsnorm.argtypes = [P, I, I, P, I, P, P, I, I, I, P, P, P,
                                                ctypes.c_double, P, P, P]
+        lib.wqo_pack_fp4.argtypes = [P, I, I, P]
+        lib.wqo_pack_fp4.restype = ctypes.c_int
+        lib.wqo_mx_matmul_add.argtypes = [P, P, P, P, I, I, I, P]
+        lib.wqo_mx_matmul_add.restype = ctypes.c_int
         lib.wqo_dynamic_quant.argtypes = [P, I, I, P, ctypes.c_int, P, P]
         lib.wqo_dynamic_quant.restype = ctypes.c_int
         lib.wqo_tiled_bytes.argtypes = [I, I]
@@ -153,6 +157,34 @@ def unpack_int4_tiled(b, K: int, N: int) -> np.ndarray:
     if rc:
         raise ValueError("wqo_unpack_int4_tiled rejected its shape")
     return out
+
+
+def pack_fp4(v) -> np.ndarray:
+    """(K, N) float32 -> (K, N/2) bytes of FP4 E2M1 codes (nearest, ties to the even
+    code, saturating at 6), even column in bits 3:0."""
+    if hasattr(v, "detach"):
+        v = v.detach().to("cpu").float().numpy()
+    v = np.ascontiguousarray(np.asarray(v, dtype=np.float32))
+    K, N = v.shape
+    out = np.empty((K, N // 2), dtype=np.uint8)
+    if _load().wqo_pack_fp4(_p(v), K, N, _p(out)):
+        raise ValueError("wqo_pack_fp4 rejected its shape")
+    return out
+
+
+def mx_matmul_add(x1, s1, x2, s2, y, K: int):
+    """y (M, N) fp64 plus the mx block-scaled product of the packed FP4 x1 (M, K/2)
+    and x2 (K, N/2) with E8M0 scales s1 (M, ceil(K/32)) and s2 (ceil(K/32), N)."""
+    def u8(a):
+        if hasattr(a, "detach"):
+            a = a.detach().to("cpu").numpy()
+        return np.ascontiguousarray(np.asarray(a, dtype=np.uint8))
+    x1, s1, x2, s2 = u8(x1), u8(s1), u8(x2), u8(s2)
+    yy = _f64(y).copy()
+    M, N = yy.shape
+    if _load().wqo_mx_matmul_add(_p(x1), _p(s1), _p(x2), _p(s2), M, K, N, _p(yy)):
+        raise ValueError("wqo_mx_matmul_add rejected its arguments")
+    return yy
 
 
 def dynamic_quant(x, smooth=None, bits: int = 8):

@@ -282,3 +282,69 @@ int wqo_dynamic_quant(const float *x, int64_t M, int64_t K, const float *smooth,
     free(row);
     return WQO_OK;
 }
+
+/* FP4 E2M1 pack (aclnnConvertWeightToINT4Pack, "Function description": FLOAT
+ * weights are packed into dense FLOAT4_E2M1). An E2M1 code is sign (bit 3),
+ * a 2-bit exponent and a 1-bit mantissa: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6
+ * for codes 0..7. A float becomes the nearest magnitude, ties to the even code,
+ * saturating at 6 (readings: the page fixes neither rounding nor overflow; a
+ * NaN input is outside the operator's domain). Codes pack two per byte along
+ * the last dimension, even column in bits 3:0, like the INT4 pack. */
+static const double kE2M1[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+static int e2m1_code(double v)
+{
+    int sign = v < 0 || (v == 0 && signbit(v)) ? 8 : 0;
+    double a = fabs(v);
+    int best = 0;
+    for (int c = 1; c < 8; ++c) {
+        double dc = fabs(a - kE2M1[c]), db = fabs(a - kE2M1[best]);
+        if (dc < db || (dc == db && (c % 2 == 0))) best = c;  /* tie: the even code */
+    }
+    if (a >= 6.0) best = 7;
+    return sign | best;
+}
+
+int wqo_pack_fp4(const float *v, int64_t K, int64_t N, uint8_t *out)
+{
+    if (K < 0 || N < 0 || (N % 2) != 0) return WQO_EINVAL;
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t j = 0; j < N / 2; ++j)
+            out[k * (N / 2) + j] = (uint8_t)(e2m1_code(v[k * N + 2 * j]) |
+                                             (e2m1_code(v[k * N + 2 * j + 1]) << 4));
+    return WQO_OK;
+}
+
+static double e2m1_value(int code)
+{
+    double m = kE2M1[code & 7];
+    return (code & 8) ? -m : m;
+}
+
+/* mx block-scaled matmul with in-place add (aclnnQuantBatchMatmulInplaceAdd,
+ * "Function description", mx quantization formula):
+ *   y[m,n] = sum_{j<kLoops} (sum_{k in slice j} x1[m,k] * x2[k,n]) * (scale1[m,j] * scale2[j,n]) + y[m,n]
+ * with gsK = 32, kLoops = ceil(K/32) (a short last slice), x1 (M, K) and x2
+ * (K, N) FP4 E2M1 codes packed two per byte along their last dimension, and
+ * E8M0 scales: byte e stands for 2^(e - 127). fp64, slices in ascending j. */
+int wqo_mx_matmul_add(const uint8_t *x1, const uint8_t *s1, const uint8_t *x2, const uint8_t *s2,
+                      int64_t M, int64_t K, int64_t N, double *y)
+{
+    if (M < 0 || K < 1 || N < 0 || (K % 2) || (N % 2)) return WQO_EINVAL;
+    int64_t J = (K + 31) / 32;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < J; ++j) {
+                double slice = 0.0;
+                for (int64_t k = 32 * j; k < K && k < 32 * (j + 1); ++k) {
+                    uint8_t a = x1[m * (K / 2) + k / 2], b = x2[k * (N / 2) + n / 2];
+                    int ca = (k % 2) ? (a >> 4) : (a & 15), cb = (n % 2) ? (b >> 4) : (b & 15);
+                    slice += e2m1_value(ca) * e2m1_value(cb);
+                }
+                acc += slice * ldexp(1.0, (int)s1[m * J + j] - 127) * ldexp(1.0, (int)s2[j * N + n] - 127);
+            }
+            y[m * N + n] += acc;
+        }
+    return WQO_OK;
+}

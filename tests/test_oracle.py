@@ -192,6 +192,91 @@ def test_dynamic_quant_properties(bits):
     assert np.array_equal(q3, q4) and np.array_equal(s3, s4)
 
 
+def _read_fp4_literals():
+    rows = []
+    with open(os.path.join(GOLDEN, "fp4_literals.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            vals, out = line.split("->")
+            rows.append(([float(v) for v in vals.split()], int(out, 16)))
+    return rows
+
+
+@pytest.mark.parametrize("vals,byte", _read_fp4_literals())
+def test_fp4_pack_literals(vals, byte):
+    assert int(oracle.pack_fp4(np.array([vals], np.float32))[0, 0]) == byte
+
+
+def test_fp4_codes_round_trip_and_midpoints():
+    mags = [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    for c in range(16):
+        v = (-1 if c & 8 else 1) * mags[c & 7]
+        if c == 8:
+            v = -0.0
+        b = oracle.pack_fp4(np.array([[v, 0.0]], np.float32))[0, 0]
+        assert b & 15 == c and b >> 4 == 0
+    for i in range(7):  # a midpoint goes to the neighbour with the even code
+        mid = (mags[i] + mags[i + 1]) / 2
+        b = oracle.pack_fp4(np.array([[mid, 0.0]], np.float32))[0, 0]
+        assert b & 15 == (i if i % 2 == 0 else i + 1)
+
+
+def _fp4_decode(b, n):
+    mags = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    lo, hi = b & 15, b >> 4
+    codes = np.stack([lo, hi], axis=-1).reshape(b.shape[0], -1)[:, :n]
+    return np.where(codes & 8, -1.0, 1.0) * mags[codes & 7]
+
+
+def _mx_problem(M, K, N, seed, scale_spread=4):
+    rng = np.random.default_rng(seed)
+    x1 = oracle.pack_fp4(rng.uniform(-6, 6, (M, K)).astype(np.float32))
+    x2 = oracle.pack_fp4(rng.uniform(-6, 6, (K, N)).astype(np.float32))
+    J = (K + 31) // 32
+    s1 = rng.integers(127 - scale_spread, 128 + scale_spread, (M, J)).astype(np.uint8)
+    s2 = rng.integers(127 - scale_spread, 128 + scale_spread, (J, N)).astype(np.uint8)
+    y = rng.standard_normal((M, N))
+    return x1, s1, x2, s2, y
+
+
+def test_mx_matmul_unit_scales_is_a_plain_matmul():
+    M, K, N = 5, 96, 6
+    x1, s1, x2, s2, y = _mx_problem(M, K, N, 1)
+    s1[:] = 127
+    s2[:] = 127
+    out = oracle.mx_matmul_add(x1, s1, x2, s2, y, K)
+    ref = _fp4_decode(x1, K) @ _fp4_decode(x2, N) + y
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-9)
+
+
+def test_mx_matmul_scales_act_per_slice_and_short_last_slice():
+    """K = 40: slices [0, 32) and [32, 40). Each slice's contribution is its plain
+    product times 2^(s1 - 127) * 2^(s2 - 127); changing one scale changes only its
+    slice, by the power of two."""
+    M, K, N = 3, 40, 4
+    x1, s1, x2, s2, y = _mx_problem(M, K, N, 2)
+    a, b = _fp4_decode(x1, K), _fp4_decode(x2, N)
+    ref = y.copy()
+    for j, (k0, k1) in enumerate(((0, 32), (32, 40))):
+        ref += (a[:, k0:k1] @ b[k0:k1, :]) * np.exp2(s1[:, j:j + 1].astype(float) - 127) \
+            * np.exp2(s2[j:j + 1, :].astype(float) - 127)
+    np.testing.assert_allclose(oracle.mx_matmul_add(x1, s1, x2, s2, y, K), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_mx_matmul_hand_worked():
+    """x1 = [[1, -0.5]], x2 = [[2, 3], [4, -6]], one slice (K = 2), scale1 = 2^1,
+    scale2 = [2^0, 2^-1], y = [[10, 20]]: row products (1*2 - 0.5*4, 1*3 + 0.5*6)
+    = (0, 6), times 2 * (1, 0.5) = (0, 6), plus y = (10, 26)."""
+    x1 = oracle.pack_fp4(np.array([[1, -0.5]], np.float32))
+    x2 = oracle.pack_fp4(np.array([[2, 3], [4, -6]], np.float32))
+    s1 = np.array([[128]], np.uint8)
+    s2 = np.array([[127, 126]], np.uint8)
+    out = oracle.mx_matmul_add(x1, s1, x2, s2, np.array([[10.0, 20.0]]), 2)
+    assert out.tolist() == [[10.0, 26.0]]
+
+
 def test_pack_rejects_odd_n():
     with pytest.raises(ValueError):
         oracle.pack_int4(np.zeros((2, 3), np.int32))

@@ -33,6 +33,10 @@ MUTATIONS = {
                                "int64_t h = kk / 32, jl = (kk % 32) / 16, t = (kk % 16) / 4, e = kk % 4;"),
     "tiled_upper_nibble_pairs": ("int64_t p = (e < 2 ? 0 : 2) + upper + 4 * (e % 2);",
                                  "int64_t p = (e < 2 ? 0 : 4) + upper + 2 * (e % 2);"),
+    "fp4_tie_to_odd": ("(dc == db && (c % 2 == 0))", "(dc == db && (c % 2 == 1))"),
+    "fp4_max_magnitude_8": ("{0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0}", "{0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 8.0}"),
+    "mx_slice_of_32_off": ("k < K && k < 32 * (j + 1)", "k < K && k < 32 * (j + 1) + 1"),
+    "mx_scale2_transposed": ("(int)s2[j * N + n] - 127", "(int)s2[n * J + j] - 127"),
     "dq_round_half_away": ("float rr = rintf(r);", "float rr = roundf(r);"),
     "dq_scale_off_by_one": ("volatile float s = amax / (float)qmax;", "volatile float s = amax / (float)(qmax + 1);"),
     "dq_smooth_ignored": ("if (smooth) v = v * smooth[k];", "(void)smooth;"),
