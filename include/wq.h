@@ -70,7 +70,12 @@ extern "C" {
  * AllReduceAddRmsNorm, "Constraints": x2 may be transposed): a (K, N) weight
  * stored as its (N, K) transpose, row-major with K contiguous; the descriptor
  * gives the stored shape (N, K). INT4_T packs two values per byte along K (k
- * even in bits 3:0), i.e. it is the WQ_INT4 packing of the (N, K) array. */
+ * even in bits 3:0), i.e. it is the WQ_INT4 packing of the (N, K) array.
+ *
+ * WQ_FP4_E2M1 is a logical 4-bit float (sign bit 3, 2-bit exponent, 1-bit
+ * mantissa: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), stored two per byte along the
+ * last dimension like WQ_INT4. WQ_E8M0 is one byte e per element, the power of
+ * two 2^(e - 127), with e = 255 standing for NaN (the OCP MX encoding). */
 typedef enum wq_dtype {
     WQ_F16 = 1,
     WQ_BF16 = 2,
@@ -80,7 +85,9 @@ typedef enum wq_dtype {
     WQ_INT4_TILED = 6,
     WQ_F32 = 7,
     WQ_INT8_T = 8,
-    WQ_INT4_T = 9
+    WQ_INT4_T = 9,
+    WQ_FP4_E2M1 = 10,
+    WQ_E8M0 = 11
 } wq_dtype;
 
 /* Tensor descriptor (the analogue of aclTensor): pointer, element type, rank
@@ -120,7 +127,10 @@ typedef enum wq_kernel {
 /* First phase of the pack (aclnnConvertWeightToINT4Pack).
  *   weight       WQ_INT32, 2-D (K, N), N even, K >= 0, N >= 0. Values should lie
  *                in [-8, 7]; any other value keeps its low four bits (two's
- *                complement truncation).
+ *                complement truncation). Or WQ_F32 (K, N) with a WQ_FP4_E2M1
+ *                output (the page's FLOAT -> FLOAT4_E2M1 pack): each float becomes
+ *                the nearest E2M1 value, ties to the even code, saturating at +-6
+ *                (the page fixes neither; a NaN input is outside the domain).
  *   weight_int4  WQ_INT4, 2-D, logical shape (K, N), i.e. K*N/2 bytes; or
  *                WQ_INT4_TILED (N % 16 == 0, 16-byte aligned), the tiled layout;
  *                or WQ_INT4_T: the same bytes as WQ_INT4, for a `weight` that is
@@ -232,6 +242,31 @@ int32_t wq_matmul_add_rmsnorm_select_kernel(
     const wq_tensor *offset, const wq_tensor *bias, const wq_tensor *residual,
     const wq_tensor *gamma, double eps, int64_t group,
     const wq_tensor *y, const wq_tensor *normOut);
+
+/* ------------------------------------------------------------------ mx block-scaled matmul */
+
+/* First phase of the mx block-scaled matmul with in-place add
+ * (aclnnQuantBatchMatmulInplaceAdd, "Function description", mx quantization):
+ *     y[m,n] += sum_j (sum_{k in slice j} x1[m,k] * x2[k,n]) * scale1[m,j] * scale2[j,n]
+ * over slices of gsK = 32 along K (kLoops = ceil(K/32), the last slice may be
+ * short).
+ *   x1      WQ_FP4_E2M1 (M, K), K even, packed along K (not transposed).
+ *   scale1  WQ_E8M0 (M, ceil(K/32)).
+ *   x2      WQ_FP4_E2M1 (K, N), N even, packed along N.
+ *   scale2  WQ_E8M0 (ceil(K/32), N).
+ *   y       WQ_F32 (M, N), read and written (it must not overlap the inputs).
+ *   ws_bytes out: 0.
+ * Each slice's sum of products is exact in fp32, the scaled slices are added in
+ * fp64 and the sum is added to y and rounded once to fp32. Errors: WQ_ERR_NULL,
+ * WQ_ERR_DTYPE, WQ_ERR_SHAPE, WQ_ERR_ALIAS. Touches no device memory. */
+int32_t wq_mx_matmul_add_get_workspace(const wq_tensor *x1, const wq_tensor *scale1,
+                                       const wq_tensor *x2, const wq_tensor *scale2,
+                                       const wq_tensor *y, uint64_t *ws_bytes);
+
+/* Second phase: enqueue the product on `stream` (a CUDA-core kernel). */
+int32_t wq_mx_matmul_add(const wq_tensor *x1, const wq_tensor *scale1, const wq_tensor *x2,
+                         const wq_tensor *scale2, const wq_tensor *y, void *ws, uint64_t ws_bytes,
+                         void *stream);
 
 /* ------------------------------------------------------------------ dynamic quantization */
 

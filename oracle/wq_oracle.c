@@ -326,7 +326,8 @@ static double e2m1_value(int code)
  *   y[m,n] = sum_{j<kLoops} (sum_{k in slice j} x1[m,k] * x2[k,n]) * (scale1[m,j] * scale2[j,n]) + y[m,n]
  * with gsK = 32, kLoops = ceil(K/32) (a short last slice), x1 (M, K) and x2
  * (K, N) FP4 E2M1 codes packed two per byte along their last dimension, and
- * E8M0 scales: byte e stands for 2^(e - 127). fp64, slices in ascending j. */
+ * E8M0 scales: byte e stands for 2^(e - 127), and 255 for NaN (the OCP MX
+ * encoding; the page does not say). fp64, slices in ascending j. */
 int wqo_mx_matmul_add(const uint8_t *x1, const uint8_t *s1, const uint8_t *x2, const uint8_t *s2,
                       int64_t M, int64_t K, int64_t N, double *y)
 {
@@ -342,7 +343,8 @@ int wqo_mx_matmul_add(const uint8_t *x1, const uint8_t *s1, const uint8_t *x2, c
                     int ca = (k % 2) ? (a >> 4) : (a & 15), cb = (n % 2) ? (b >> 4) : (b & 15);
                     slice += e2m1_value(ca) * e2m1_value(cb);
                 }
-                acc += slice * ldexp(1.0, (int)s1[m * J + j] - 127) * ldexp(1.0, (int)s2[j * N + n] - 127);
+                if (s1[m * J + j] == 255 || s2[j * N + n] == 255) acc += NAN;
+                else acc += slice * ldexp(1.0, (int)s1[m * J + j] - 127) * ldexp(1.0, (int)s2[j * N + n] - 127);
             }
             y[m * N + n] += acc;
         }

@@ -213,3 +213,60 @@ def test_pack_validation(B):
     # empty weight: valid, nothing to do
     assert B.lib.wq_pack_int4(r(D(B, B.DType.INT32, (0, 32))), r(D(B, B.DType.INT4, (0, 32))),
                               None, 0, None) == 0
+
+
+def test_fp4_pack_validation(B):
+    r = ctypes.byref
+    ws = ctypes.c_uint64(7)
+    w = D(B, B.DType.F32, (64, 32)); o = D(B, B.DType.FP4_E2M1, (64, 32))
+    assert B.lib.wq_pack_int4_get_workspace(r(w), r(o), r(ws)) == 0 and ws.value == 0
+    # F32 only with an FP4 output, FP4 only from F32
+    assert B.lib.wq_pack_int4_get_workspace(r(w), r(D(B, B.DType.INT4, (64, 32))), r(ws)) == 2
+    assert B.lib.wq_pack_int4_get_workspace(r(D(B, B.DType.INT32, (64, 32))), r(o), r(ws)) == 2
+    assert B.lib.wq_pack_int4_get_workspace(r(D(B, B.DType.F32, (64, 31))),
+                                            r(D(B, B.DType.FP4_E2M1, (64, 31))), r(ws)) == 3
+    assert B.lib.wq_pack_int4_get_workspace(r(w), r(D(B, B.DType.FP4_E2M1, (32, 32))), r(ws)) == 3
+    alias = D(B, B.DType.FP4_E2M1, (64, 32), addr=w.data + 64)
+    assert B.lib.wq_pack_int4_get_workspace(r(w), r(alias), r(ws)) == 9
+    assert B.lib.wq_pack_int4(r(D(B, B.DType.F32, (0, 32))), r(D(B, B.DType.FP4_E2M1, (0, 32))),
+                              None, 0, None) == 0
+
+
+def _mx(B, M=16, K=96, N=64, J=None):
+    J = (K + 31) // 32 if J is None else J
+    return [D(B, B.DType.FP4_E2M1, (M, K)), D(B, B.DType.E8M0, (M, J)),
+            D(B, B.DType.FP4_E2M1, (K, N)), D(B, B.DType.E8M0, (J, N)), D(B, B.DType.F32, (M, N))]
+
+
+def _mx_ws(B, ds):
+    ws = ctypes.c_uint64(7)
+    st = B.lib.wq_mx_matmul_add_get_workspace(*[ctypes.byref(d) for d in ds], ctypes.byref(ws))
+    return st, ws.value
+
+
+def test_mx_matmul_validation(B):
+    assert _mx_ws(B, _mx(B)) == (0, 0)
+    assert _mx_ws(B, _mx(B, K=70))[0] == 0             # short last slice: J = 3
+    assert _mx_ws(B, _mx(B, M=0))[0] == 0
+    assert _mx_ws(B, _mx(B, K=70, J=2))[0] == 3        # scale slices must be ceil(K/32)
+    assert _mx_ws(B, _mx(B, K=95))[0] == 3             # K odd
+    assert _mx_ws(B, _mx(B, N=63))[0] == 3             # N odd
+    assert _mx_ws(B, _mx(B, K=0))[0] == 3
+    ds = _mx(B); ds[2] = D(B, B.DType.FP4_E2M1, (64, 64))
+    assert _mx_ws(B, ds)[0] == 3                       # x2 rows != K
+    ds = _mx(B); ds[4] = D(B, B.DType.F32, (16, 62))
+    assert _mx_ws(B, ds)[0] == 3
+    ds = _mx(B); ds[0] = D(B, B.DType.INT4, (16, 96))
+    assert _mx_ws(B, ds)[0] == 2
+    ds = _mx(B); ds[3] = D(B, B.DType.INT8, (3, 64))
+    assert _mx_ws(B, ds)[0] == 2
+    ds = _mx(B); ds[4] = D(B, B.DType.F16, (16, 64))
+    assert _mx_ws(B, ds)[0] == 2
+    ds = _mx(B); ds[4] = D(B, B.DType.F32, (16, 64), addr=ds[1].data + 8)
+    assert _mx_ws(B, ds)[0] == 9                       # y overlaps scale1
+    ds = _mx(B); ds[1] = None
+    assert B.lib.wq_mx_matmul_add_get_workspace(*[ctypes.byref(d) if d is not None else None
+                                                  for d in ds], ctypes.byref(ctypes.c_uint64())) == 1
+    # an empty product is valid and launches nothing
+    ds = _mx(B, M=0)
+    assert B.lib.wq_mx_matmul_add(*[ctypes.byref(d) for d in ds], None, 0, None) == 0

@@ -14,7 +14,7 @@ _API = ("pack_int4", "pack_int4_get_workspace", "matmul_add_rmsnorm",
         "WHERE_SELF_CHECK", "noalloc_read_device_status", "set_wait_limits_for_testing",
         "WHERE_PREFILL_ROW_BLOCK", "WHERE_DECODE_GRID", "HEADER_BYTES", "TiledInt4",
         "tiled_bytes", "pack_int4_tiled", "int4_to_tiled", "tiled_to_int4", "dynamic_quant",
-        "TransposedWeight", "convert_int4")
+        "TransposedWeight", "convert_int4", "pack_fp4", "mx_matmul_add")
 
 
 def __getattr__(name):

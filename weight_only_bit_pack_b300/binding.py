@@ -58,6 +58,8 @@ class DType(enum.IntEnum):
     F32 = 7
     INT8_T = 8
     INT4_T = 9
+    FP4_E2M1 = 10
+    E8M0 = 11
 
 
 class WQError(RuntimeError):
@@ -110,6 +112,8 @@ _T = [_P] * 7 + [ctypes.c_double, ctypes.c_int64, _P, _P]
 lib.wq_pack_int4_get_workspace.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint64)]
 lib.wq_pack_int4.argtypes = [_P, _P, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
 lib.wq_convert_int4_layout.argtypes = [_P, _P, ctypes.c_void_p]
+lib.wq_mx_matmul_add_get_workspace.argtypes = [_P, _P, _P, _P, _P, ctypes.POINTER(ctypes.c_uint64)]
+lib.wq_mx_matmul_add.argtypes = [_P, _P, _P, _P, _P, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
 lib.wq_dynamic_quant_get_workspace.argtypes = [_P, _P, _P, _P, ctypes.POINTER(ctypes.c_uint64)]
 lib.wq_dynamic_quant.argtypes = [_P, _P, _P, _P, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
 lib.wq_matmul_add_rmsnorm_get_workspace.argtypes = _T + [ctypes.POINTER(ctypes.c_uint64)]
@@ -135,7 +139,8 @@ for _f in ("wq_pack_int4_get_workspace", "wq_pack_int4", "wq_matmul_add_rmsnorm_
            "wq_matmul_add_rmsnorm_ex", "wq_matmul_add_rmsnorm_select_kernel",
            "wq_read_device_status", "wq_version", "wq_matmul_add_rmsnorm_noalloc",
            "wq_check_device_timeout", "wq_noalloc_read_device_status", "wq_test_set_wait_limits",
-           "wq_convert_int4_layout", "wq_dynamic_quant_get_workspace", "wq_dynamic_quant"):
+           "wq_convert_int4_layout", "wq_dynamic_quant_get_workspace", "wq_dynamic_quant",
+           "wq_mx_matmul_add_get_workspace", "wq_mx_matmul_add"):
     getattr(lib, _f).restype = ctypes.c_int32
 
 _TORCH2WQ = {torch.float16: DType.F16, torch.bfloat16: DType.BF16, torch.int8: DType.INT8,
@@ -281,6 +286,33 @@ def dynamic_quant(x: torch.Tensor, smooth_scales: Optional[torch.Tensor] = None,
     _check(lib.wq_dynamic_quant_get_workspace(*[_ref(v) for v in d], ctypes.byref(ws)))
     _check(lib.wq_dynamic_quant(*[_ref(v) for v in d], None, 0, _stream(stream)))
     return y, scale
+
+
+def pack_fp4(weight: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """(K, N) float32 -> (K, N/2) uint8 of FP4 E2M1 codes (``wq_pack_int4`` with an
+    FP4_E2M1 output): nearest value, ties to the even code, saturating at +-6."""
+    K, N = weight.shape
+    if out is None:
+        out = torch.empty((K, N // 2), dtype=torch.uint8, device=weight.device)
+    wd, od = describe(weight), describe(out, DType.FP4_E2M1, (K, N))
+    ws = ctypes.c_uint64(0)
+    _check(lib.wq_pack_int4_get_workspace(_ref(wd), _ref(od), ctypes.byref(ws)))
+    _check(lib.wq_pack_int4(_ref(wd), _ref(od), None, 0, _stream(stream)))
+    return out
+
+
+def mx_matmul_add(x1: torch.Tensor, scale1: torch.Tensor, x2: torch.Tensor, scale2: torch.Tensor,
+                  y: torch.Tensor, stream=None) -> torch.Tensor:
+    """``y += mx(x1, scale1) @ mx(x2, scale2)`` (``wq_mx_matmul_add``): x1 (M, K/2) and
+    x2 (K, N/2) uint8 FP4 E2M1 codes, scale1 (M, ceil(K/32)) and scale2 (ceil(K/32), N)
+    uint8 E8M0 exponents, y float32 (M, N) updated in place and returned."""
+    M, K, N = x1.shape[0], x1.shape[1] * 2, x2.shape[1] * 2
+    d = [describe(x1, DType.FP4_E2M1, (M, K)), describe(scale1, DType.E8M0),
+         describe(x2, DType.FP4_E2M1, (K, N)), describe(scale2, DType.E8M0), describe(y)]
+    ws = ctypes.c_uint64(0)
+    _check(lib.wq_mx_matmul_add_get_workspace(*[_ref(v) for v in d], ctypes.byref(ws)))
+    _check(lib.wq_mx_matmul_add(*[_ref(v) for v in d], None, 0, _stream(stream)))
+    return y
 
 
 def pack_int4_bytes(n_logical: int, data: torch.Tensor) -> WqTensor:

@@ -55,8 +55,8 @@ int64_t numel(const wq_tensor *t) {
 int64_t elem_bits(int dt) {
   switch (dt) {
     case WQ_F16: case WQ_BF16: return 16;
-    case WQ_INT8: case WQ_INT8_T: return 8;
-    case WQ_INT4: case WQ_INT4_TILED: case WQ_INT4_T: return 4;
+    case WQ_INT8: case WQ_INT8_T: case WQ_E8M0: return 8;
+    case WQ_INT4: case WQ_INT4_TILED: case WQ_INT4_T: case WQ_FP4_E2M1: return 4;
     case WQ_INT32: case WQ_F32: return 32;
     default: return 0;
   }
@@ -95,7 +95,8 @@ const char *dtname(int dt) {
     case WQ_F16: return "F16"; case WQ_BF16: return "BF16"; case WQ_INT8: return "INT8";
     case WQ_INT4: return "INT4"; case WQ_INT32: return "INT32";
     case WQ_INT4_TILED: return "INT4_TILED"; case WQ_F32: return "F32";
-    case WQ_INT8_T: return "INT8_T"; case WQ_INT4_T: return "INT4_T"; default: return "?";
+    case WQ_INT8_T: return "INT8_T"; case WQ_INT4_T: return "INT4_T";
+    case WQ_FP4_E2M1: return "FP4_E2M1"; case WQ_E8M0: return "E8M0"; default: return "?";
   }
 }
 
@@ -384,6 +385,18 @@ const char *wq_last_error(void) { return g_last_error.c_str(); }
 
 static int32_t validate_pack(const wq_tensor *w, const wq_tensor *o) {
   if (!w || !o) return fail(WQ_ERR_NULL, "weight and weight_int4 are required");
+  if (w->dtype == WQ_F32 || o->dtype == WQ_FP4_E2M1) {  // FLOAT -> FLOAT4_E2M1
+    if (w->dtype != WQ_F32 || o->dtype != WQ_FP4_E2M1)
+      return fail(WQ_ERR_DTYPE, "an FP4_E2M1 pack takes an F32 weight, got %s -> %s",
+                  dtname(w->dtype), dtname(o->dtype));
+    if (!valid_rank(w) || !valid_rank(o) || w->ndim != 2 || !same_shape(w, o))
+      return fail(WQ_ERR_SHAPE, "weight and the output must be 2-D of one logical shape");
+    if (w->shape[1] % 2 != 0) return fail(WQ_ERR_SHAPE, "the last dimension must be even for FP4");
+    if (numel(w) > 0 && (!w->data || !o->data))
+      return fail(WQ_ERR_NULL, "non-empty tensors need data pointers");
+    if (overlap(w, o)) return fail(WQ_ERR_ALIAS, "the output overlaps the weight");
+    return WQ_OK;
+  }
   if (w->dtype != WQ_INT32) return fail(WQ_ERR_DTYPE, "weight must be INT32, got %s", dtname(w->dtype));
   if (o->dtype != WQ_INT4 && o->dtype != WQ_INT4_TILED && o->dtype != WQ_INT4_T)
     return fail(WQ_ERR_DTYPE, "weight_int4 must be INT4, INT4_TILED or INT4_T, got %s",
@@ -416,6 +429,12 @@ int32_t wq_pack_int4(const wq_tensor *w, const wq_tensor *o, void *ws, uint64_t 
   int32_t st = validate_pack(w, o);
   if (st) return st;
   if (numel(w) == 0) return ok();
+  if (o->dtype == WQ_FP4_E2M1) {
+    cudaError_t e = launch_pack_fp4((const float *)w->data, (uint8_t *)o->data, w->shape[0],
+                                    w->shape[1], (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "FP4 pack kernel launch");
+    return ok();
+  }
   cudaError_t e = o->dtype == WQ_INT4_TILED
                       ? launch_pack_int4_tiled((const int32_t *)w->data, (uint8_t *)o->data,
                                                w->shape[0], w->shape[1], (cudaStream_t)stream)
@@ -469,6 +488,67 @@ int32_t wq_convert_int4_layout(const wq_tensor *src, const wq_tensor *dst, void 
   else
     e = launch_int4_remap(in, src->dtype, out, dst->dtype, K, N, s);
   if (e != cudaSuccess) return cuda_fail(e, "layout conversion launch");
+  return ok();
+}
+
+// ------------------------------------------------------------------ mx block-scaled matmul
+
+static int32_t validate_mx(const wq_tensor *x1, const wq_tensor *s1, const wq_tensor *x2,
+                           const wq_tensor *s2, const wq_tensor *y, int64_t &M, int64_t &K,
+                           int64_t &N) {
+  if (!x1 || !s1 || !x2 || !s2 || !y) return fail(WQ_ERR_NULL, "x1, scale1, x2, scale2 and y are required");
+  const wq_tensor *all[] = {x1, s1, x2, s2, y};
+  for (const wq_tensor *t : all)
+    if (!valid_rank(t) || t->ndim != 2) return fail(WQ_ERR_SHAPE, "every operand is 2-D");
+  if (x1->dtype != WQ_FP4_E2M1 || x2->dtype != WQ_FP4_E2M1)
+    return fail(WQ_ERR_DTYPE, "x1 and x2 must be FP4_E2M1");
+  if (s1->dtype != WQ_E8M0 || s2->dtype != WQ_E8M0)
+    return fail(WQ_ERR_DTYPE, "scale1 and scale2 must be E8M0");
+  if (y->dtype != WQ_F32) return fail(WQ_ERR_DTYPE, "y must be F32");
+  M = x1->shape[0];
+  K = x1->shape[1];
+  N = x2->shape[1];
+  if (K < 1 || K > kMaxKN || N > kMaxKN || M > kMaxRows)
+    return fail(WQ_ERR_SHAPE, "k must lie in [1, 65535], n in [0, 65535]");
+  if (K % 2 || N % 2) return fail(WQ_ERR_SHAPE, "k and n must be even (two FP4 codes per byte)");
+  if (x2->shape[0] != K) return fail(WQ_ERR_SHAPE, "x2 must be (k, n) with x1's k");
+  const int64_t J = (K + 31) / 32;
+  if (s1->shape[0] != M || s1->shape[1] != J)
+    return fail(WQ_ERR_SHAPE, "scale1 must be (m, ceil(k/32) = %lld)", (long long)J);
+  if (s2->shape[0] != J || s2->shape[1] != N)
+    return fail(WQ_ERR_SHAPE, "scale2 must be (ceil(k/32) = %lld, n)", (long long)J);
+  if (y->shape[0] != M || y->shape[1] != N) return fail(WQ_ERR_SHAPE, "y must be (m, n)");
+  for (const wq_tensor *t : all)
+    if (numel(t) > 0 && !t->data) return fail(WQ_ERR_NULL, "a non-empty tensor has no data");
+  const wq_tensor *ins[] = {x1, s1, x2, s2};
+  for (const wq_tensor *t : ins)
+    if (overlap(y, t)) return fail(WQ_ERR_ALIAS, "y overlaps an input");
+  return WQ_OK;
+}
+
+int32_t wq_mx_matmul_add_get_workspace(const wq_tensor *x1, const wq_tensor *s1,
+                                       const wq_tensor *x2, const wq_tensor *s2,
+                                       const wq_tensor *y, uint64_t *ws_bytes) {
+  if (!ws_bytes) return fail(WQ_ERR_NULL, "ws_bytes is required");
+  int64_t M, K, N;
+  int32_t st = validate_mx(x1, s1, x2, s2, y, M, K, N);
+  if (st) return st;
+  *ws_bytes = 0;
+  return ok();
+}
+
+int32_t wq_mx_matmul_add(const wq_tensor *x1, const wq_tensor *s1, const wq_tensor *x2,
+                         const wq_tensor *s2, const wq_tensor *y, void *ws, uint64_t ws_bytes,
+                         void *stream) {
+  (void)ws; (void)ws_bytes;
+  int64_t M, K, N;
+  int32_t st = validate_mx(x1, s1, x2, s2, y, M, K, N);
+  if (st) return st;
+  if (M == 0 || N == 0) return ok();
+  cudaError_t e = launch_mx_matmul_add((const uint8_t *)x1->data, (const uint8_t *)s1->data,
+                                       (const uint8_t *)x2->data, (const uint8_t *)s2->data,
+                                       (float *)y->data, M, K, N, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "mx matmul launch");
   return ok();
 }
 

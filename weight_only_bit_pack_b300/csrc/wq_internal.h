@@ -86,6 +86,11 @@ cudaError_t launch_int4_tiled_to_nd(const uint8_t *in, uint8_t *out, int64_t K, 
 cudaError_t launch_int4_remap(const uint8_t *in, int in_layout, uint8_t *out, int out_layout,
                               int64_t K, int64_t N, cudaStream_t s);
 cudaError_t launch_decode_tiled(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
+// FP4 E2M1 pack and the mx block-scaled matmul (wq_fp4.cu).
+cudaError_t launch_pack_fp4(const float *in, uint8_t *out, int64_t K, int64_t N, cudaStream_t s);
+cudaError_t launch_mx_matmul_add(const uint8_t *x1, const uint8_t *s1, const uint8_t *x2,
+                                 const uint8_t *s2, float *y, int64_t M, int64_t K, int64_t N,
+                                 cudaStream_t s);
 // Per-token symmetric dynamic quantization (wq_dynquant.cu); bits 8 or 4.
 cudaError_t launch_dynamic_quant(const void *x, const void *smooth, int dtype, int64_t M, int64_t K,
                                  int bits, void *y, float *scale, cudaStream_t s);
