@@ -15,13 +15,15 @@
 //   warps 4-11   dequant: packed weight -> B operand (W^T, 256 x 64, K-major,
 //                128-byte swizzle), in one of two forms (below).
 //   warps 12-15  epilogue (one per TMEM lane quarter): y = acc + bias +
-//                residual, written to HBM; per-row partial sum(y^2) (of the
-//                fp32 y) published to the workspace; the accumulator is handed
-//                back to the MMA as soon as it has been read. Then, for the
-//                previous tile, wait until every n-tile of its row block has
-//                published, sum the partials in a fixed order, and write
-//                normOut = y * rstd * gamma from the y this thread stored
-//                (still in L2: a row block of y is 128 x N x 2 bytes).
+//                residual, with the residual read and y written as 32 x 32
+//                boxes through shared memory by the TMA (the next residual box
+//                is in flight while one is used); per-row partial sum(y^2) (of
+//                the fp32 y) published to the workspace; the accumulator is
+//                handed back to the MMA as soon as it has been read. Then, for
+//                the previous tile, wait until every n-tile of its row block
+//                has published and write normOut = y * rstd * gamma a row per
+//                warp instruction (coalesced), rstd from the partials summed in
+//                a fixed order, y from L2 (a row block of y is 128 MH x N x 2 bytes).
 // Operand modes:
 //   RAWQ   per-tensor / per-channel scales: B holds the integer q itself (exact
 //          in fp16 and bf16), the MMA accumulates x1*q in fp32, and the epilogue
@@ -68,10 +70,11 @@ using namespace sm100;
 
 constexpr int BM = 128, BN = 256, BK = 64;
 // Stage counts: NR raw stages (x1 tile + packed weight tile + scale/offset
-// rows) and NB dequantized-weight stages, within 227 KB of shared memory:
-// INT8 tiles are twice as large, and a 256-row x1 tile twice as large again.
-template <int WBITS, int MH> struct Stages {
-  static constexpr int NR = MH == 2 ? 3 : (WBITS == 4 ? 4 : 3), NB = MH == 2 ? 2 : 3;
+// rows) and NB dequantized-weight stages, within 227 KB of shared memory next
+// to the epilogue's 24 KB of residual and y boxes: INT8 tiles are twice as
+// large, and a 256-row x1 tile twice as large again.
+template <int WBITS, int MH, int MODE> struct Stages {
+  static constexpr int NR = MH == 2 ? 3 : (WBITS == 4 && MODE == 0 ? 4 : 3), NB = MH == 2 ? 2 : 3;
 };
 constexpr int SO_ROWS = 3;  // group rows a 64-deep k-stage can touch (group >= 32)
 constexpr int kThreads = 512;
@@ -109,7 +112,7 @@ struct PrefillArgs {
 template <int WBITS, int MH, int MODE>
 struct Layout {
   static_assert(MH == 1 || (MH == 2 && WBITS == 4), "256-row tiles with INT4 weights only");
-  static constexpr int NR = Stages<WBITS, MH>::NR, NB = Stages<WBITS, MH>::NB;
+  static constexpr int NR = Stages<WBITS, MH, MODE>::NR, NB = Stages<WBITS, MH, MODE>::NB;
   static constexpr uint32_t A_HALF = BM * BK * 2;             // 16 KB: one 128-row half
   static constexpr uint32_t A_BYTES = MH * A_HALF;
   static constexpr uint32_t BQ_BYTES = BK * BN * WBITS / 8;   // 8 or 16 KB
@@ -120,9 +123,14 @@ struct Layout {
   static constexpr uint32_t BQ_OFF = A_OFF + NR * A_BYTES;
   static constexpr uint32_t B_OFF = BQ_OFF + NR * BQ_BYTES;
   static constexpr uint32_t S_OFF = B_OFF + NB * B_BYTES;
-  static constexpr uint32_t BAR_OFF = S_OFF + NR * SO_BYTES;
-  static constexpr int NBARS = 2 * NR + 2 * NB + 4 + 1;
+  // epilogue boxes of 32 rows x 32 columns (64-byte rows, 64-byte swizzle): per
+  // epilogue warp two residual boxes and one y box
+  static constexpr uint32_t EPI_BOX = 32 * 64;
+  static constexpr uint32_t EPI_OFF = (S_OFF + NR * SO_BYTES + 1023) / 1024 * 1024;
+  static constexpr uint32_t BAR_OFF = EPI_OFF + 3 * 4 * EPI_BOX;
+  static constexpr int NBARS = 2 * NR + 2 * NB + 4 + 1 + 8;
   static constexpr uint32_t SMEM = BAR_OFF + 8 * NBARS + 16 + 1024;
+  static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
 // barrier indices (NR, NB are the kernel's stage counts)
@@ -133,6 +141,7 @@ struct Layout {
 #define ACCFULL(b) (2 * NR + 2 * NB + (b))
 #define ACCEMPTY(b) (2 * NR + 2 * NB + 2 + (b))
 #define DRAIN() (2 * NR + 2 * NB + 4)
+#define RESFULL(q, b) (2 * NR + 2 * NB + 5 + 2 * (q) + (b))
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -182,7 +191,8 @@ template <int DT, int WBITS, int MODE, int MH>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                    const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_dx,
-                   const __grid_constant__ CUtensorMap tm_ox, const PrefillArgs a) {
+                   const __grid_constant__ CUtensorMap tm_ox, const __grid_constant__ CUtensorMap tm_r,
+                   const __grid_constant__ CUtensorMap tm_yo, const PrefillArgs a) {
   using L = Layout<WBITS, MH, MODE>;
   constexpr int NACC = 2 / MH;   // accumulator buffers of MH x 256 TMEM columns
   constexpr int TM = BM * MH;    // output rows per tile
@@ -215,10 +225,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(ACCEMPTY(b)), kEpiWarps);
     }
     mbar_init(BAR(DRAIN()), 1);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(BAR(RESFULL(q, 0)), 1);
+      mbar_init(BAR(RESFULL(q, 1)), 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_x);
     prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_r);
+    prefetch_tmap(&tm_yo);
     if (MODE == kF16Emu) {
       prefetch_tmap(&tm_s);
       if (a.kTilesX) {
@@ -486,73 +502,108 @@ __global__ void __launch_bounds__(kThreads, 1)
   ddone:;
   } else if (warp >= kEpiWarp0) {
     // ---------------------------------------------------------------- epilogue
+    // Thread = TMEM lane = output row. Global traffic goes through 32 x 32
+    // boxes in shared memory moved by the TMA (64-byte rows, 64-byte swizzle:
+    // 16-byte chunk j of row r sits at r*64 + ((j ^ ((r >> 1) & 3)) << 4), so a
+    // row read or written by its thread is free of bank conflicts): the
+    // residual box of the next 32 columns is loaded while this one is used, and
+    // each y box is stored as soon as it is written.
     const int qd = warp & 3;  // TMEM lane quarter
     const int rit = 32 * qd + lane;
     const T *bias = static_cast<const T *>(a.bias);
-    const T *res = static_cast<const T *>(a.residual);
     const T *gam = static_cast<const T *>(a.gamma);
-    T *yout = static_cast<T *>(a.y);
+    const T *yout = static_cast<const T *>(a.y);
     T *nout = static_cast<T *>(a.normOut);
     const uint32_t lane_addr = tmem_base + ((uint32_t)(32 * qd) << 16);
+    const uint32_t rbox = sbase + L::EPI_OFF + (uint32_t)qd * 3u * L::EPI_BOX;  // two residual boxes
+    const uint32_t ybox = rbox + 2u * L::EPI_BOX;
+    const uint32_t row_off = (uint32_t)lane * 64u;
+    const uint32_t swz = (uint32_t)((lane >> 1) & 3);
+    uint32_t rc = 0;      // residual boxes used so far: box rc & 1, phase (rc >> 1) & 1
+    uint32_t issued = 0;  // residual box loads issued (those in [rc, issued) are in flight)
     int lt = 0;
     long long prev_t = -1;
     bool ok = true;
 
+    // Normalises the previous tile's rows: warp = row (32 lanes x 8 columns
+    // cover a 256-column tile row with 16-byte accesses), rows of this warp's
+    // lane quarter only, whose y this warp stored.
     auto normalize = [&](long long t) -> bool {
       const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
       // wait until every n-tile of this row block published its partial sums
       {
         const uint32_t target = (uint32_t)(kEpiWarps * a.nTilesN) + a.extra;
-        const long long t0 = clock64();
         bool done = false;
-        while (true) {
-          done = ld_acquire_u32(a.counters + rb) >= target;
-          if (done || *abort_flag) break;
-          if (clock64() - t0 > a.budget) {
-            *abort_flag = 1;
-            record_timeout(a.status, kWhereRowBlock);
-            break;
+        if (lane == 0) {
+          const long long t0 = clock64();
+          while (true) {
+            done = ld_acquire_u32(a.counters + rb) >= target;
+            if (done || *abort_flag) break;
+            if (clock64() - t0 > a.budget) {
+              *abort_flag = 1;
+              record_timeout(a.status, kWhereRowBlock);
+              break;
+            }
+            __nanosleep(64);
           }
-          __nanosleep(64);
         }
-        if (!__all_sync(0xffffffffu, done)) return false;
+        done = __shfl_sync(0xffffffffu, done, 0);
+        __syncwarp();  // the lanes' reads below come after lane 0's acquire
+        if (!done) return false;
       }
-      const int n0 = nt * BN;
-      const int n1 = n0 + BN < a.N ? n0 + BN : a.N;
+      const int n = nt * BN + 8 * lane;
+      const bool col_ok = n < a.N;  // N % 16 == 0 keeps every 8-column group whole
+      uint4 g = make_uint4(0u, 0u, 0u, 0u);
+      if (col_ok) g = *reinterpret_cast<const uint4 *>(gam + n);
+      const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+      const int nparts = a.nTilesN;
 #pragma unroll 1
       for (int h = 0; h < MH; ++h) {
-        const long long m = (long long)rb * TM + h * BM + rit;
-        if (m >= a.M) break;
-        float tot = 0.f;
-        const float *rp = a.rowpart + m * a.nTilesN;
-        for (int j = 0; j < a.nTilesN; ++j) tot += __ldcg(rp + j);
-        const float rstd = rsqrtf(tot / (float)a.N + a.eps);
-        // the row's y of this tile, as this thread stored it, 8 columns a load
-        // (N % 16 == 0 keeps every 8-column group whole)
-#pragma unroll 4
-        for (int n = n0; n < n1; n += 8) {
-          const uint4 yv = __ldcg(reinterpret_cast<const uint4 *>(yout + m * a.N + n));
-          const uint4 g = *reinterpret_cast<const uint4 *>(gam + n);
-          const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w}, gw[4] = {g.x, g.y, g.z, g.w};
-          uint32_t o[4];
+        const long long mbase = (long long)rb * TM + h * BM + 32 * qd;
+#pragma unroll 1
+        for (int r0 = 0; r0 < 32; r0 += 4) {
+          float tot[4];
+          uint4 yv[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 y2 = unpack2<DT>(yw[i]), g2 = unpack2<DT>(gw[i]);
-            o[i] = pack2<DT>(y2.x * rstd * g2.x, y2.y * rstd * g2.y);
+          for (int u = 0; u < 4; ++u) {
+            const long long m = mbase + r0 + u;
+            tot[u] = 0.f;
+            yv[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (m < a.M) {
+              const float *rp = a.rowpart + m * nparts;
+              for (int j = lane; j < nparts; j += 32) tot[u] += __ldcg(rp + j);
+              if (col_ok) yv[u] = __ldcg(reinterpret_cast<const uint4 *>(yout + m * a.N + n));
+            }
           }
-          *reinterpret_cast<uint4 *>(nout + m * a.N + n) = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) tot[u] += __shfl_xor_sync(0xffffffffu, tot[u], o);
+            const long long m = mbase + r0 + u;
+            if (m < a.M && col_ok) {
+              const float rstd = rsqrtf(tot[u] / (float)a.N + a.eps);
+              const uint32_t yw[4] = {yv[u].x, yv[u].y, yv[u].z, yv[u].w};
+              uint32_t o4[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 y2 = unpack2<DT>(yw[i]), g2 = unpack2<DT>(gw[i]);
+                o4[i] = pack2<DT>(y2.x * rstd * g2.x, y2.y * rstd * g2.y);
+              }
+              *reinterpret_cast<uint4 *>(nout + m * a.N + n) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+            }
+          }
         }
       }
       return true;
     };
 
-    // Pulls this thread's residual rows of tile t into L2 (4 lines of 128 bytes
-    // per 256-column row), a whole main loop before the y pass reads them, so
-    // the pass does not wait on HBM for every 32-column chunk.
+    // Pulls this warp's residual rows of tile t into L2 (lane = row), a whole
+    // main loop before the y pass's boxes read them.
     auto prefetch_residual = [&](long long t) {
       if (t >= a.nTiles) return;
       const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
       const int n0 = nt * BN;
+      const T *res = static_cast<const T *>(a.residual);
 #pragma unroll
       for (int h = 0; h < MH; ++h) {
         const long long m = (long long)rb * TM + h * BM + rit;
@@ -563,20 +614,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(rowp + b));
       }
     };
+    // lane 0: load the residual box (32 rows from m0, 32 columns from n) into box rc & 1
+    auto load_residual = [&](uint32_t k, int n, long long m0) {
+      issued = k + 1;
+      if (lane == 0) {
+        fence_proxy_async_smem();  // the lanes' earlier reads of this box come first
+        const uint32_t bar = BAR(RESFULL(qd, (int)(k & 1)));
+        mbar_arrive_expect_tx(bar, L::EPI_BOX);
+        tma_load_2d(rbox + (k & 1) * L::EPI_BOX, &tm_r, n, (int)m0, bar);
+      }
+    };
+    constexpr int CPH = BN / 32;  // 32-column chunks per tile row
     prefetch_residual(blockIdx.x);
     for (long long t = blockIdx.x; t < a.nTiles && ok; t += gridDim.x, ++lt) {
       const int buf = lt % NACC;
+      const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
+      const int n0 = nt * BN;
+      // boxes of this tile inside the output: nch column boxes for each half
+      // whose 32 rows of this warp start before M
+      const int nch = (a.N - n0 + 31) / 32 < CPH ? (a.N - n0 + 31) / 32 : CPH;
+      auto half_live = [&](int h) { return (long long)rb * TM + h * BM + 32 * qd < a.M; };
+      if (half_live(0)) load_residual(rc, n0, (long long)rb * TM + 32 * qd);  // first box
       if (!wait_bar_warp(BAR(ACCFULL(buf)), (uint32_t)((lt / NACC) & 1), abort_flag, a.status,
                          kWhereEpiAcc)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
-      const int n0 = nt * BN;
 #pragma unroll 1
-      for (int h = 0; h < MH; ++h) {
-        const long long m = (long long)rb * TM + h * BM + rit;
+      for (int h = 0; h < MH && ok; ++h) {
+        if (!half_live(h)) break;
+        const long long mrow0 = (long long)rb * TM + h * BM + 32 * qd;  // the warp's first row
+        const long long m = mrow0 + lane;
         const bool row_ok = m < a.M;
         const uint32_t taddr = lane_addr + (uint32_t)((buf + h) * BN);
         float ss = 0.f;
@@ -591,16 +660,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < nch; ++c, ++rc) {
+          // the next box of this tile (next chunk, or the next half's first)
+          if (c + 1 < nch)
+            load_residual(rc + 1, n0 + 32 * (c + 1), mrow0);
+          else if (h + 1 < MH && half_live(h + 1))
+            load_residual(rc + 1, n0, mrow0 + BM);
           uint32_t r[32];
           tmem_ld32(taddr + 32 * c, r);
           tmem_wait_ld();
+          if (!wait_bar_warp(BAR(RESFULL(qd, (int)(rc & 1))), (rc >> 1) & 1u, abort_flag, a.status,
+                             kWhereEpiAcc)) {
+            ok = false;
+            break;
+          }
+          const uint32_t rb_addr = rbox + (rc & 1) * L::EPI_BOX + row_off;
+          uint32_t yo[16];
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             const int n = n0 + 32 * c + 8 * v;
+            // mm = the operator's x1 @ W for these 8 columns
+            float mmv[8];
             if (n < a.N) {
-              // mm = the operator's x1 @ W for these 8 columns
-              float mmv[8];
               if constexpr (MODE == kRawQ) {
                 uint32_t sw[4], ow[4] = {0u, 0u, 0u, 0u};
                 if (a.Ns == 1) {
@@ -634,36 +715,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                   mmv[i] = scale_pow2(__uint_as_float(r[8 * v + i]), em + en);
                 }
               }
-              uint32_t bw[4] = {0u, 0u, 0u, 0u}, rw[4] = {0u, 0u, 0u, 0u};
-              if (bias) {
-                const uint4 bb = *reinterpret_cast<const uint4 *>(bias + n);
-                bw[0] = bb.x; bw[1] = bb.y; bw[2] = bb.z; bw[3] = bb.w;
-              }
-              if (row_ok) {
-                const uint4 rr = *reinterpret_cast<const uint4 *>(res + m * a.N + n);
-                rw[0] = rr.x; rw[1] = rr.y; rw[2] = rr.z; rw[3] = rr.w;
-              }
-              float yv[8];
-              uint32_t yo[4];
+            } else {
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const float2 b2 = unpack2<DT>(bw[i]);
-                const float2 r2 = unpack2<DT>(rw[i]);
-                yv[2 * i] = mmv[2 * i] + b2.x + r2.x;
-                yv[2 * i + 1] = mmv[2 * i + 1] + b2.y + r2.y;
-                yo[i] = pack2<DT>(yv[2 * i], yv[2 * i + 1]);
-              }
-              if (row_ok) {
+              for (int i = 0; i < 8; ++i) mmv[i] = 0.f;
+            }
+            uint32_t bw[4] = {0u, 0u, 0u, 0u};
+            if (bias && n < a.N) {
+              const uint4 bb = *reinterpret_cast<const uint4 *>(bias + n);
+              bw[0] = bb.x; bw[1] = bb.y; bw[2] = bb.z; bw[3] = bb.w;
+            }
+            uint32_t rw[4];
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(rw[0]), "=r"(rw[1]), "=r"(rw[2]), "=r"(rw[3])
+                         : "r"(rb_addr + ((((uint32_t)v) ^ swz) << 4)));
+            float yv[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) ss = fmaf(yv[i], yv[i], ss);
-                *reinterpret_cast<uint4 *>(yout + m * a.N + n) =
-                    make_uint4(yo[0], yo[1], yo[2], yo[3]);
-              }
+            for (int i = 0; i < 4; ++i) {
+              const float2 b2 = unpack2<DT>(bw[i]);
+              const float2 r2 = unpack2<DT>(rw[i]);
+              yv[2 * i] = mmv[2 * i] + b2.x + r2.x;
+              yv[2 * i + 1] = mmv[2 * i + 1] + b2.y + r2.y;
+              yo[4 * v + i] = pack2<DT>(yv[2 * i], yv[2 * i + 1]);
+            }
+            if (row_ok && n < a.N) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) ss = fmaf(yv[i], yv[i], ss);
             }
           }
+          // the previous y box has been read by its store: overwrite and store it
+          if (lane == 0) bulk_wait_group_read<0>();
+          __syncwarp();
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            st_shared_v4(ybox + row_off + ((((uint32_t)v) ^ swz) << 4), yo[4 * v], yo[4 * v + 1],
+                         yo[4 * v + 2], yo[4 * v + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tm_yo, ybox, n0 + 32 * c, (int)mrow0);
+            bulk_commit_group();
+          }
         }
-        if (row_ok) a.rowpart[m * a.nTilesN + nt] = ss;
+        if (row_ok && ok) a.rowpart[m * a.nTilesN + nt] = ss;
       }  // halves
+      if (!ok) break;
       // the accumulator has been read: hand it back to the MMA issuer
       tc_fence_before();
       __syncwarp();
@@ -678,6 +773,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       prefetch_residual(t + gridDim.x);
       if (prev_t >= 0) {
+        // the previous tile's y boxes have landed in global memory
+        if (lane == 0) {
+          bulk_wait_group_all();
+          fence_proxy_async_global();
+        }
+        __syncwarp();
         if (!normalize(prev_t)) {
           ok = false;
           break;
@@ -685,6 +786,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       prev_t = t;
     }
+    if (lane == 0) {
+      // no copy of this warp may still be in flight when the CTA exits
+      for (uint32_t k = rc; k < issued; ++k) drain_bar(BAR(RESFULL(qd, (int)(k & 1))), (k >> 1) & 1u);
+      bulk_wait_group_all();
+      fence_proxy_async_global();
+    }
+    __syncwarp();
     if (ok && prev_t >= 0) normalize(prev_t);
   }
 
@@ -915,8 +1023,26 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
       if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
   }
+  // residual (read) and y (written) in 32 x 32 boxes of the epilogue
+  CUtensorMap tm_r, tm_yo;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.N * 2};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType t =
+        DT == WQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = enc(&tm_r, t, 2, const_cast<void *>(p.residual), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    r = enc(&tm_yo, t, 2, p.y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   prefill_kernel<DT, WBITS, MODE, MH>
-      <<<plan.grid, kThreads, L::SMEM, s>>>(tm_x, tm_w, tm_s, tm_dx, tm_ox, args);
+      <<<plan.grid, kThreads, L::SMEM, s>>>(tm_x, tm_w, tm_s, tm_dx, tm_ox, tm_r, tm_yo, args);
   return cudaGetLastError();
 }
 
