@@ -71,16 +71,19 @@ using namespace sm100;
 constexpr int BM = 128, BN = 256, BK = 64;
 // Stage counts: NR raw stages (x1 tile + packed weight tile + scale/offset
 // rows) and NB dequantized-weight stages, within 227 KB of shared memory next
-// to the epilogue's 24 KB of residual and y boxes: INT8 tiles are twice as
+// to the epilogue's 32 KB of residual and y boxes: INT8 tiles are twice as
 // large, and a 256-row x1 tile twice as large again.
 template <int WBITS, int MH, int MODE> struct Stages {
-  static constexpr int NR = MH == 2 ? 3 : (WBITS == 4 && MODE == 0 ? 4 : 3), NB = MH == 2 ? 2 : 3;
+  static constexpr int NR = MH == 2 ? 3 : (WBITS == 4 && MODE == 0 ? 4 : 3);
+  static constexpr int NB = MH == 2 || (WBITS == 8 && MODE == 1) ? 2 : 3;
 };
 constexpr int SO_ROWS = 3;  // group rows a 64-deep k-stage can touch (group >= 32)
 constexpr int kThreads = 512;
 constexpr int kDqWarp0 = 4, kDqWarps = 8;
 constexpr int kEpiWarp0 = 12, kEpiWarps = 4;
 constexpr uint32_t kTmemCols = 512;
+// n-tiles per row are at most the grid (<= SMs): 5 per lane cover 160
+constexpr int kPartsPerLane = 5;
 
 // Where a bounded wait gave up (upper bits of the status word).
 enum Where : uint32_t {
@@ -119,16 +122,17 @@ struct Layout {
   static constexpr uint32_t B_BYTES = BN * BK * 2;            // 32 KB
   // F16EMU: rows of S16 pairs (3 KB); RAWQ reads scales in the epilogue
   static constexpr uint32_t SO_BYTES = MODE == kF16Emu ? SO_ROWS * BN * 4 : 0;
+  // epilogue boxes of 32 rows x 32 columns (64-byte rows, 64-byte swizzle): per
+  // epilogue warp three residual boxes and one y box
+  static constexpr uint32_t EPI_BOX = 32 * 64;
+  static constexpr int NRES = 3;
   static constexpr uint32_t A_OFF = 0;
   static constexpr uint32_t BQ_OFF = A_OFF + NR * A_BYTES;
   static constexpr uint32_t B_OFF = BQ_OFF + NR * BQ_BYTES;
-  static constexpr uint32_t S_OFF = B_OFF + NB * B_BYTES;
-  // epilogue boxes of 32 rows x 32 columns (64-byte rows, 64-byte swizzle): per
-  // epilogue warp two residual boxes and one y box
-  static constexpr uint32_t EPI_BOX = 32 * 64;
-  static constexpr uint32_t EPI_OFF = (S_OFF + NR * SO_BYTES + 1023) / 1024 * 1024;
-  static constexpr uint32_t BAR_OFF = EPI_OFF + 3 * 4 * EPI_BOX;
-  static constexpr int NBARS = 2 * NR + 2 * NB + 4 + 1 + 8;
+  static constexpr uint32_t EPI_OFF = B_OFF + NB * B_BYTES;   // 1024-byte aligned
+  static constexpr uint32_t S_OFF = EPI_OFF + (NRES + 1) * 4 * EPI_BOX;
+  static constexpr uint32_t BAR_OFF = S_OFF + NR * SO_BYTES;
+  static constexpr int NBARS = 2 * NR + 2 * NB + 4 + 1 + 4 * NRES;
   static constexpr uint32_t SMEM = BAR_OFF + 8 * NBARS + 16 + 1024;
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
@@ -141,7 +145,7 @@ struct Layout {
 #define ACCFULL(b) (2 * NR + 2 * NB + (b))
 #define ACCEMPTY(b) (2 * NR + 2 * NB + 2 + (b))
 #define DRAIN() (2 * NR + 2 * NB + 4)
-#define RESFULL(q, b) (2 * NR + 2 * NB + 5 + 2 * (q) + (b))
+#define RESFULL(q, b) (2 * NR + 2 * NB + 5 + 3 * (q) + (b))
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -192,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                    const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_dx,
                    const __grid_constant__ CUtensorMap tm_ox, const __grid_constant__ CUtensorMap tm_r,
-                   const __grid_constant__ CUtensorMap tm_yo, const PrefillArgs a) {
+                   const PrefillArgs a) {
   using L = Layout<WBITS, MH, MODE>;
   constexpr int NACC = 2 / MH;   // accumulator buffers of MH x 256 TMEM columns
   constexpr int TM = BM * MH;    // output rows per tile
@@ -225,16 +229,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(ACCEMPTY(b)), kEpiWarps);
     }
     mbar_init(BAR(DRAIN()), 1);
-    for (int q = 0; q < 4; ++q) {
-      mbar_init(BAR(RESFULL(q, 0)), 1);
-      mbar_init(BAR(RESFULL(q, 1)), 1);
-    }
+    for (int q = 0; q < 4; ++q)
+      for (int b = 0; b < L::NRES; ++b) mbar_init(BAR(RESFULL(q, b)), 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_x);
     prefetch_tmap(&tm_w);
     prefetch_tmap(&tm_r);
-    prefetch_tmap(&tm_yo);
     if (MODE == kF16Emu) {
       prefetch_tmap(&tm_s);
       if (a.kTilesX) {
@@ -503,11 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kEpiWarp0) {
     // ---------------------------------------------------------------- epilogue
     // Thread = TMEM lane = output row. Global traffic goes through 32 x 32
-    // boxes in shared memory moved by the TMA (64-byte rows, 64-byte swizzle:
-    // 16-byte chunk j of row r sits at r*64 + ((j ^ ((r >> 1) & 3)) << 4), so a
-    // row read or written by its thread is free of bank conflicts): the
-    // residual box of the next 32 columns is loaded while this one is used, and
-    // each y box is stored as soon as it is written.
+    // boxes in shared memory (64-byte rows, 64-byte swizzle: 16-byte chunk j of
+    // row r sits at r*64 + ((j ^ ((r >> 1) & 3)) << 4), so a row read or
+    // written by its thread is free of bank conflicts): the TMA loads the
+    // residual boxes two ahead of their use, and each y box, written a row per
+    // thread, leaves as coalesced 16-byte stores of whole box rows.
     const int qd = warp & 3;  // TMEM lane quarter
     const int rit = 32 * qd + lane;
     const T *bias = static_cast<const T *>(a.bias);
@@ -515,11 +516,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const T *yout = static_cast<const T *>(a.y);
     T *nout = static_cast<T *>(a.normOut);
     const uint32_t lane_addr = tmem_base + ((uint32_t)(32 * qd) << 16);
-    const uint32_t rbox = sbase + L::EPI_OFF + (uint32_t)qd * 3u * L::EPI_BOX;  // two residual boxes
-    const uint32_t ybox = rbox + 2u * L::EPI_BOX;
+    constexpr int NRES = L::NRES;
+    const uint32_t rbox = sbase + L::EPI_OFF + (uint32_t)qd * (NRES + 1) * L::EPI_BOX;
+    const uint32_t ybox = rbox + (uint32_t)NRES * L::EPI_BOX;
     const uint32_t row_off = (uint32_t)lane * 64u;
     const uint32_t swz = (uint32_t)((lane >> 1) & 3);
-    uint32_t rc = 0;      // residual boxes used so far: box rc & 1, phase (rc >> 1) & 1
+    T *yst = static_cast<T *>(a.y);
+    uint32_t rc = 0;      // residual boxes used so far: box rc % NRES, phase (rc / NRES) & 1
     uint32_t issued = 0;  // residual box loads issued (those in [rc, issued) are in flight)
     int lt = 0;
     long long prev_t = -1;
@@ -564,16 +567,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r0 = 0; r0 < 32; r0 += 4) {
           float tot[4];
           uint4 yv[4];
+          // all loads of the four rows first (kPartsPerLane partial sums per
+          // lane cover the row's n-tiles), then the sums
+          float pv[4][kPartsPerLane];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const long long m = mbase + r0 + u;
-            tot[u] = 0.f;
             yv[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (m < a.M) {
-              const float *rp = a.rowpart + m * nparts;
-              for (int j = lane; j < nparts; j += 32) tot[u] += __ldcg(rp + j);
-              if (col_ok) yv[u] = __ldcg(reinterpret_cast<const uint4 *>(yout + m * a.N + n));
+            const bool live = m < a.M;
+            const float *rp = a.rowpart + m * nparts;
+#pragma unroll
+            for (int i = 0; i < kPartsPerLane; ++i) {
+              const int j = lane + 32 * i;
+              pv[u][i] = live && j < nparts ? __ldcg(rp + j) : 0.f;
             }
+            if (live && col_ok) yv[u] = __ldcg(reinterpret_cast<const uint4 *>(yout + m * a.N + n));
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            tot[u] = 0.f;
+#pragma unroll
+            for (int i = 0; i < kPartsPerLane; ++i) tot[u] += pv[u][i];
           }
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -614,14 +628,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(rowp + b));
       }
     };
-    // lane 0: load the residual box (32 rows from m0, 32 columns from n) into box rc & 1
+    // lane 0: load residual box k (32 rows from m0, 32 columns from n) into box k % NRES
     auto load_residual = [&](uint32_t k, int n, long long m0) {
       issued = k + 1;
       if (lane == 0) {
         fence_proxy_async_smem();  // the lanes' earlier reads of this box come first
-        const uint32_t bar = BAR(RESFULL(qd, (int)(k & 1)));
+        const uint32_t bar = BAR(RESFULL(qd, (int)(k % NRES)));
         mbar_arrive_expect_tx(bar, L::EPI_BOX);
-        tma_load_2d(rbox + (k & 1) * L::EPI_BOX, &tm_r, n, (int)m0, bar);
+        tma_load_2d(rbox + (k % NRES) * L::EPI_BOX, &tm_r, n, (int)m0, bar);
       }
     };
     constexpr int CPH = BN / 32;  // 32-column chunks per tile row
@@ -630,11 +644,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int buf = lt % NACC;
       const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
       const int n0 = nt * BN;
+      // this tile's per-column parameters, 8 columns a lane (lane l holds
+      // columns n0 + 8l ..), handed to the lanes that need them by shuffles
+      uint4 cb = make_uint4(0u, 0u, 0u, 0u), cs = cb, co = cb;  // bias, scale or e_col, offset
+      {
+        const int nl = n0 + 8 * lane;
+        if (nl < a.N) {
+          if (bias) cb = *reinterpret_cast<const uint4 *>(bias + nl);
+          if constexpr (MODE == kRawQ) {
+            if (a.Ns != 1) {
+              cs = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.scale) + nl);
+              if (a.offset) co = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.offset) + nl);
+            }
+          } else {
+            cs = *reinterpret_cast<const uint4 *>(a.e_col + nl);
+          }
+        }
+      }
       // boxes of this tile inside the output: nch column boxes for each half
       // whose 32 rows of this warp start before M
       const int nch = (a.N - n0 + 31) / 32 < CPH ? (a.N - n0 + 31) / 32 : CPH;
       auto half_live = [&](int h) { return (long long)rb * TM + h * BM + 32 * qd < a.M; };
-      if (half_live(0)) load_residual(rc, n0, (long long)rb * TM + 32 * qd);  // first box
+      int nlive = 0;
+      while (nlive < MH && half_live(nlive)) ++nlive;
+      const int nbox = nlive * nch;  // this warp's boxes of the tile, half-major
+      const uint32_t rc0 = rc;
+      // box i of the tile: half i / nch, columns n0 + 32 (i % nch)
+      auto load_box = [&](int i) {
+        if (i < nbox)
+          load_residual(rc0 + (uint32_t)i, n0 + 32 * (i % nch),
+                        (long long)rb * TM + (i / nch) * BM + 32 * qd);
+      };
+      load_box(0);
+      load_box(1);
       if (!wait_bar_warp(BAR(ACCFULL(buf)), (uint32_t)((lt / NACC) & 1), abort_flag, a.status,
                          kWhereEpiAcc)) {
         ok = false;
@@ -642,8 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
 #pragma unroll 1
-      for (int h = 0; h < MH && ok; ++h) {
-        if (!half_live(h)) break;
+      for (int h = 0; h < nlive && ok; ++h) {
         const long long mrow0 = (long long)rb * TM + h * BM + 32 * qd;  // the warp's first row
         const long long m = mrow0 + lane;
         const bool row_ok = m < a.M;
@@ -661,25 +702,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll 1
         for (int c = 0; c < nch; ++c, ++rc) {
-          // the next box of this tile (next chunk, or the next half's first)
-          if (c + 1 < nch)
-            load_residual(rc + 1, n0 + 32 * (c + 1), mrow0);
-          else if (h + 1 < MH && half_live(h + 1))
-            load_residual(rc + 1, n0, mrow0 + BM);
+          load_box(h * nch + c + 2);  // two boxes ahead
           uint32_t r[32];
           tmem_ld32(taddr + 32 * c, r);
           tmem_wait_ld();
-          if (!wait_bar_warp(BAR(RESFULL(qd, (int)(rc & 1))), (rc >> 1) & 1u, abort_flag, a.status,
-                             kWhereEpiAcc)) {
+          if (!wait_bar_warp(BAR(RESFULL(qd, (int)(rc % NRES))), (rc / NRES) & 1u, abort_flag,
+                             a.status, kWhereEpiAcc)) {
             ok = false;
             break;
           }
-          const uint32_t rb_addr = rbox + (rc & 1) * L::EPI_BOX + row_off;
+          const uint32_t rb_addr = rbox + (rc % NRES) * L::EPI_BOX + row_off;
           uint32_t yo[16];
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             const int n = n0 + 32 * c + 8 * v;
-            // mm = the operator's x1 @ W for these 8 columns
+            // mm = the operator's x1 @ W for these 8 columns (held by lane g)
+            const int g = 4 * c + v;
+            auto bcast = [&](uint4 q, uint32_t (&w)[4]) {
+              w[0] = __shfl_sync(0xffffffffu, q.x, g);
+              w[1] = __shfl_sync(0xffffffffu, q.y, g);
+              w[2] = __shfl_sync(0xffffffffu, q.z, g);
+              w[3] = __shfl_sync(0xffffffffu, q.w, g);
+            };
+            uint32_t bw[4], cw[4];
+            bcast(cb, bw);
+            bcast(cs, cw);
             float mmv[8];
             if (n < a.N) {
               if constexpr (MODE == kRawQ) {
@@ -692,12 +739,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ow[0] = ow[1] = ow[2] = ow[3] = ob | (ob << 16);
                   }
                 } else {
-                  const uint4 sv = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.scale) + n);
-                  sw[0] = sv.x; sw[1] = sv.y; sw[2] = sv.z; sw[3] = sv.w;
-                  if (a.offset) {
-                    const uint4 ov = *reinterpret_cast<const uint4 *>(static_cast<const T *>(a.offset) + n);
-                    ow[0] = ov.x; ow[1] = ov.y; ow[2] = ov.z; ow[3] = ov.w;
-                  }
+                  sw[0] = cw[0]; sw[1] = cw[1]; sw[2] = cw[2]; sw[3] = cw[3];
+                  if (a.offset) bcast(co, ow);
                 }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -707,22 +750,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                   mmv[2 * i + 1] = fmaf(s2.y, __uint_as_float(r[8 * v + 2 * i + 1]), o2.y * rs);
                 }
               } else {
-                const uint4 ev = *reinterpret_cast<const uint4 *>(a.e_col + n);
-                const uint32_t ew[4] = {ev.x, ev.y, ev.z, ev.w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                  const int en = (int)(int16_t)((ew[i >> 1] >> (16 * (i & 1))) & 0xFFFFu);
+                  const int en = (int)(int16_t)((cw[i >> 1] >> (16 * (i & 1))) & 0xFFFFu);
                   mmv[i] = scale_pow2(__uint_as_float(r[8 * v + i]), em + en);
                 }
               }
             } else {
 #pragma unroll
               for (int i = 0; i < 8; ++i) mmv[i] = 0.f;
-            }
-            uint32_t bw[4] = {0u, 0u, 0u, 0u};
-            if (bias && n < a.N) {
-              const uint4 bb = *reinterpret_cast<const uint4 *>(bias + n);
-              bw[0] = bb.x; bw[1] = bb.y; bw[2] = bb.z; bw[3] = bb.w;
             }
             uint32_t rw[4];
             asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
@@ -742,18 +778,26 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int i = 0; i < 8; ++i) ss = fmaf(yv[i], yv[i], ss);
             }
           }
-          // the previous y box has been read by its store: overwrite and store it
-          if (lane == 0) bulk_wait_group_read<0>();
+          // the y box: every lane has read the previous one; write this thread's
+          // row, then store whole box rows (lanes 4i..4i+3 cover row 8u + i)
           __syncwarp();
 #pragma unroll
           for (int v = 0; v < 4; ++v)
             st_shared_v4(ybox + row_off + ((((uint32_t)v) ^ swz) << 4), yo[4 * v], yo[4 * v + 1],
                          yo[4 * v + 2], yo[4 * v + 3]);
-          fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tm_yo, ybox, n0 + 32 * c, (int)mrow0);
-            bulk_commit_group();
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int rr = 8 * u + (lane >> 2), j = lane & 3;
+            const long long my = mrow0 + rr;
+            const int ny = n0 + 32 * c + 8 * j;
+            uint32_t q0, q1, q2, q3;
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(q0), "=r"(q1), "=r"(q2), "=r"(q3)
+                         : "r"(ybox + (uint32_t)rr * 64u +
+                               ((((uint32_t)j) ^ (((uint32_t)rr >> 1) & 3u)) << 4)));
+            if (my < a.M && ny < a.N)
+              *reinterpret_cast<uint4 *>(yst + my * a.N + ny) = make_uint4(q0, q1, q2, q3);
           }
         }
         if (row_ok && ok) a.rowpart[m * a.nTilesN + nt] = ss;
@@ -773,12 +817,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       prefetch_residual(t + gridDim.x);
       if (prev_t >= 0) {
-        // the previous tile's y boxes have landed in global memory
-        if (lane == 0) {
-          bulk_wait_group_all();
-          fence_proxy_async_global();
-        }
-        __syncwarp();
         if (!normalize(prev_t)) {
           ok = false;
           break;
@@ -788,9 +826,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) {
       // no copy of this warp may still be in flight when the CTA exits
-      for (uint32_t k = rc; k < issued; ++k) drain_bar(BAR(RESFULL(qd, (int)(k & 1))), (k >> 1) & 1u);
-      bulk_wait_group_all();
-      fence_proxy_async_global();
+      for (uint32_t k = rc; k < issued; ++k)
+        drain_bar(BAR(RESFULL(qd, (int)(k % NRES))), (k / NRES) & 1u);
     }
     __syncwarp();
     if (ok && prev_t >= 0) normalize(prev_t);
@@ -848,6 +885,7 @@ bool prefill_applicable(const Problem &p) {
     if (!aligned16(q)) return false;
   const int64_t nTilesN = (p.N + BN - 1) / BN;
   if (nTilesN > device_info().sms) return false;        // row-block waits need n-tiles <= CTAs
+  if (nTilesN > 32 * kPartsPerLane) return false;       // partial sums a normalising warp reads
   return true;
 }
 
@@ -1023,8 +1061,8 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
       if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
   }
-  // residual (read) and y (written) in 32 x 32 boxes of the epilogue
-  CUtensorMap tm_r, tm_yo;
+  // the residual, read in 32 x 32 boxes by the epilogue
+  CUtensorMap tm_r;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.M};
     const cuuint64_t strides[1] = {(cuuint64_t)p.N * 2};
@@ -1036,13 +1074,9 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    r = enc(&tm_yo, t, 2, p.y, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
   prefill_kernel<DT, WBITS, MODE, MH>
-      <<<plan.grid, kThreads, L::SMEM, s>>>(tm_x, tm_w, tm_s, tm_dx, tm_ox, tm_r, tm_yo, args);
+      <<<plan.grid, kThreads, L::SMEM, s>>>(tm_x, tm_w, tm_s, tm_dx, tm_ox, tm_r, args);
   return cudaGetLastError();
 }
 

@@ -272,38 +272,6 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uin
       : "memory");
 }
 
-// 2-D tiled store of the box at (x = inner coordinate, y) from shared memory,
-// as one operation of the thread's current bulk async-group. Parts of the box
-// past the tensor's extent are not written.
-__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   tmap),
-               "r"(src), "r"(x), "r"(y)
-               : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit_group() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Waits until the thread's bulk async-groups other than the N most recent
-// have finished reading their shared-memory sources.
-template <int N>
-__device__ __forceinline__ void bulk_wait_group_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-// Waits until all of the thread's bulk async-groups have completed (writes done).
-__device__ __forceinline__ void bulk_wait_group_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// Orders the async proxy's completed global writes before later generic-proxy
-// accesses of this thread (and, through a barrier, of others).
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 // Named barrier for a subset of the CTA's warps (id 1..15).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
