@@ -1034,7 +1034,9 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
     const int64_t ld = so_ld(p, plan);
     const cuuint64_t dims[2] = {(cuuint64_t)ld, (cuuint64_t)p.G};
     const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
-    const cuuint32_t rows = (cuuint32_t)(p.G < SO_ROWS ? p.G : SO_ROWS);
+    // group rows a 64-deep k-stage touches: one when groups are whole multiples of it
+    const cuuint32_t rows =
+        p.group % BK == 0 ? 1u : (cuuint32_t)(p.G < SO_ROWS ? p.G : SO_ROWS);
     const cuuint32_t box[2] = {BN, rows};
     const cuuint32_t estr[2] = {1, 1};
     args.so_bytes = rows * BN * 4;
