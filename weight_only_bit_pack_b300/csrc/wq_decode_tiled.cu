@@ -48,6 +48,7 @@ constexpr int TTHREADS = TW * 32;
 constexpr int TSL = 2;              // pairs a warp's run can touch
 constexpr uint32_t kTGbarOff = 128; // header: grid counters (arrive, depart)
 enum TWhere : uint32_t { kTWhereGrid = 15 };
+constexpr int kTParts = 5;          // per-CTA partial sums a lane reads: grid <= 160
 
 struct DTArgs {
   const void *x1;
@@ -438,8 +439,17 @@ __global__ void __launch_bounds__(TTHREADS, 1) decode_tiled_kernel(const DTArgs 
   // 1/RMS of row m: warp m sums the CTAs' partials (lane-strided, then a fixed
   // shuffle tree: the same order in every CTA and every run)
   if (warp < a.M && !s_abort) {
+    // all of the lane's loads first (the grid has at most 32 * kTParts CTAs),
+    // then the sum in CTA order
+    float pv[kTParts];
+#pragma unroll
+    for (int i = 0; i < kTParts; ++i) {
+      const int c = lane + 32 * i;
+      pv[i] = c < a.G ? __ldcg(a.ss + c * 16 + warp) : 0.f;
+    }
     float tot2 = 0.f;
-    for (int c = lane; c < a.G; c += 32) tot2 += __ldcg(a.ss + c * 16 + warp);
+#pragma unroll
+    for (int i = 0; i < kTParts; ++i) tot2 += pv[i];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) tot2 += __shfl_xor_sync(0xffffffffu, tot2, o);
     if (lane == 0) s_rstd[warp] = rsqrtf(tot2 / (float)a.N + a.eps);
@@ -466,7 +476,8 @@ __global__ void __launch_bounds__(TTHREADS, 1) decode_tiled_kernel(const DTArgs 
 // ------------------------------------------------------------------ host side
 
 int tiled_grid_size(const Problem &p) {
-  const int sms = device_info().sms > 0 ? device_info().sms : 148;
+  int sms = device_info().sms > 0 ? device_info().sms : 148;
+  if (sms > 32 * kTParts) sms = 32 * kTParts;  // the row sums' readers cover that many CTAs
   const int ncg = (int)(p.N / 16);
   return ncg < sms ? ncg : sms;
 }
