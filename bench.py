@@ -451,6 +451,68 @@ def time_dynamic_quant(wq, dev, stream, bits, steps, warmup, peaks, M=8192, K=81
     return out
 
 
+def _graph_time(stream, dev, fn, steps, warmup):
+    """Per-call device time (ms) of fn(i) replayed from a CUDA graph of `steps` calls."""
+    for i in range(warmup):
+        fn(i)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        for i in range(steps):
+            fn(i)
+    gr.replay()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    gr.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    del gr
+    return ev0.elapsed_time(ev1) / steps
+
+
+# fp32 FMA peak of the CUDA cores: 148 SMs x 128 lanes x 2 FLOP x 2.032 GHz (unit
+# counts and maximum SM clock of the part)
+FP32_FMA_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+
+
+def time_fp4(wq, dev, stream, steps, warmup, peaks):
+    """FP4 E2M1 pack of a float32 (8192, 28672) weight, and the mx block-scaled
+    matmul with in-place add on a gradient-accumulation shape: y (4096, 4096) +=
+    x1^T-stored (8192 tokens, 4096) @ x2 (8192, 4096), FP4 operands, E8M0 scales."""
+    out = []
+    g = torch.Generator(device=dev).manual_seed(7)
+    K, N = 8192, 28672
+    R = 2  # 2 x 940 MB of float32 input > 2x L2
+    ws = [torch.randn((K, N), generator=g, device=dev) * 3 for _ in range(R)]
+    os_ = [torch.empty((K, N // 2), dtype=torch.uint8, device=dev) for _ in range(R)]
+    ms = _graph_time(stream, dev, lambda i: wq.pack_fp4(ws[i % R], out=os_[i % R], stream=stream),
+                     steps, warmup)
+    nbytes = K * N * 4 + K * N // 2
+    out.append({"workload": f"pack_fp4_f32_K{K}_N{N}", "kernel": "pack_fp4", "ms_per_step": ms,
+                "GB/s": nbytes / (ms * 1e-3) / 1e9, "roofline_bound": "hbm",
+                "roofline_frac": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                "l2": f"rotating {R} inputs of {K * N * 4 / 1e6:.0f} MB"})
+    del ws, os_
+    M, KT, N2 = 4096, 8192, 4096
+    J = KT // 32
+    x1 = torch.randint(0, 256, (KT, M // 2), generator=g, device=dev, dtype=torch.uint8)
+    s1 = torch.randint(120, 134, (J, M), generator=g, device=dev, dtype=torch.uint8)
+    x2 = torch.randint(0, 256, (KT, N2 // 2), generator=g, device=dev, dtype=torch.uint8)
+    s2 = torch.randint(120, 134, (J, N2), generator=g, device=dev, dtype=torch.uint8)
+    y = torch.zeros((M, N2), dtype=torch.float32, device=dev)
+    ms = _graph_time(stream, dev, lambda i: wq.mx_matmul_add(x1, s1, x2, s2, y, x1_transposed=True,
+                                                             stream=stream), 3, 1)
+    tf = 2.0 * M * N2 * KT / (ms * 1e-3) / 1e12
+    out.append({"workload": f"mx_matmul_add_fp4_M{M}_K{KT}_N{N2}_x1T", "kernel": "mx_matmul_add",
+                "ms_per_step": ms, "TFLOP/s": tf, "roofline_bound": "alu",
+                "roofline_peak": FP32_FMA_TFLOPS, "roofline_frac": tf / FP32_FMA_TFLOPS})
+    del x1, s1, x2, s2, y
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return out
+
+
 EXTRA = (("decode", 2000), ("decode@tiled", 2000), ("sweep:1", 1000), ("sweep:1@tiled", 1000),
          ("sweep:16", 1000), ("sweep:16@tiled", 1000), ("w8a16", 50), ("prefill", 20))
 
@@ -717,6 +779,7 @@ def run_ours(args, world, rank, local):
             extras.append(time_extra(wq, cfg, dev, stream, n, W, peaks))
         for bits in (8, 4):
             extras.append(time_dynamic_quant(wq, dev, stream, bits, 50, W, peaks))
+        extras += time_fp4(wq, dev, stream, 20, W, peaks)
         line["workloads"] = extras
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -75,7 +75,10 @@ extern "C" {
  * WQ_FP4_E2M1 is a logical 4-bit float (sign bit 3, 2-bit exponent, 1-bit
  * mantissa: magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), stored two per byte along the
  * last dimension like WQ_INT4. WQ_E8M0 is one byte e per element, the power of
- * two 2^(e - 127), with e = 255 standing for NaN (the OCP MX encoding). */
+ * two 2^(e - 127), with e = 255 standing for NaN (the OCP MX encoding).
+ * WQ_FP4_E2M1_T is the same element type for an operand given transposed: like
+ * WQ_INT4_T the descriptor gives the stored shape, (K, M) for an x1 whose
+ * logical shape is (M, K), packed two per byte along M. */
 typedef enum wq_dtype {
     WQ_F16 = 1,
     WQ_BF16 = 2,
@@ -87,7 +90,8 @@ typedef enum wq_dtype {
     WQ_INT8_T = 8,
     WQ_INT4_T = 9,
     WQ_FP4_E2M1 = 10,
-    WQ_E8M0 = 11
+    WQ_E8M0 = 11,
+    WQ_FP4_E2M1_T = 12
 } wq_dtype;
 
 /* Tensor descriptor (the analogue of aclTensor): pointer, element type, rank
@@ -250,8 +254,12 @@ int32_t wq_matmul_add_rmsnorm_select_kernel(
  *     y[m,n] += sum_j (sum_{k in slice j} x1[m,k] * x2[k,n]) * scale1[m,j] * scale2[j,n]
  * over slices of gsK = 32 along K (kLoops = ceil(K/32), the last slice may be
  * short).
- *   x1      WQ_FP4_E2M1 (M, K), K even, packed along K (not transposed).
- *   scale1  WQ_E8M0 (M, ceil(K/32)).
+ *   x1      WQ_FP4_E2M1 (M, K), K even, packed along K; or WQ_FP4_E2M1_T,
+ *           stored (K, M) packed along M, M even (the page's transposeX1 =
+ *           true, the form its constraints list as supported).
+ *   scale1  WQ_E8M0 (M, ceil(K/32)); with a transposed x1, stored (ceil(K/32), M)
+ *           (the scales follow x1's storage order: a reading, the page's table
+ *           of scale shapes is not legible).
  *   x2      WQ_FP4_E2M1 (K, N), N even, packed along N.
  *   scale2  WQ_E8M0 (ceil(K/32), N).
  *   y       WQ_F32 (M, N), read and written (it must not overlap the inputs).

@@ -270,3 +270,16 @@ def test_mx_matmul_validation(B):
     # an empty product is valid and launches nothing
     ds = _mx(B, M=0)
     assert B.lib.wq_mx_matmul_add(*[ctypes.byref(d) for d in ds], None, 0, None) == 0
+
+
+def test_mx_matmul_transposed_x1_validation(B):
+    def ds(M=16, K=96, N=64, sM=None):
+        J = (K + 31) // 32
+        return [D(B, B.DType.FP4_E2M1_T, (K, M)), D(B, B.DType.E8M0, (J, sM if sM else M)),
+                D(B, B.DType.FP4_E2M1, (K, N)), D(B, B.DType.E8M0, (J, N)), D(B, B.DType.F32, (M, N))]
+    assert _mx_ws(B, ds()) == (0, 0)
+    assert _mx_ws(B, ds(M=15))[0] == 3            # packed along m: m even
+    bad = ds(); bad[1] = D(B, B.DType.E8M0, (16, 3))
+    assert _mx_ws(B, bad)[0] == 3                 # scale1 follows x1's storage: (J, m)
+    bad = ds(); bad[2] = D(B, B.DType.FP4_E2M1_T, (64, 96))
+    assert _mx_ws(B, bad)[0] == 2                 # x2 is never the transposed form

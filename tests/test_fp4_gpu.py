@@ -148,3 +148,26 @@ def test_mx_matmul_add_accumulates_in_place(wq):
         wq.mx_matmul_add(x1.cuda(), s1.cuda(), x2.cuda(), s2.cuda(), yd)
     torch.cuda.synchronize()
     assert np.array_equal(yd.cpu().numpy().view(np.uint32), want.astype(np.float32).view(np.uint32))
+
+
+def _codes_transposed(x1):
+    """(M, K/2) codes packed along K -> the same codes of x1^T, (K, M/2) packed along M."""
+    b = x1.to(torch.int32)
+    codes = torch.stack([b & 15, b >> 4], dim=2).reshape(x1.shape[0], -1)  # (M, K)
+    t = codes.t().contiguous()                                             # (K, M)
+    return (t[:, 0::2] | (t[:, 1::2] << 4)).to(torch.uint8)
+
+
+@pytest.mark.parametrize("M,K,N", [(2, 32, 2), (8, 70, 10), (64, 256, 130), (18, 96, 64)])
+def test_mx_matmul_add_transposed_x1(wq, M, K, N):
+    # the page's supported form: x1 given as (K, M) in memory, scale1 as (ceil(K/32), M)
+    x1, s1, x2, s2, y = _mx_case(M, K, N, seed=77 + M + K)
+    with np.errstate(over="ignore"):
+        want = oracle.mx_matmul_add(x1, s1, x2, s2, y.double(), K).astype(np.float32)
+    x1t = _codes_transposed(x1)
+    assert x1t.shape == (K, M // 2)
+    yd = y.cuda().contiguous()
+    wq.mx_matmul_add(x1t.cuda(), s1.t().contiguous().cuda(), x2.cuda(), s2.cuda(), yd,
+                     x1_transposed=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(yd.cpu().numpy().view(np.uint32), want.view(np.uint32))

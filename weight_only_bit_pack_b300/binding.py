@@ -60,6 +60,7 @@ class DType(enum.IntEnum):
     INT4_T = 9
     FP4_E2M1 = 10
     E8M0 = 11
+    FP4_E2M1_T = 12
 
 
 class WQError(RuntimeError):
@@ -302,12 +303,19 @@ def pack_fp4(weight: torch.Tensor, out: Optional[torch.Tensor] = None, stream=No
 
 
 def mx_matmul_add(x1: torch.Tensor, scale1: torch.Tensor, x2: torch.Tensor, scale2: torch.Tensor,
-                  y: torch.Tensor, stream=None) -> torch.Tensor:
+                  y: torch.Tensor, x1_transposed: bool = False, stream=None) -> torch.Tensor:
     """``y += mx(x1, scale1) @ mx(x2, scale2)`` (``wq_mx_matmul_add``): x1 (M, K/2) and
     x2 (K, N/2) uint8 FP4 E2M1 codes, scale1 (M, ceil(K/32)) and scale2 (ceil(K/32), N)
-    uint8 E8M0 exponents, y float32 (M, N) updated in place and returned."""
-    M, K, N = x1.shape[0], x1.shape[1] * 2, x2.shape[1] * 2
-    d = [describe(x1, DType.FP4_E2M1, (M, K)), describe(scale1, DType.E8M0),
+    uint8 E8M0 exponents, y float32 (M, N) updated in place and returned. With
+    ``x1_transposed`` x1 is (K, M/2) (packed along M) and scale1 (ceil(K/32), M)."""
+    N = x2.shape[1] * 2
+    if x1_transposed:
+        K, M = x1.shape[0], x1.shape[1] * 2
+        dx1 = describe(x1, DType.FP4_E2M1_T, (K, M))
+    else:
+        M, K = x1.shape[0], x1.shape[1] * 2
+        dx1 = describe(x1, DType.FP4_E2M1, (M, K))
+    d = [dx1, describe(scale1, DType.E8M0),
          describe(x2, DType.FP4_E2M1, (K, N)), describe(scale2, DType.E8M0), describe(y)]
     ws = ctypes.c_uint64(0)
     _check(lib.wq_mx_matmul_add_get_workspace(*[_ref(v) for v in d], ctypes.byref(ws)))

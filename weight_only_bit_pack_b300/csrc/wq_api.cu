@@ -56,7 +56,8 @@ int64_t elem_bits(int dt) {
   switch (dt) {
     case WQ_F16: case WQ_BF16: return 16;
     case WQ_INT8: case WQ_INT8_T: case WQ_E8M0: return 8;
-    case WQ_INT4: case WQ_INT4_TILED: case WQ_INT4_T: case WQ_FP4_E2M1: return 4;
+    case WQ_INT4: case WQ_INT4_TILED: case WQ_INT4_T: case WQ_FP4_E2M1: case WQ_FP4_E2M1_T:
+      return 4;
     case WQ_INT32: case WQ_F32: return 32;
     default: return 0;
   }
@@ -96,7 +97,8 @@ const char *dtname(int dt) {
     case WQ_INT4: return "INT4"; case WQ_INT32: return "INT32";
     case WQ_INT4_TILED: return "INT4_TILED"; case WQ_F32: return "F32";
     case WQ_INT8_T: return "INT8_T"; case WQ_INT4_T: return "INT4_T";
-    case WQ_FP4_E2M1: return "FP4_E2M1"; case WQ_E8M0: return "E8M0"; default: return "?";
+    case WQ_FP4_E2M1: return "FP4_E2M1"; case WQ_E8M0: return "E8M0";
+    case WQ_FP4_E2M1_T: return "FP4_E2M1_T"; default: return "?";
   }
 }
 
@@ -500,21 +502,26 @@ static int32_t validate_mx(const wq_tensor *x1, const wq_tensor *s1, const wq_te
   const wq_tensor *all[] = {x1, s1, x2, s2, y};
   for (const wq_tensor *t : all)
     if (!valid_rank(t) || t->ndim != 2) return fail(WQ_ERR_SHAPE, "every operand is 2-D");
-  if (x1->dtype != WQ_FP4_E2M1 || x2->dtype != WQ_FP4_E2M1)
-    return fail(WQ_ERR_DTYPE, "x1 and x2 must be FP4_E2M1");
+  if ((x1->dtype != WQ_FP4_E2M1 && x1->dtype != WQ_FP4_E2M1_T) || x2->dtype != WQ_FP4_E2M1)
+    return fail(WQ_ERR_DTYPE, "x1 must be FP4_E2M1 or FP4_E2M1_T and x2 FP4_E2M1");
   if (s1->dtype != WQ_E8M0 || s2->dtype != WQ_E8M0)
     return fail(WQ_ERR_DTYPE, "scale1 and scale2 must be E8M0");
   if (y->dtype != WQ_F32) return fail(WQ_ERR_DTYPE, "y must be F32");
-  M = x1->shape[0];
-  K = x1->shape[1];
+  const bool x1t = x1->dtype == WQ_FP4_E2M1_T;
+  M = x1t ? x1->shape[1] : x1->shape[0];
+  K = x1t ? x1->shape[0] : x1->shape[1];
   N = x2->shape[1];
   if (K < 1 || K > kMaxKN || N > kMaxKN || M > kMaxRows)
     return fail(WQ_ERR_SHAPE, "k must lie in [1, 65535], n in [0, 65535]");
   if (K % 2 || N % 2) return fail(WQ_ERR_SHAPE, "k and n must be even (two FP4 codes per byte)");
+  if (x1t && M % 2) return fail(WQ_ERR_SHAPE, "a transposed x1 packs along m: m must be even");
   if (x2->shape[0] != K) return fail(WQ_ERR_SHAPE, "x2 must be (k, n) with x1's k");
   const int64_t J = (K + 31) / 32;
-  if (s1->shape[0] != M || s1->shape[1] != J)
+  if (!x1t && (s1->shape[0] != M || s1->shape[1] != J))
     return fail(WQ_ERR_SHAPE, "scale1 must be (m, ceil(k/32) = %lld)", (long long)J);
+  if (x1t && (s1->shape[0] != J || s1->shape[1] != M))
+    return fail(WQ_ERR_SHAPE, "with a transposed x1, scale1 must be (ceil(k/32) = %lld, m)",
+                (long long)J);
   if (s2->shape[0] != J || s2->shape[1] != N)
     return fail(WQ_ERR_SHAPE, "scale2 must be (ceil(k/32) = %lld, n)", (long long)J);
   if (y->shape[0] != M || y->shape[1] != N) return fail(WQ_ERR_SHAPE, "y must be (m, n)");
@@ -546,8 +553,9 @@ int32_t wq_mx_matmul_add(const wq_tensor *x1, const wq_tensor *s1, const wq_tens
   if (st) return st;
   if (M == 0 || N == 0) return ok();
   cudaError_t e = launch_mx_matmul_add((const uint8_t *)x1->data, (const uint8_t *)s1->data,
-                                       (const uint8_t *)x2->data, (const uint8_t *)s2->data,
-                                       (float *)y->data, M, K, N, (cudaStream_t)stream);
+                                       x1->dtype == WQ_FP4_E2M1_T, (const uint8_t *)x2->data,
+                                       (const uint8_t *)s2->data, (float *)y->data, M, K, N,
+                                       (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "mx matmul launch");
   return ok();
 }

@@ -8,7 +8,8 @@
 // HBM-bound: 4 bytes read and half a byte written per element.
 //
 // mx matmul (aclnnQuantBatchMatmulInplaceAdd, "Function description", mx
-// quantization): y[m,n] += sum_j (sum_{k in slice j} x1[m,k] x2[k,n]) *
+// quantization; x1 as given or transposed, (K, M) in memory, the form the
+// page's constraints list): y[m,n] += sum_j (sum_{k in slice j} x1[m,k] x2[k,n]) *
 // scale1[m,j] * scale2[j,n], slices of gsK = 32 along K (the last one may be
 // short), FP4 E2M1 operands and E8M0 scales (byte e = 2^(e - 127), 255 = NaN).
 // A CUDA-core kernel: one thread per output column n and 8 rows; a slice's sum
@@ -56,7 +57,9 @@ __device__ __forceinline__ float e2m1_value(uint32_t code) {
   return (code & 8u) ? -v : v;
 }
 
-// grid (ceil(N / 128), <= 65535 row blocks); thread = column n, 8 rows per block
+// grid (ceil(N / 128), <= 65535 row blocks); thread = column n, 8 rows per block.
+// X1T: x1 stored (K, M) packed along M, scale1 stored (J, M).
+template <bool X1T>
 __global__ void __launch_bounds__(kMxThreads)
     mx_matmul_add_kernel(const uint8_t *__restrict__ x1, const uint8_t *__restrict__ s1,
                          const uint8_t *__restrict__ x2, const uint8_t *__restrict__ s2,
@@ -76,13 +79,21 @@ __global__ void __launch_bounds__(kMxThreads)
         const int r = i / kGs, kk = i % kGs;
         float v = 0.f;
         if (m0 + r < M && kk < klen) {
-          const int64_t k = k0 + kk;
-          const uint32_t b = x1[(m0 + r) * (K / 2) + k / 2];
-          v = e2m1_value((k & 1) ? (b >> 4) : (b & 15u));
+          const int64_t k = k0 + kk, m = m0 + r;
+          if constexpr (X1T) {
+            const uint32_t b = x1[k * (M / 2) + m / 2];
+            v = e2m1_value((m & 1) ? (b >> 4) : (b & 15u));
+          } else {
+            const uint32_t b = x1[m * (K / 2) + k / 2];
+            v = e2m1_value((k & 1) ? (b >> 4) : (b & 15u));
+          }
         }
         xs[r][kk] = v;
       }
-      if (threadIdx.x < kMxRows) ss[threadIdx.x] = m0 + threadIdx.x < M ? s1[(m0 + threadIdx.x) * J + j] : 127;
+      if (threadIdx.x < kMxRows) {
+        const int64_t m = m0 + threadIdx.x;
+        ss[threadIdx.x] = m < M ? (X1T ? s1[j * M + m] : s1[m * J + j]) : 127;
+      }
       __syncthreads();
       if (n >= N) continue;
       float slice[kMxRows];
@@ -128,13 +139,16 @@ cudaError_t launch_pack_fp4(const float *in, uint8_t *out, int64_t K, int64_t N,
   return cudaGetLastError();
 }
 
-cudaError_t launch_mx_matmul_add(const uint8_t *x1, const uint8_t *s1, const uint8_t *x2,
+cudaError_t launch_mx_matmul_add(const uint8_t *x1, const uint8_t *s1, bool x1t, const uint8_t *x2,
                                  const uint8_t *s2, float *y, int64_t M, int64_t K, int64_t N,
                                  cudaStream_t s) {
   int64_t rows = (M + kMxRows - 1) / kMxRows;
   if (rows > 65535) rows = 65535;
   const dim3 grid((unsigned)((N + kMxThreads - 1) / kMxThreads), (unsigned)rows, 1);
-  mx_matmul_add_kernel<<<grid, kMxThreads, 0, s>>>(x1, s1, x2, s2, y, M, K, N);
+  if (x1t)
+    mx_matmul_add_kernel<true><<<grid, kMxThreads, 0, s>>>(x1, s1, x2, s2, y, M, K, N);
+  else
+    mx_matmul_add_kernel<false><<<grid, kMxThreads, 0, s>>>(x1, s1, x2, s2, y, M, K, N);
   return cudaGetLastError();
 }
 
