@@ -502,9 +502,15 @@ def time_fp4(wq, dev, stream, steps, warmup, peaks):
     s2 = torch.randint(120, 134, (J, N2), generator=g, device=dev, dtype=torch.uint8)
     y = torch.zeros((M, N2), dtype=torch.float32, device=dev)
     ms = _graph_time(stream, dev, lambda i: wq.mx_matmul_add(x1, s1, x2, s2, y, x1_transposed=True,
-                                                             stream=stream), 3, 1)
+                                                             stream=stream), 10, 2)
     tf = 2.0 * M * N2 * KT / (ms * 1e-3) / 1e12
-    out.append({"workload": f"mx_matmul_add_fp4_M{M}_K{KT}_N{N2}_x1T", "kernel": "mx_matmul_add",
+    out.append({"workload": f"mx_matmul_add_fp4_M{M}_K{KT}_N{N2}_x1T", "kernel": "mx_matmul_add (tensor cores)",
+                "ms_per_step": ms, "TFLOP/s": tf, "roofline_bound": "tensor",
+                "roofline_peak": peaks["bf16_tflops"], "roofline_frac": tf / peaks["bf16_tflops"]})
+    ms = _graph_time(stream, dev, lambda i: wq.mx_matmul_add(x1, s1, x2, s2, y, x1_transposed=True,
+                                                             kernel="exact", stream=stream), 2, 1)
+    tf = 2.0 * M * N2 * KT / (ms * 1e-3) / 1e12
+    out.append({"workload": f"mx_matmul_add_fp4_M{M}_K{KT}_N{N2}_x1T", "kernel": "mx_matmul_add (exact, CUDA cores)",
                 "ms_per_step": ms, "TFLOP/s": tf, "roofline_bound": "alu",
                 "roofline_peak": FP32_FMA_TFLOPS, "roofline_frac": tf / FP32_FMA_TFLOPS})
     del x1, s1, x2, s2, y

@@ -264,17 +264,30 @@ int32_t wq_matmul_add_rmsnorm_select_kernel(
  *   scale2  WQ_E8M0 (ceil(K/32), N).
  *   y       WQ_F32 (M, N), read and written (it must not overlap the inputs).
  *   ws_bytes out: 0.
- * Each slice's sum of products is exact in fp32, the scaled slices are added in
- * fp64 and the sum is added to y and rounded once to fp32. Errors: WQ_ERR_NULL,
- * WQ_ERR_DTYPE, WQ_ERR_SHAPE, WQ_ERR_ALIAS. Touches no device memory. */
+ * Each slice's sum of products is exact (a multiple of 1/4 below 2^11). With
+ * the default kernel (tensor cores, WQ_MX_KERNEL_TENSOR) the scaled slices are
+ * added in fp32, one rounding per slice: |error| <= (kLoops + 3) * 2^-24 *
+ * (|y| + sum_j |slice_j * scale1 * scale2|) plus subnormal rounding. With
+ * WQ_MX_KERNEL_EXACT (CUDA cores) they are added in fp64 and the sum is added
+ * to y and rounded once to fp32: the exactly rounded result unless the fp64
+ * sum itself rounds. Errors: WQ_ERR_NULL, WQ_ERR_DTYPE, WQ_ERR_SHAPE,
+ * WQ_ERR_ALIAS. Touches no device memory. */
 int32_t wq_mx_matmul_add_get_workspace(const wq_tensor *x1, const wq_tensor *scale1,
                                        const wq_tensor *x2, const wq_tensor *scale2,
                                        const wq_tensor *y, uint64_t *ws_bytes);
 
-/* Second phase: enqueue the product on `stream` (a CUDA-core kernel). */
+/* Second phase: enqueue the product on `stream` (the tensor-core kernel). */
 int32_t wq_mx_matmul_add(const wq_tensor *x1, const wq_tensor *scale1, const wq_tensor *x2,
                          const wq_tensor *scale2, const wq_tensor *y, void *ws, uint64_t ws_bytes,
                          void *stream);
+
+enum { WQ_MX_KERNEL_TENSOR = 0, WQ_MX_KERNEL_EXACT = 1 };
+
+/* The same with a choice of kernel (WQ_MX_KERNEL_*; anything else is
+ * WQ_ERR_UNSUPPORTED). */
+int32_t wq_mx_matmul_add_ex(const wq_tensor *x1, const wq_tensor *scale1, const wq_tensor *x2,
+                            const wq_tensor *scale2, const wq_tensor *y, int32_t kernel, void *ws,
+                            uint64_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------ dynamic quantization */
 

@@ -283,3 +283,11 @@ def test_mx_matmul_transposed_x1_validation(B):
     assert _mx_ws(B, bad)[0] == 3                 # scale1 follows x1's storage: (J, m)
     bad = ds(); bad[2] = D(B, B.DType.FP4_E2M1_T, (64, 96))
     assert _mx_ws(B, bad)[0] == 2                 # x2 is never the transposed form
+
+
+def test_mx_kernel_selector(B):
+    ds = _mx(B, M=0)
+    r = [ctypes.byref(d) for d in ds]
+    assert B.lib.wq_mx_matmul_add_ex(*r, 0, None, 0, None) == 0
+    assert B.lib.wq_mx_matmul_add_ex(*r, 1, None, 0, None) == 0
+    assert B.lib.wq_mx_matmul_add_ex(*r, 7, None, 0, None) == 6

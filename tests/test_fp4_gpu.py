@@ -94,7 +94,7 @@ def _check_mx(wq, x1, s1, x2, s2, y):
     with np.errstate(over="ignore"):  # products beyond fp32 range round to inf on both sides
         want = oracle.mx_matmul_add(x1, s1, x2, s2, y.double(), K).astype(np.float32)
     yd = y.cuda().contiguous()
-    wq.mx_matmul_add(x1.cuda(), s1.cuda(), x2.cuda(), s2.cuda(), yd)
+    wq.mx_matmul_add(x1.cuda(), s1.cuda(), x2.cuda(), s2.cuda(), yd, kernel="exact")
     torch.cuda.synchronize()
     got = yd.cpu().numpy()
     assert np.array_equal(np.isnan(got), np.isnan(want))
@@ -124,7 +124,7 @@ def test_mx_matmul_add_large_sample(wq):
     M, K, N = 16, 4096, 4096
     x1, s1, x2, s2, y = _mx_case(M, K, N, seed=11)
     yd = y.cuda()
-    wq.mx_matmul_add(x1.cuda(), s1.cuda(), x2.cuda(), s2.cuda(), yd)
+    wq.mx_matmul_add(x1.cuda(), s1.cuda(), x2.cuda(), s2.cuda(), yd, kernel="exact")
     torch.cuda.synchronize()
     got = yd.cpu().numpy()
     g = np.random.default_rng(0)
@@ -145,7 +145,7 @@ def test_mx_matmul_add_accumulates_in_place(wq):
     want = oracle.mx_matmul_add(x1, s1, x2, s2, want.astype(np.float32).astype(np.float64), 64)
     yd = y.cuda()
     for _ in range(2):
-        wq.mx_matmul_add(x1.cuda(), s1.cuda(), x2.cuda(), s2.cuda(), yd)
+        wq.mx_matmul_add(x1.cuda(), s1.cuda(), x2.cuda(), s2.cuda(), yd, kernel="exact")
     torch.cuda.synchronize()
     assert np.array_equal(yd.cpu().numpy().view(np.uint32), want.astype(np.float32).view(np.uint32))
 
@@ -168,6 +168,81 @@ def test_mx_matmul_add_transposed_x1(wq, M, K, N):
     assert x1t.shape == (K, M // 2)
     yd = y.cuda().contiguous()
     wq.mx_matmul_add(x1t.cuda(), s1.t().contiguous().cuda(), x2.cuda(), s2.cuda(), yd,
-                     x1_transposed=True)
+                     x1_transposed=True, kernel="exact")
     torch.cuda.synchronize()
     assert np.array_equal(yd.cpu().numpy().view(np.uint32), want.view(np.uint32))
+
+
+# ---------------------------------------------------------------- tensor-core kernel
+
+def _abs_codes(x):
+    return (x & 0x77).to(torch.uint8)  # both nibbles' sign bits cleared
+
+
+def _check_tc(wq, x1, s1, x2, s2, y, x1_transposed=False):
+    K = x1.shape[1] * 2
+    J = (K + 31) // 32
+    with np.errstate(over="ignore", invalid="ignore"):
+        want = oracle.mx_matmul_add(x1, s1, x2, s2, y.double(), K)
+        mag = oracle.mx_matmul_add(_abs_codes(x1), s1, _abs_codes(x2), s2, y.double().abs(), K)
+    tol = (J + 3) * 2.0 ** -24 * mag + (J + 2) * 2.0 ** -149
+    yd = y.cuda().contiguous()
+    if x1_transposed:
+        wq.mx_matmul_add(_codes_transposed(x1).cuda(), s1.t().contiguous().cuda(), x2.cuda(), s2.cuda(),
+                         yd, x1_transposed=True)
+    else:
+        wq.mx_matmul_add(x1.cuda(), s1.cuda(), x2.cuda(), s2.cuda(), yd)
+    torch.cuda.synchronize()
+    got = yd.cpu().numpy().astype(np.float64)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    ok = ~nan
+    err = np.abs(got[ok] - want[ok])
+    assert np.all(err <= tol[ok]), (err - tol[ok]).max()
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 32, 2), (3, 70, 10), (128, 128, 128), (130, 256, 258),
+                                   (256, 1024, 384), (9, 2, 4), (5, 34, 258), (200, 96, 136)])
+def test_mx_tensor_kernel_within_bound(wq, M, K, N):
+    _check_tc(wq, *_mx_case(M, K, N, seed=5000 + M * 7 + K + N))
+
+
+@pytest.mark.parametrize("M,K,N", [(2, 32, 2), (130, 70, 10), (128, 256, 130), (256, 512, 256)])
+def test_mx_tensor_kernel_transposed_x1(wq, M, K, N):
+    _check_tc(wq, *_mx_case(M, K, N, seed=6000 + M + K + N), x1_transposed=True)
+
+
+def test_mx_tensor_kernel_wide_exponents(wq):
+    # scales from 2^-127 to 2^53 on each side: products from 2^-254 to 2^106, no fp32 overflow
+    x1, s1, x2, s2, y = _mx_case(160, 256, 136, seed=8, lo=0, hi=181)
+    _check_tc(wq, x1, s1, x2, s2, y)
+
+
+def test_mx_tensor_kernel_large_row_exponents(wq):
+    # row scales 2^118 .. 2^127 with column scales 2^-127 .. 2^-108: the slices
+    # take the two-step path (a row exponent alone could overflow acc * 2^e1)
+    x1, s1, x2, s2, y = _mx_case(64, 128, 64, seed=9, lo=245, hi=255)
+    s2[:] = torch.randint(0, 20, s2.shape, generator=torch.Generator().manual_seed(10), dtype=torch.uint8)
+    _check_tc(wq, x1, s1, x2, s2, y)
+
+
+def test_mx_tensor_kernel_nan_scale(wq):
+    _check_tc(wq, *_mx_case(140, 96, 130, seed=11, nan_at=(133, 2)))
+
+
+def test_mx_tensor_kernel_sampled_large(wq):
+    # the bench's gradient-accumulation shape, x1 transposed, rows sampled
+    M, K, N = 4096, 8192, 4096
+    x1, s1, x2, s2, y = _mx_case(M, K, N, seed=12, lo=120, hi=134)
+    yd = y.cuda()
+    wq.mx_matmul_add(_codes_transposed(x1).cuda(), s1.t().contiguous().cuda(), x2.cuda(), s2.cuda(), yd,
+                     x1_transposed=True)
+    torch.cuda.synchronize()
+    got = yd.cpu().numpy().astype(np.float64)
+    J = K // 32
+    for m in (0, 1, 127, 128, 2049, 4095):
+        want = oracle.mx_matmul_add(x1[m:m + 1], s1[m:m + 1], x2, s2, y[m:m + 1].double(), K)
+        mag = oracle.mx_matmul_add(_abs_codes(x1[m:m + 1]), s1[m:m + 1], _abs_codes(x2), s2,
+                                   y[m:m + 1].double().abs(), K)
+        tol = (J + 3) * 2.0 ** -24 * mag
+        assert np.all(np.abs(got[m:m + 1] - want) <= tol), m

@@ -115,6 +115,8 @@ lib.wq_pack_int4.argtypes = [_P, _P, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_
 lib.wq_convert_int4_layout.argtypes = [_P, _P, ctypes.c_void_p]
 lib.wq_mx_matmul_add_get_workspace.argtypes = [_P, _P, _P, _P, _P, ctypes.POINTER(ctypes.c_uint64)]
 lib.wq_mx_matmul_add.argtypes = [_P, _P, _P, _P, _P, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
+lib.wq_mx_matmul_add_ex.argtypes = [_P, _P, _P, _P, _P, ctypes.c_int32, ctypes.c_void_p, ctypes.c_uint64,
+                                    ctypes.c_void_p]
 lib.wq_dynamic_quant_get_workspace.argtypes = [_P, _P, _P, _P, ctypes.POINTER(ctypes.c_uint64)]
 lib.wq_dynamic_quant.argtypes = [_P, _P, _P, _P, ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
 lib.wq_matmul_add_rmsnorm_get_workspace.argtypes = _T + [ctypes.POINTER(ctypes.c_uint64)]
@@ -141,7 +143,7 @@ for _f in ("wq_pack_int4_get_workspace", "wq_pack_int4", "wq_matmul_add_rmsnorm_
            "wq_read_device_status", "wq_version", "wq_matmul_add_rmsnorm_noalloc",
            "wq_check_device_timeout", "wq_noalloc_read_device_status", "wq_test_set_wait_limits",
            "wq_convert_int4_layout", "wq_dynamic_quant_get_workspace", "wq_dynamic_quant",
-           "wq_mx_matmul_add_get_workspace", "wq_mx_matmul_add"):
+           "wq_mx_matmul_add_get_workspace", "wq_mx_matmul_add", "wq_mx_matmul_add_ex"):
     getattr(lib, _f).restype = ctypes.c_int32
 
 _TORCH2WQ = {torch.float16: DType.F16, torch.bfloat16: DType.BF16, torch.int8: DType.INT8,
@@ -303,11 +305,14 @@ def pack_fp4(weight: torch.Tensor, out: Optional[torch.Tensor] = None, stream=No
 
 
 def mx_matmul_add(x1: torch.Tensor, scale1: torch.Tensor, x2: torch.Tensor, scale2: torch.Tensor,
-                  y: torch.Tensor, x1_transposed: bool = False, stream=None) -> torch.Tensor:
+                  y: torch.Tensor, x1_transposed: bool = False, kernel: str = "tensor",
+                  stream=None) -> torch.Tensor:
     """``y += mx(x1, scale1) @ mx(x2, scale2)`` (``wq_mx_matmul_add``): x1 (M, K/2) and
     x2 (K, N/2) uint8 FP4 E2M1 codes, scale1 (M, ceil(K/32)) and scale2 (ceil(K/32), N)
     uint8 E8M0 exponents, y float32 (M, N) updated in place and returned. With
-    ``x1_transposed`` x1 is (K, M/2) (packed along M) and scale1 (ceil(K/32), M)."""
+    ``x1_transposed`` x1 is (K, M/2) (packed along M) and scale1 (ceil(K/32), M).
+    ``kernel``: "tensor" (slices on the tensor cores, fp32 sum) or "exact" (fp64 sum)."""
+    kid = {"tensor": 0, "exact": 1}[kernel]
     N = x2.shape[1] * 2
     if x1_transposed:
         K, M = x1.shape[0], x1.shape[1] * 2
@@ -319,7 +324,7 @@ def mx_matmul_add(x1: torch.Tensor, scale1: torch.Tensor, x2: torch.Tensor, scal
          describe(x2, DType.FP4_E2M1, (K, N)), describe(scale2, DType.E8M0), describe(y)]
     ws = ctypes.c_uint64(0)
     _check(lib.wq_mx_matmul_add_get_workspace(*[_ref(v) for v in d], ctypes.byref(ws)))
-    _check(lib.wq_mx_matmul_add(*[_ref(v) for v in d], None, 0, _stream(stream)))
+    _check(lib.wq_mx_matmul_add_ex(*[_ref(v) for v in d], kid, None, 0, _stream(stream)))
     return y
 
 

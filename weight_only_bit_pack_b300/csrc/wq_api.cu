@@ -544,20 +544,32 @@ int32_t wq_mx_matmul_add_get_workspace(const wq_tensor *x1, const wq_tensor *s1,
   return ok();
 }
 
-int32_t wq_mx_matmul_add(const wq_tensor *x1, const wq_tensor *s1, const wq_tensor *x2,
-                         const wq_tensor *s2, const wq_tensor *y, void *ws, uint64_t ws_bytes,
-                         void *stream) {
+int32_t wq_mx_matmul_add_ex(const wq_tensor *x1, const wq_tensor *s1, const wq_tensor *x2,
+                            const wq_tensor *s2, const wq_tensor *y, int32_t kernel, void *ws,
+                            uint64_t ws_bytes, void *stream) {
   (void)ws; (void)ws_bytes;
+  if (kernel != WQ_MX_KERNEL_TENSOR && kernel != WQ_MX_KERNEL_EXACT)
+    return fail(WQ_ERR_UNSUPPORTED, "unknown mx kernel %d", (int)kernel);
   int64_t M, K, N;
   int32_t st = validate_mx(x1, s1, x2, s2, y, M, K, N);
   if (st) return st;
   if (M == 0 || N == 0) return ok();
-  cudaError_t e = launch_mx_matmul_add((const uint8_t *)x1->data, (const uint8_t *)s1->data,
-                                       x1->dtype == WQ_FP4_E2M1_T, (const uint8_t *)x2->data,
-                                       (const uint8_t *)s2->data, (float *)y->data, M, K, N,
-                                       (cudaStream_t)stream);
+  const bool x1t = x1->dtype == WQ_FP4_E2M1_T;
+  const uint8_t *a = (const uint8_t *)x1->data, *sa = (const uint8_t *)s1->data;
+  const uint8_t *b = (const uint8_t *)x2->data, *sb = (const uint8_t *)s2->data;
+  cudaError_t e = kernel == WQ_MX_KERNEL_EXACT
+                      ? launch_mx_matmul_add(a, sa, x1t, b, sb, (float *)y->data, M, K, N,
+                                             (cudaStream_t)stream)
+                      : launch_mx_matmul_add_tc(a, sa, x1t, b, sb, (float *)y->data, M, K, N,
+                                                (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "mx matmul launch");
   return ok();
+}
+
+int32_t wq_mx_matmul_add(const wq_tensor *x1, const wq_tensor *s1, const wq_tensor *x2,
+                         const wq_tensor *s2, const wq_tensor *y, void *ws, uint64_t ws_bytes,
+                         void *stream) {
+  return wq_mx_matmul_add_ex(x1, s1, x2, s2, y, WQ_MX_KERNEL_TENSOR, ws, ws_bytes, stream);
 }
 
 // ------------------------------------------------------------------ dynamic quantization

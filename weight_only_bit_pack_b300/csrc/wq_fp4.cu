@@ -18,9 +18,15 @@
 // once to fp32 when it is added to y.
 #include "wq_common.cuh"
 #include "wq_internal.h"
+#include "wq_sm100.cuh"
 
 namespace wq {
 namespace {
+
+using sm100::ldmatrix_x4;
+using sm100::ldmatrix_x4_trans;
+using sm100::mma_16816;
+using sm100::smem_u32;
 
 __device__ __forceinline__ uint32_t e2m1x2(float even, float odd) {
   uint16_t r;
@@ -124,6 +130,220 @@ __global__ void __launch_bounds__(kMxThreads)
   }
 }
 
+// ---------------------------------------------------------------- tensor-core form
+//
+// The same product with the slice sums on the tensor cores: E2M1 codes become
+// fp16 exactly (cvt.rn.f16x2.e2m1x2), each 32-deep slice is two m16n8k16 MMAs
+// with fp32 accumulation -- exact, as the slice sum of E2M1 products is a
+// multiple of 1/4 below 2^11 -- and the slice is then scaled and added to the
+// running fp32 sum: tot = fma(acc * 2^(e1 - 127), 2^(e2 - 127), tot). The
+// first product is exact (acc has <= 13 significant bits above 2^-2, and
+// 2^-127 is an fp32 subnormal, so acc * 2^-127 is a multiple of 2^-129); a row
+// exponent above 117 could overflow it, so a slice whose scales reach 245
+// takes a two-step path on the combined exponent instead. One rounding per
+// slice (the add), against the exact kernel's fp64 sum.
+//
+// CTA tile 128 x 128 outputs, 8 warps as 2 (M) x 4 (N), warp tile 64 x 32
+// (4 x 4 MMA tiles); a slice's codes are fetched into registers one slice
+// ahead, decoded and stored into the other of two shared buffers: x2 and a
+// transposed x1 as [k][128 + 8 pad] fp16 rows (ldmatrix.trans gives the
+// fragments), an x1 given as (M, K) as [m][32 + 8 pad] rows (plain ldmatrix).
+
+constexpr int kTcThreads = 256, kTcT = 128;
+constexpr int kRowH = kTcT + 8;   // halves per [k][*] row (272 bytes: conflict-free ldmatrix)
+constexpr int kRowA = kGs + 8;    // halves per [m][k] row (80 bytes)
+
+// two fp16 values of the E2M1 codes in bits 3:0 (low half) and 7:4 (high half)
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(r) : "r"(byte));
+  return r;
+}
+
+// 2^(e - 127) for an E8M0 byte as an fp32 factor (e = 0 gives the subnormal
+// 2^-127, e = 255 NaN)
+__device__ __forceinline__ float e8m0_factor(uint32_t e) {
+  return e == 255u ? __int_as_float(0x7fc00000) : (e ? __int_as_float((int)(e << 23)) : __int_as_float(0x00400000));
+}
+
+// acc * 2^e for e in [-254, 254] in two exact power-of-two steps
+__device__ __forceinline__ float scale_two_step(float acc, int e) {
+  const int a = e < -126 ? -126 : (e > 127 ? 127 : e);
+  int b = e - a;
+  b = b < -126 ? -126 : (b > 127 ? 127 : b);
+  return acc * __int_as_float((a + 127) << 23) * __int_as_float((b + 127) << 23);
+}
+
+template <bool X1T>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    mx_mma_kernel(const uint8_t *__restrict__ x1, const uint8_t *__restrict__ s1,
+                  const uint8_t *__restrict__ x2, const uint8_t *__restrict__ s2,
+                  float *__restrict__ y, int64_t M, int64_t K, int64_t N) {
+  constexpr int A_HALVES = X1T ? kGs * kRowH : kTcT * kRowA;
+  __shared__ __align__(16) __half as[2][A_HALVES];
+  __shared__ __align__(16) __half bs[2][kGs * kRowH];
+  __shared__ uint8_t es1[2][kTcT], es2[2][kTcT];
+  __shared__ int huge[2];  // a scale of this slice is 245..254
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int wm = warp & 1, wn = warp >> 1;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t m0 = (int64_t)blockIdx.y * kTcT, n0 = (int64_t)blockIdx.x * kTcT;
+  const int64_t J = (K + kGs - 1) / kGs;
+
+  // ---- one slice's global codes and scales in registers (8 + 8 bytes a thread)
+  uint32_t ra[8], rb[8], rs = 0;
+  auto fetch = [&](int64_t j) {
+    const int64_t k0 = j * kGs;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int q = i * kTcThreads + tid;
+      if constexpr (X1T) {  // (K, M/2): 32 k-rows x 64 bytes
+        const int64_t k = k0 + q / 64, b = m0 / 2 + q % 64;
+        ra[i] = (k < K && b < M / 2) ? x1[k * (M / 2) + b] : 0u;
+      } else {              // (M, K/2): 128 rows x 16 bytes
+        const int64_t m = m0 + q / 16, b = k0 / 2 + q % 16;
+        ra[i] = (m < M && b < K / 2) ? x1[m * (K / 2) + b] : 0u;
+      }
+      const int64_t k = k0 + q / 64, b = n0 / 2 + q % 64;
+      rb[i] = (k < K && b < N / 2) ? x2[k * (N / 2) + b] : 0u;
+    }
+    rs = 127u;
+    if (tid < kTcT) {
+      const int64_t m = m0 + tid;
+      if (m < M) rs = X1T ? s1[j * M + m] : s1[m * J + j];
+    } else {
+      const int64_t n = n0 + tid - kTcT;
+      if (n < N) rs = s2[j * N + n];
+    }
+  };
+  auto store = [&](int buf) {
+    uint32_t *aw = reinterpret_cast<uint32_t *>(as[buf]);
+    uint32_t *bw = reinterpret_cast<uint32_t *>(bs[buf]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int q = i * kTcThreads + tid;
+      if constexpr (X1T) aw[((q / 64) * kRowH) / 2 + q % 64] = e2m1x2_to_f16x2(ra[i]);
+      else aw[((q / 16) * kRowA) / 2 + q % 16] = e2m1x2_to_f16x2(ra[i]);
+      bw[((q / 64) * kRowH) / 2 + q % 64] = e2m1x2_to_f16x2(rb[i]);
+    }
+    if (tid < kTcT) es1[buf][tid] = (uint8_t)rs;
+    else es2[buf][tid - kTcT] = (uint8_t)rs;
+    if (rs >= 245u && rs != 255u) huge[buf] = 1;
+  };
+
+  float tot[4][4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tot[a][b][c] = 0.f;
+
+  if (tid == 0) huge[0] = huge[1] = 0;
+  __syncthreads();
+  fetch(0);
+  store(0);
+  __syncthreads();
+  for (int64_t j = 0; j < J; ++j) {
+    const int buf = (int)(j & 1);
+    const uint32_t a_base = smem_u32(as[0]) + (uint32_t)buf * (uint32_t)sizeof(as[0]);
+    const uint32_t b_base = smem_u32(bs[0]) + (uint32_t)buf * (uint32_t)sizeof(bs[0]);
+    if (j + 1 < J) fetch(j + 1);  // in flight during this slice's MMAs
+    float acc[4][4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      uint32_t af[4][4], bf[4][2];
+      const int sub = lane >> 3, r8 = lane & 7;
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        const int mb = wm * 64 + mt * 16;
+        if constexpr (X1T) {
+          const int k = kk * 16 + r8 + 8 * (sub >> 1), m = mb + 8 * (sub & 1);
+          ldmatrix_x4_trans(a_base + (uint32_t)(k * kRowH + m) * 2u, af[mt][0], af[mt][1],
+                            af[mt][2], af[mt][3]);
+        } else {
+          const int m = mb + r8 + 8 * (sub & 1), k = kk * 16 + 8 * (sub >> 1);
+          ldmatrix_x4(a_base + (uint32_t)(m * kRowA + k) * 2u, af[mt][0], af[mt][1], af[mt][2],
+                      af[mt][3]);
+        }
+      }
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {
+        const int k = kk * 16 + r8 + 8 * (sub & 1), n = wn * 32 + np * 16 + 8 * (sub >> 1);
+        ldmatrix_x4_trans(b_base + (uint32_t)(k * kRowH + n) * 2u, bf[2 * np][0], bf[2 * np][1],
+                          bf[2 * np + 1][0], bf[2 * np + 1][1]);
+      }
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+          mma_16816<false>(acc[mt][nt], af[mt][0], af[mt][1], af[mt][2], af[mt][3], bf[nt][0], bf[nt][1]);
+    }
+    // scale the slice and add it: element c of tile (mt, nt) is row g + 8 (c >> 1),
+    // column 2t + (c & 1)
+    if (!huge[buf]) {
+      float hc[4][2];
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int cb = wn * 32 + nt * 8 + 2 * t;
+        hc[nt][0] = e8m0_factor(es2[buf][cb]);
+        hc[nt][1] = e8m0_factor(es2[buf][cb + 1]);
+      }
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        const float f0 = e8m0_factor(es1[buf][wm * 64 + mt * 16 + g]);
+        const float f1 = e8m0_factor(es1[buf][wm * 64 + mt * 16 + g + 8]);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          const float h0 = hc[nt][0], h1 = hc[nt][1];
+          tot[mt][nt][0] = fmaf(acc[mt][nt][0] * f0, h0, tot[mt][nt][0]);
+          tot[mt][nt][1] = fmaf(acc[mt][nt][1] * f0, h1, tot[mt][nt][1]);
+          tot[mt][nt][2] = fmaf(acc[mt][nt][2] * f1, h0, tot[mt][nt][2]);
+          tot[mt][nt][3] = fmaf(acc[mt][nt][3] * f1, h1, tot[mt][nt][3]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t e1 = es1[buf][wm * 64 + mt * 16 + g + 8 * (c >> 1)];
+            const uint32_t e2 = es2[buf][wn * 32 + nt * 8 + 2 * t + (c & 1)];
+            const float v = (e1 == 255u || e2 == 255u)
+                                ? __int_as_float(0x7fc00000)
+                                : scale_two_step(acc[mt][nt][c], (int)e1 + (int)e2 - 254);
+            tot[mt][nt][c] += v;
+          }
+    }
+    if (j + 1 < J) {
+      if (tid == 0) huge[buf ^ 1] = 0;  // the other buffer was last read a slice ago
+      __syncthreads();                  // (and its flag with it)
+      store(buf ^ 1);
+    }
+    __syncthreads();
+  }
+  // y += tot
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int64_t m = m0 + wm * 64 + mt * 16 + g + 8 * (c >> 1);
+        const int64_t n = n0 + wn * 32 + nt * 8 + 2 * t + (c & 1);
+        if (m < M && n < N) y[m * N + n] += tot[mt][nt][c];
+      }
+}
+
 }  // namespace
 
 cudaError_t launch_pack_fp4(const float *in, uint8_t *out, int64_t K, int64_t N, cudaStream_t s) {
@@ -136,6 +356,17 @@ cudaError_t launch_pack_fp4(const float *in, uint8_t *out, int64_t K, int64_t N,
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   pack_fp4_kernel<<<(unsigned)blocks, 256, 0, s>>>(in, out, nvec, tail, nbytes);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_matmul_add_tc(const uint8_t *x1, const uint8_t *s1, bool x1t,
+                                    const uint8_t *x2, const uint8_t *s2, float *y, int64_t M,
+                                    int64_t K, int64_t N, cudaStream_t s) {
+  const dim3 grid((unsigned)((N + kTcT - 1) / kTcT), (unsigned)((M + kTcT - 1) / kTcT), 1);
+  if (x1t)
+    mx_mma_kernel<true><<<grid, kTcThreads, 0, s>>>(x1, s1, x2, s2, y, M, K, N);
+  else
+    mx_mma_kernel<false><<<grid, kTcThreads, 0, s>>>(x1, s1, x2, s2, y, M, K, N);
   return cudaGetLastError();
 }
 

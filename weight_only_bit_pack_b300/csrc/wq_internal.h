@@ -88,7 +88,12 @@ cudaError_t launch_int4_remap(const uint8_t *in, int in_layout, uint8_t *out, in
 cudaError_t launch_decode_tiled(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
 // FP4 E2M1 pack and the mx block-scaled matmul (wq_fp4.cu).
 cudaError_t launch_pack_fp4(const float *in, uint8_t *out, int64_t K, int64_t N, cudaStream_t s);
-// x1t: x1 stored (K, M) packed along M and scale1 (ceil(K/32), M)
+// x1t: x1 stored (K, M) packed along M and scale1 (ceil(K/32), M). The first
+// form is exact (fp64 slice sums); the _tc form runs the slices on the tensor
+// cores and adds them in fp32.
+cudaError_t launch_mx_matmul_add_tc(const uint8_t *x1, const uint8_t *s1, bool x1t,
+                                    const uint8_t *x2, const uint8_t *s2, float *y, int64_t M,
+                                    int64_t K, int64_t N, cudaStream_t s);
 cudaError_t launch_mx_matmul_add(const uint8_t *x1, const uint8_t *s1, bool x1t, const uint8_t *x2,
                                  const uint8_t *s2, float *y, int64_t M, int64_t K, int64_t N,
                                  cudaStream_t s);
