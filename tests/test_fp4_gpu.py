@@ -207,8 +207,10 @@ def test_mx_tensor_kernel_within_bound(wq, M, K, N):
     _check_tc(wq, *_mx_case(M, K, N, seed=5000 + M * 7 + K + N))
 
 
-@pytest.mark.parametrize("M,K,N", [(2, 32, 2), (130, 70, 10), (128, 256, 130), (256, 512, 256)])
+@pytest.mark.parametrize("M,K,N", [(2, 32, 2), (130, 70, 10), (128, 256, 130), (256, 512, 256),
+                                   (128, 70, 128), (64, 1000, 96), (160, 2048, 352)])
 def test_mx_tensor_kernel_transposed_x1(wq, M, K, N):
+    # M and N multiples of 32 take the copy-ring kernel, the others the register-fetch one
     _check_tc(wq, *_mx_case(M, K, N, seed=6000 + M + K + N), x1_transposed=True)
 
 

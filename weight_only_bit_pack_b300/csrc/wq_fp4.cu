@@ -174,6 +174,90 @@ __device__ __forceinline__ float scale_two_step(float acc, int e) {
   return acc * __int_as_float((a + 127) << 23) * __int_as_float((b + 127) << 23);
 }
 
+// One slice of a warp's 64 x 32 tile: two m16n8k16 MMAs deep from the fp16
+// tiles at a_base / b_base, then scaled by the slice's E8M0 bytes (e1s per tile
+// row, e2s per tile column) and added to tot.
+template <bool X1T>
+__device__ __forceinline__ void mx_slice(uint32_t a_base, uint32_t b_base, const uint8_t *e1s,
+                                         const uint8_t *e2s, bool huge, float (&tot)[4][4][4],
+                                         int lane, int wm, int wn) {
+  const int g = lane >> 2, t = lane & 3;
+  float acc[4][4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk) {
+    uint32_t af[4][4], bf[4][2];
+    const int sub = lane >> 3, r8 = lane & 7;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const int mb = wm * 64 + mt * 16;
+      if constexpr (X1T) {
+        const int k = kk * 16 + r8 + 8 * (sub >> 1), m = mb + 8 * (sub & 1);
+        ldmatrix_x4_trans(a_base + (uint32_t)(k * kRowH + m) * 2u, af[mt][0], af[mt][1],
+                          af[mt][2], af[mt][3]);
+      } else {
+        const int m = mb + r8 + 8 * (sub & 1), k = kk * 16 + 8 * (sub >> 1);
+        ldmatrix_x4(a_base + (uint32_t)(m * kRowA + k) * 2u, af[mt][0], af[mt][1], af[mt][2],
+                    af[mt][3]);
+      }
+    }
+#pragma unroll
+    for (int np = 0; np < 2; ++np) {
+      const int k = kk * 16 + r8 + 8 * (sub & 1), n = wn * 32 + np * 16 + 8 * (sub >> 1);
+      ldmatrix_x4_trans(b_base + (uint32_t)(k * kRowH + n) * 2u, bf[2 * np][0], bf[2 * np][1],
+                        bf[2 * np + 1][0], bf[2 * np + 1][1]);
+    }
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+        mma_16816<false>(acc[mt][nt], af[mt][0], af[mt][1], af[mt][2], af[mt][3], bf[nt][0], bf[nt][1]);
+  }
+  // scale the slice and add it: element c of tile (mt, nt) is row g + 8 (c >> 1),
+  // column 2t + (c & 1)
+  if (!huge) {
+    float hc[4][2];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const int cb = wn * 32 + nt * 8 + 2 * t;
+      hc[nt][0] = e8m0_factor(e2s[cb]);
+      hc[nt][1] = e8m0_factor(e2s[cb + 1]);
+    }
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const float f0 = e8m0_factor(e1s[wm * 64 + mt * 16 + g]);
+      const float f1 = e8m0_factor(e1s[wm * 64 + mt * 16 + g + 8]);
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const float h0 = hc[nt][0], h1 = hc[nt][1];
+        tot[mt][nt][0] = fmaf(acc[mt][nt][0] * f0, h0, tot[mt][nt][0]);
+        tot[mt][nt][1] = fmaf(acc[mt][nt][1] * f0, h1, tot[mt][nt][1]);
+        tot[mt][nt][2] = fmaf(acc[mt][nt][2] * f1, h0, tot[mt][nt][2]);
+        tot[mt][nt][3] = fmaf(acc[mt][nt][3] * f1, h1, tot[mt][nt][3]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t e1 = e1s[wm * 64 + mt * 16 + g + 8 * (c >> 1)];
+          const uint32_t e2 = e2s[wn * 32 + nt * 8 + 2 * t + (c & 1)];
+          const float v = (e1 == 255u || e2 == 255u)
+                              ? __int_as_float(0x7fc00000)
+                              : scale_two_step(acc[mt][nt][c], (int)e1 + (int)e2 - 254);
+          tot[mt][nt][c] += v;
+        }
+  }
+}
+
 template <bool X1T>
 __global__ void __launch_bounds__(kTcThreads, 1)
     mx_mma_kernel(const uint8_t *__restrict__ x1, const uint8_t *__restrict__ s1,
@@ -250,80 +334,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t a_base = smem_u32(as[0]) + (uint32_t)buf * (uint32_t)sizeof(as[0]);
     const uint32_t b_base = smem_u32(bs[0]) + (uint32_t)buf * (uint32_t)sizeof(bs[0]);
     if (j + 1 < J) fetch(j + 1);  // in flight during this slice's MMAs
-    float acc[4][4][4];
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      uint32_t af[4][4], bf[4][2];
-      const int sub = lane >> 3, r8 = lane & 7;
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-        const int mb = wm * 64 + mt * 16;
-        if constexpr (X1T) {
-          const int k = kk * 16 + r8 + 8 * (sub >> 1), m = mb + 8 * (sub & 1);
-          ldmatrix_x4_trans(a_base + (uint32_t)(k * kRowH + m) * 2u, af[mt][0], af[mt][1],
-                            af[mt][2], af[mt][3]);
-        } else {
-          const int m = mb + r8 + 8 * (sub & 1), k = kk * 16 + 8 * (sub >> 1);
-          ldmatrix_x4(a_base + (uint32_t)(m * kRowA + k) * 2u, af[mt][0], af[mt][1], af[mt][2],
-                      af[mt][3]);
-        }
-      }
-#pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        const int k = kk * 16 + r8 + 8 * (sub & 1), n = wn * 32 + np * 16 + 8 * (sub >> 1);
-        ldmatrix_x4_trans(b_base + (uint32_t)(k * kRowH + n) * 2u, bf[2 * np][0], bf[2 * np][1],
-                          bf[2 * np + 1][0], bf[2 * np + 1][1]);
-      }
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-          mma_16816<false>(acc[mt][nt], af[mt][0], af[mt][1], af[mt][2], af[mt][3], bf[nt][0], bf[nt][1]);
-    }
-    // scale the slice and add it: element c of tile (mt, nt) is row g + 8 (c >> 1),
-    // column 2t + (c & 1)
-    if (!huge[buf]) {
-      float hc[4][2];
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int cb = wn * 32 + nt * 8 + 2 * t;
-        hc[nt][0] = e8m0_factor(es2[buf][cb]);
-        hc[nt][1] = e8m0_factor(es2[buf][cb + 1]);
-      }
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt) {
-        const float f0 = e8m0_factor(es1[buf][wm * 64 + mt * 16 + g]);
-        const float f1 = e8m0_factor(es1[buf][wm * 64 + mt * 16 + g + 8]);
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-          const float h0 = hc[nt][0], h1 = hc[nt][1];
-          tot[mt][nt][0] = fmaf(acc[mt][nt][0] * f0, h0, tot[mt][nt][0]);
-          tot[mt][nt][1] = fmaf(acc[mt][nt][1] * f0, h1, tot[mt][nt][1]);
-          tot[mt][nt][2] = fmaf(acc[mt][nt][2] * f1, h0, tot[mt][nt][2]);
-          tot[mt][nt][3] = fmaf(acc[mt][nt][3] * f1, h1, tot[mt][nt][3]);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint32_t e1 = es1[buf][wm * 64 + mt * 16 + g + 8 * (c >> 1)];
-            const uint32_t e2 = es2[buf][wn * 32 + nt * 8 + 2 * t + (c & 1)];
-            const float v = (e1 == 255u || e2 == 255u)
-                                ? __int_as_float(0x7fc00000)
-                                : scale_two_step(acc[mt][nt][c], (int)e1 + (int)e2 - 254);
-            tot[mt][nt][c] += v;
-          }
-    }
+    mx_slice<X1T>(a_base, b_base, es1[buf], es2[buf], huge[buf] != 0, tot, lane, wm, wn);
     if (j + 1 < J) {
       if (tid == 0) huge[buf ^ 1] = 0;  // the other buffer was last read a slice ago
       __syncthreads();                  // (and its flag with it)
@@ -340,6 +351,143 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int c = 0; c < 4; ++c) {
         const int64_t m = m0 + wm * 64 + mt * 16 + g + 8 * (c >> 1);
         const int64_t n = n0 + wn * 32 + nt * 8 + 2 * t + (c & 1);
+        if (m < M && n < N) y[m * N + n] += tot[mt][nt][c];
+      }
+}
+
+// The transposed-x1 form (the page's supported one) with x1, x2 and the scales
+// copied a raw slice at a time by cp.async into a ring of kRing stages, three
+// slices ahead of their use, then decoded into the fp16 tiles: the copies no
+// longer wait on a single slice of compute. Needs M and N multiples of 32 and
+// 16-byte aligned operands (16-byte copies that never straddle the edge).
+constexpr int kRing = 4;
+constexpr uint32_t kRawA = kGs * 64, kRawB = kGs * 64, kRawS = 2 * kTcT;
+constexpr uint32_t kRawStage = kRawA + kRawB + kRawS;
+constexpr uint32_t kF16Tile = kGs * kRowH * 2;
+constexpr uint32_t kRingSmem = kRing * kRawStage + 4 * kF16Tile;
+
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_group() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    mx_mma_ring_kernel(const uint8_t *__restrict__ x1, const uint8_t *__restrict__ s1,
+                       const uint8_t *__restrict__ x2, const uint8_t *__restrict__ s2,
+                       float *__restrict__ y, int64_t M, int64_t K, int64_t N) {
+  extern __shared__ __align__(16) uint8_t mx_smem[];
+  __shared__ int huge[2];
+  const uint32_t raw = smem_u32(mx_smem);
+  const uint32_t fa = raw + kRing * kRawStage;  // two A tiles, then two B tiles
+  const uint32_t fb = fa + 2 * kF16Tile;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int wm = warp & 1, wn = warp >> 1;
+  const int64_t m0 = (int64_t)blockIdx.y * kTcT, n0 = (int64_t)blockIdx.x * kTcT;
+  const int64_t J = (K + kGs - 1) / kGs;
+
+  // stage st of the ring: 32 rows x 64 bytes of x1 (threads 0..127) and of x2
+  // (threads 128..255), 16 bytes a thread, and the slice's 128 + 128 scale bytes
+  // (threads 0..15); copies past K, M or N read nothing and fill zeros
+  auto issue = [&](int64_t st) {
+    if (st < J) {
+      const uint32_t slot = raw + (uint32_t)(st % kRing) * kRawStage;
+      const int64_t k0 = st * kGs;
+      const int row = (tid & 127) >> 2, c = tid & 3;
+      const bool kin = k0 + row < K;
+      if (tid < 128) {
+        const bool ok = kin && m0 / 2 + 16 * c < M / 2;
+        cp_async16_zfill(slot + (uint32_t)(row * 64 + 16 * c),
+                         ok ? x1 + (k0 + row) * (M / 2) + m0 / 2 + 16 * c : x1, ok);
+      } else {
+        const bool ok = kin && n0 / 2 + 16 * c < N / 2;
+        cp_async16_zfill(slot + kRawA + (uint32_t)(row * 64 + 16 * c),
+                         ok ? x2 + (k0 + row) * (N / 2) + n0 / 2 + 16 * c : x2, ok);
+      }
+      if (tid < 8) {
+        const bool ok = m0 + 16 * tid < M;
+        cp_async16_zfill(slot + kRawA + kRawB + 16u * tid, ok ? s1 + st * M + m0 + 16 * tid : s1, ok);
+      } else if (tid < 16) {
+        const int q = tid - 8;
+        const bool ok = n0 + 16 * q < N;
+        cp_async16_zfill(slot + kRawA + kRawB + kTcT + 16u * q, ok ? s2 + st * N + n0 + 16 * q : s2, ok);
+      }
+    }
+    cp_async_commit_group();  // one group per stage on every thread, empty or not
+  };
+  // raw stage st -> fp16 tiles b: 8 bytes of codes a thread for each operand
+  auto decode = [&](int64_t st, int b) {
+    const uint32_t slot = raw + (uint32_t)(st % kRing) * kRawStage;
+    const int row = tid >> 3, off = (tid & 7) * 8;
+#pragma unroll
+    for (int op = 0; op < 2; ++op) {
+      uint32_t lo, hi;
+      asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];"
+                   : "=r"(lo), "=r"(hi)
+                   : "r"(slot + (op ? kRawA : 0u) + (uint32_t)(row * 64 + off)));
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        w[i] = e2m1x2_to_f16x2((lo >> (8 * i)) & 0xFFu);
+        w[4 + i] = e2m1x2_to_f16x2((hi >> (8 * i)) & 0xFFu);
+      }
+      const uint32_t dst = (op ? fb : fa) + (uint32_t)b * kF16Tile + (uint32_t)(row * kRowH * 2 + off * 4);
+      asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                   "r"(w[3])
+                   : "memory");
+      asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst + 16), "r"(w[4]), "r"(w[5]),
+                   "r"(w[6]), "r"(w[7])
+                   : "memory");
+    }
+    const uint32_t e = mx_smem[(st % kRing) * kRawStage + kRawA + kRawB + tid];
+    if (e >= 245u && e != 255u) huge[b] = 1;
+  };
+
+  float tot[4][4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tot[a][b][c] = 0.f;
+
+  if (tid == 0) huge[0] = huge[1] = 0;
+#pragma unroll
+  for (int st = 0; st < kRing - 1; ++st) issue(st);
+  cp_async_wait_group<kRing - 2>();
+  __syncthreads();
+  decode(0, 0);
+  __syncthreads();
+  for (int64_t j = 0; j < J; ++j) {
+    const int buf = (int)(j & 1);
+    issue(j + kRing - 1);
+    const uint8_t *es = mx_smem + (j % kRing) * kRawStage + kRawA + kRawB;
+    mx_slice<true>(fa + (uint32_t)buf * kF16Tile, fb + (uint32_t)buf * kF16Tile, es, es + kTcT,
+                   huge[buf] != 0, tot, lane, wm, wn);
+    if (j + 1 < J) {
+      cp_async_wait_group<kRing - 2>();  // stage j + 1 has landed (this thread's copies)
+      if (tid == 0) huge[buf ^ 1] = 0;   // last read a slice ago
+      __syncthreads();                   // ... and everyone's, and tiles buf ^ 1 are free
+      decode(j + 1, buf ^ 1);
+    }
+    __syncthreads();
+  }
+  cp_async_wait_group<0>();  // no copy in flight at exit (only empty groups remain)
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int64_t m = m0 + wm * 64 + mt * 16 + (lane >> 2) + 8 * (c >> 1);
+        const int64_t n = n0 + wn * 32 + nt * 8 + 2 * (lane & 3) + (c & 1);
         if (m < M && n < N) y[m * N + n] += tot[mt][nt][c];
       }
 }
@@ -363,7 +511,13 @@ cudaError_t launch_mx_matmul_add_tc(const uint8_t *x1, const uint8_t *s1, bool x
                                     const uint8_t *x2, const uint8_t *s2, float *y, int64_t M,
                                     int64_t K, int64_t N, cudaStream_t s) {
   const dim3 grid((unsigned)((N + kTcT - 1) / kTcT), (unsigned)((M + kTcT - 1) / kTcT), 1);
-  if (x1t)
+  auto a16 = [](const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
+  if (x1t && M % 32 == 0 && N % 32 == 0 && a16(x1) && a16(x2) && a16(s1) && a16(s2)) {
+    static cudaError_t attr = cudaFuncSetAttribute(
+        mx_mma_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingSmem);
+    if (attr != cudaSuccess) return attr;
+    mx_mma_ring_kernel<<<grid, kTcThreads, kRingSmem, s>>>(x1, s1, x2, s2, y, M, K, N);
+  } else if (x1t)
     mx_mma_kernel<true><<<grid, kTcThreads, 0, s>>>(x1, s1, x2, s2, y, M, K, N);
   else
     mx_mma_kernel<false><<<grid, kTcThreads, 0, s>>>(x1, s1, x2, s2, y, M, K, N);
