@@ -7,9 +7,10 @@
 // two rows and the whole pack is a flat map from 2*i, 2*i+1 to byte i.
 //
 // The kernel is bound by HBM: 8 bytes read and 1 written per output byte. Each
-// thread turns 32 int32 (eight 16-byte streaming loads) into one 16-byte store;
-// a grid-stride loop over 16-byte units keeps every SM busy, and a scalar tail
-// covers a byte count that is not a multiple of 16 or unaligned pointers.
+// thread turns 8 int32 (two neighbouring 16-byte streaming loads, so a warp
+// reads 1 KB contiguously) into one 4-byte store; a grid-stride loop over 4-byte
+// units keeps every SM busy, and a scalar tail covers a byte count that is not
+// a multiple of 4 or unaligned pointers.
 #include "wq_internal.h"
 #include "wq_common.cuh"
 
@@ -29,16 +30,9 @@ __global__ void __launch_bounds__(256) pack_int4_kernel(const int32_t *__restric
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   for (int64_t i = tid; i < nvec; i += stride) {
-    const int32_t *src = in + i * 32;
-    uint4 v[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = ld_stream_u4(src + 4 * j);
-    uint4 o;
-    o.x = nib8(v[0], v[1]);
-    o.y = nib8(v[2], v[3]);
-    o.z = nib8(v[4], v[5]);
-    o.w = nib8(v[6], v[7]);
-    st_stream_u4(out + i * 16, o);
+    const int32_t *src = in + i * 8;
+    const uint4 a = ld_stream_u4(src), b = ld_stream_u4(src + 4);
+    __stcs(reinterpret_cast<unsigned int *>(out) + i, nib8(a, b));
   }
   for (int64_t b = tail_begin + tid; b < nbytes; b += stride) {
     const uint32_t lo = (uint32_t)in[2 * b] & 0xFu;
@@ -51,9 +45,9 @@ __global__ void __launch_bounds__(256) pack_int4_kernel(const int32_t *__restric
 
 cudaError_t launch_pack_int4(const int32_t *in, uint8_t *out, int64_t K, int64_t N, cudaStream_t s) {
   const int64_t nbytes = K * (N / 2);
-  const bool aligned = ((uintptr_t)in % 16 == 0) && ((uintptr_t)out % 16 == 0);
-  const int64_t nvec = aligned ? nbytes / 16 : 0;
-  const int64_t tail = nvec * 16;
+  const bool aligned = ((uintptr_t)in % 16 == 0) && ((uintptr_t)out % 4 == 0);
+  const int64_t nvec = aligned ? nbytes / 4 : 0;
+  const int64_t tail = nvec * 4;
   const int64_t work = nvec > 0 ? nvec : (nbytes - tail);
   const int threads = 256;
   int64_t blocks = (work + threads - 1) / threads;
