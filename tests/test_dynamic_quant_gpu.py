@@ -27,7 +27,7 @@ def _check(wq, x, smooth, bits):
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("bits", [8, 4])
 @pytest.mark.parametrize("shape", [(1, 8), (3, 200), (8192, 4096), (2, 5, 1024), (7, 65534),
-                                   (33, 6)])
+                                   (33, 6), (300, 8192), (9, 6144), (5, 2056), (4, 8200)])
 @pytest.mark.parametrize("smooth", [False, True])
 def test_dynamic_quant_bit_exact(wq, dtype, bits, shape, smooth):
     g = torch.Generator(device="cuda").manual_seed(sum(shape) + bits)
