@@ -438,6 +438,17 @@ __global__ void __launch_bounds__(TTHREADS, 1) decode_tiled_kernel(const DTArgs 
   __syncthreads();
   // 1/RMS of row m: warp m sums the CTAs' partials (lane-strided, then a fixed
   // shuffle tree: the same order in every CTA and every run)
+  // the last CTA through clears the grid counters for the next call; with
+  // fewer than TW rows the last warp has no row sum to form, so its atomic's
+  // round trip overlaps the sums below (else thread 0 departs after them)
+  auto depart = [&]() {
+    if (atomicAdd(a.gbar + 1, 1u) == (uint32_t)a.G - 1u) {
+      atomicExch(a.gbar, 0u);
+      atomicExch(a.gbar + 1, 0u);
+    }
+  };
+  const bool early = a.M < TW;
+  if (early && threadIdx.x == TTHREADS - 32) depart();
   if (warp < a.M && !s_abort) {
     // all of the lane's loads first (the grid has at most 32 * kTParts CTAs),
     // then the sum in CTA order
@@ -455,13 +466,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) decode_tiled_kernel(const DTArgs 
     if (lane == 0) s_rstd[warp] = rsqrtf(tot2 / (float)a.N + a.eps);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    // the last CTA through clears the grid counters for the next call
-    if (atomicAdd(a.gbar + 1, 1u) == (uint32_t)a.G - 1u) {
-      atomicExch(a.gbar, 0u);
-      atomicExch(a.gbar + 1, 0u);
-    }
-  }
+  if (!early && threadIdx.x == 0) depart();
   if (s_abort) return;  // a CTA whose wait gave up writes no normOut
   for (int e = threadIdx.x; e < a.M * npair; e += TTHREADS) {
     const int m = e / npair, col = 2 * (e - m * npair);
