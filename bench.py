@@ -75,7 +75,7 @@ def parse_args():
 
 def make_problem(config: str, device):
     from weight_only_bit_pack_b300 import inputs
-    config = config.split("@")[0]  # "@tiled": same workload, weight in the tiled layout
+    config = config.split("@")[0]  # "@tiled", "@transposed": same workload, weight layout
     if config in inputs.CONFIGS:
         return inputs.CONFIGS[config](device)
     if config.startswith("sweep_pt:"):
@@ -301,15 +301,28 @@ def cpu_baseline(p, seconds=10.0, max_reps=200):
 
 # ------------------------------------------------------------------ our arm
 
+def layout_of(config):
+    """Weight layout named by a config's suffix: "@tiled", "@transposed", else dense."""
+    return config.split("@")[1] if "@" in config else "dense"
+
+
+def layout_suffix(layout):
+    return "" if layout == "dense" else "_" + layout
+
+
 class Runner:
     """R distinct input sets of one workload on the device (weights packed once,
     then copied), a zeroed workspace, and step(i) = one C-ABI call on set i % R."""
 
-    def __init__(self, wq, p, kernel, dev, stream, tiled=False):
-        self.p, self.kernel, self.stream, self.tiled = p, kernel, stream, tiled
+    def __init__(self, wq, p, kernel, dev, stream, layout="dense"):
+        self.p, self.kernel, self.stream = p, kernel, stream
+        self.layout, self.tiled = layout, layout == "tiled"
+        tiled = self.tiled
         self.w_src = p.x2
         if tiled:
             self.w0 = wq.pack_int4_tiled(p.x2)
+        elif layout == "transposed":
+            self.w0 = wq.TransposedWeight(wq.pack_int4(p.x2.t().contiguous()), 4)
         else:
             self.w0 = wq.pack_int4(p.x2) if p.wbits == 4 else p.x2.contiguous()
         self.ab = alg_bytes(p)
@@ -319,8 +332,12 @@ class Runner:
         self.R = max(1, min(R, 64))
         self.sets = []
         for i in range(self.R):
-            w = (wq.TiledInt4(self.w0.data.clone(), self.w0.K, self.w0.N) if tiled
-                 else self.w0.clone())
+            if tiled:
+                w = wq.TiledInt4(self.w0.data.clone(), self.w0.K, self.w0.N)
+            elif layout == "transposed":
+                w = wq.TransposedWeight(self.w0.data.clone(), 4)
+            else:
+                w = self.w0.clone()
             s = {"x1": p.x1.clone(), "w": w, "scale": p.scale.clone(),
                  "offset": None if p.offset is None else p.offset.clone(),
                  "bias": None if p.bias is None else p.bias.clone(),
@@ -389,7 +406,7 @@ def time_extra(wq, config, dev, stream, steps, warmup, peaks):
     """Device time of one named workload (graph replay, CUDA events), for the
     line's "workloads" key."""
     p = make_problem(config, dev)
-    r = Runner(wq, p, 0, dev, stream, tiled=config.endswith("@tiled"))
+    r = Runner(wq, p, 0, dev, stream, layout=layout_of(config))
     for i in range(warmup):
         r.step(i)
     graphs = capture_graphs(r, steps)
@@ -405,7 +422,7 @@ def time_extra(wq, config, dev, stream, steps, warmup, peaks):
     torch.cuda.synchronize(dev)
     ms = ev0.elapsed_time(ev1) / steps
     roof = roofline(p, ms, peaks)
-    out = {"workload": p.name + ("_tiled" if r.tiled else ""), "M": p.M, "K": p.K, "N": p.N,
+    out = {"workload": p.name + layout_suffix(r.layout), "M": p.M, "K": p.K, "N": p.N,
            "kernel":
            ["auto", "generic", "decode", "prefill"][r.chosen], "steps": steps, "ms_per_step": ms,
            "TFLOP/s": 2.0 * p.M * p.K * p.N / (ms * 1e-3) / 1e12,
@@ -561,7 +578,7 @@ def run_ours(args, world, rank, local):
 
     stream = torch.cuda.Stream(device=dev)
     torch.cuda.set_stream(stream)
-    runner = Runner(wq, p, kernel, dev, stream, tiled=args.config.endswith("@tiled"))
+    runner = Runner(wq, p, kernel, dev, stream, layout=layout_of(args.config))
     w_src, w0, ab, R, sets = runner.w_src, runner.w0, runner.ab, runner.R, runner.sets
     chosen = runner.chosen
     step = runner.step
@@ -709,7 +726,7 @@ def run_ours(args, world, rank, local):
 
     # INT32 -> INT4 pack of this workload's weight (once per weight in deployment)
     pack = None
-    if not args.no_pack and p.wbits == 4:
+    if not args.no_pack and p.wbits == 4 and runner.layout != "transposed":
         if runner.tiled:
             out = wq.TiledInt4(torch.empty_like(w0.data), w0.K, w0.N)
             pack_fn = lambda: wq.pack_int4_tiled(w_src, out=out, stream=stream)  # noqa: E731
@@ -738,7 +755,7 @@ def run_ours(args, world, rank, local):
     roof = roofline(p, ms_step, peaks)
     # the dominant kernel's DRAM bytes per launch, from the committed ncu capture
     kname = {3: "prefill_kernel", 2: "decode_kernel"}.get(chosen, "generic_gemm_kernel")
-    wname = p.name + ("_tiled" if runner.tiled else "")
+    wname = p.name + layout_suffix(runner.layout)
     roof["traffic"] = traffic_record(kname, wname)
     roof["traffic_source"] = ("profiles/traffic.md (ncu dram__bytes_read.sum + "
                               "dram__bytes_write.sum of one launch)"

@@ -267,10 +267,20 @@ int32_t make_plan(const Problem &p, int32_t kernel, Plan &plan) {
     return WQ_OK;
   }
   int chosen = kernel;
-  if (p.transposed) {  // a transposed weight: the generic kernel reads it in place
-    if (chosen == WQ_KERNEL_DECODE || chosen == WQ_KERNEL_PREFILL)
-      return fail(WQ_ERR_UNSUPPORTED, "the decode and prefill kernels do not read a transposed x2 "
+  if (p.transposed) {
+    // a transposed weight: the transposed-operand large-M kernel (INT4, bf16
+    // per-group scales, no offset), else the generic kernel reads it in place
+    if (chosen == WQ_KERNEL_DECODE)
+      return fail(WQ_ERR_UNSUPPORTED, "the decode kernels do not read a transposed x2 "
                                       "(convert an INT4_T weight with wq_convert_int4_layout)");
+    if (chosen == WQ_KERNEL_PREFILL || (chosen == WQ_KERNEL_AUTO && p.M > 16)) {
+      if (plan_prefill_t(p, plan)) return WQ_OK;
+      if (chosen == WQ_KERNEL_PREFILL)
+        return fail(WQ_ERR_UNSUPPORTED,
+                    "the prefill kernel reads a transposed x2 only as INT4 with bf16 per-group "
+                    "scales (group %% 32 == 0) and no offset, k %% 64 == 0, n %% 32 == 0 and "
+                    "16-byte aligned tensors");
+    }
     chosen = WQ_KERNEL_GENERIC;
   }
   if (p.tiled) {
@@ -700,7 +710,7 @@ int32_t wq_matmul_add_rmsnorm_ex(
       if (e != cudaSuccess) return cuda_fail(e, "epilogue kernel launch");
       break;
     case WQ_KERNEL_PREFILL:
-      e = launch_prefill(p, plan, ws, s);
+      e = plan.mode == 2 ? launch_prefill_t(p, plan, ws, s) : launch_prefill(p, plan, ws, s);
       if (e != cudaSuccess) return cuda_fail(e, "prefill kernel launch");
       break;
     case WQ_KERNEL_DECODE:

@@ -97,6 +97,12 @@ cudaError_t launch_mx_matmul_add_tc(const uint8_t *x1, const uint8_t *s1, bool x
 cudaError_t launch_mx_matmul_add(const uint8_t *x1, const uint8_t *s1, bool x1t, const uint8_t *x2,
                                  const uint8_t *s2, float *y, int64_t M, int64_t K, int64_t N,
                                  cudaStream_t s);
+// Large-M kernel for transposed INT4 weights with bf16 per-group scales and no
+// offset (wq_prefill_t.cu), and its scale pre-pass (wq_prep.cu).
+bool prefill_t_applicable(const Problem &p);
+bool plan_prefill_t(const Problem &p, Plan &plan);
+cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
+cudaError_t launch_so_prep_t(const Problem &p, int16_t *e_col, uint32_t *S16T, cudaStream_t s);
 // Per-token symmetric dynamic quantization (wq_dynquant.cu); bits 8 or 4.
 cudaError_t launch_dynamic_quant(const void *x, const void *smooth, int dtype, int64_t M, int64_t K,
                                  int bits, void *y, float *scale, cudaStream_t s);

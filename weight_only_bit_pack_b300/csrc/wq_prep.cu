@@ -176,6 +176,22 @@ __global__ void __launch_bounds__(256)
     const int c = n & 255, l = c >> 3, i = c & 7;
     dst = (n - c) + (i < 4 ? 4 * l + i : 128 + 4 * l + (i - 4));
   }
+  if (int4 == 2) {
+    // transposed INT4 weights: one word per (group, column), S16 in bits 15:0
+    // for the even k of a byte and S16 / 16 in bits 31:16 for the odd k
+    // (whose nibble is used in place at bits 7:4), plain column order
+    if (n < N) {
+      const int e = s_exp[cx];
+#pragma unroll 4
+      for (int g = gy; g < G; g += 8) {
+        const float v = E::to_f(S[(int64_t)g * N + n]);
+        const uint32_t lo = (uint32_t)__half_as_ushort(__float2half_rn(scale_pow2(v, -e)));
+        const uint32_t hi = (uint32_t)__half_as_ushort(__float2half_rn(scale_pow2(v, -e - 4)));
+        S16[(int64_t)g * N + n] = lo | (hi << 16);
+      }
+    }
+    return;
+  }
   if (n < ld) {
     const int e = s_exp[cx];
     const int es = (int4 && (n & 1)) ? -e - 4 : -e;  // odd INT4 columns: scale / 16 (exact)
@@ -215,6 +231,18 @@ cudaError_t launch_row_prep(const Problem &p, float *rowsum, int16_t *e_row, __h
     row_prep_kernel<WQ_F16><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const __half *>(p.x1), p.M,
                                                              (int)p.K, rowsum, e_row, x16, dext,
                                                              group, G, ldx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_so_prep_t(const Problem &p, int16_t *e_col, uint32_t *S16T, cudaStream_t s) {
+  const int N = (int)p.N;
+  const int blocks = (N + 31) / 32;
+  if (p.dtype == WQ_BF16)
+    so_prep_kernel<WQ_BF16><<<blocks, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(p.scale), nullptr,
+                                                   (int)p.G, N, N, 8.f, 2, e_col, S16T, nullptr, 0);
+  else
+    so_prep_kernel<WQ_F16><<<blocks, 256, 0, s>>>(static_cast<const __half *>(p.scale), nullptr,
+                                                  (int)p.G, N, N, 8.f, 2, e_col, S16T, nullptr, 0);
   return cudaGetLastError();
 }
 
