@@ -13,14 +13,16 @@
 // Output tile: 256 weight columns (two halves of 128 TMEM lanes, MMA M = 128)
 // x 128 rows of x1 (MMA N = 128), tiles in row-block-major order, one
 // persistent CTA per SM. Warp roles (16 warps):
-//   warp 0       TMA producer: x1 tile (128 rows x 64, fp16 copy with a per-row
-//                power of two, 128-byte swizzle, K-major) per k-step.
+//   warp 0       TMA producer, per k-step: x1 tile (128 rows x 64, fp16 copy
+//                with a per-row power of two, 128-byte swizzle, K-major), the
+//                tile's 256 packed weight rows (32 bytes each, 32-byte swizzle)
+//                and two rows of scale words.
 //   warp 1       TMEM owner (512 columns: D halves at 0 and 128, four A stages
 //                of 64 columns at 256 + 64 s, half h at + 32 h) and MMA issuer
 //                (kind::f16, A from TMEM, B from shared memory, K = 16).
 //   warps 4-11   dequant: warp (half h, lane quarter q) owns weight rows
 //                n = 128 h + 32 q + lane of the tile; per k-step a thread
-//                reads its row's 32 bytes (64 k) from HBM, forms q * S16 in
+//                reads its row's 32 bytes (64 k) from the stage, forms q * S16 in
 //                fp16 (exact) as 32 columns of (k even, k odd) pairs and stores
 //                them to its TMEM lane. The odd k's nibble is used in place at
 //                bits 7:4 (as 1152 + 16 q, with S16 / 16), the even k's at
@@ -67,8 +69,6 @@ enum WhereT : uint32_t {
 };
 
 struct TArgs {
-  const uint8_t *wt;        // (N, K/2) packed INT4, K contiguous
-  const uint32_t *S16T;     // (G, N) words: S16 in bits 15:0, S16 / 16 in bits 31:16
   const int16_t *e_row, *e_col;
   const void *bias, *gamma;
   void *y, *normOut;
@@ -82,10 +82,15 @@ struct TArgs {
   uint32_t extra;
 };
 
+// A stage: x1 tile (16 KB, 128-byte swizzle), the tile's packed weight rows
+// (256 rows x 32 bytes, 32-byte swizzle) and two rows of scale words (2 KB).
 struct LayoutT {
   static constexpr uint32_t X_BYTES = TM * TK * 2;                  // 16 KB
+  static constexpr uint32_t W_BYTES = TN * TK / 2;                  // 8 KB
+  static constexpr uint32_t S_BYTES = 2 * TN * 4;                   // 2 KB
+  static constexpr uint32_t STAGE = X_BYTES + W_BYTES + S_BYTES;    // 26 KB, 1024-aligned
   static constexpr uint32_t X_OFF = 0;
-  static constexpr uint32_t EPI_OFF = X_OFF + NRX * X_BYTES;        // 1024-aligned
+  static constexpr uint32_t EPI_OFF = X_OFF + NRX * STAGE;          // 1024-aligned
   static constexpr uint32_t BAR_OFF = EPI_OFF + kEpiN * (kNRes + 1) * kBox;
   static constexpr int NBARS = 2 * NRX + 2 * NRA + 2 + 1 + kEpiN * kNRes;
   static constexpr uint32_t SMEM = BAR_OFF + 8 * NBARS + 16 + 1024;
@@ -143,7 +148,8 @@ __device__ __forceinline__ uint32_t sub_mul2_h(uint32_t v, uint32_t c, uint32_t 
 }
 
 __global__ void __launch_bounds__(kThreadsT, 1)
-    prefill_t_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_r,
+    prefill_t_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                     const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_r,
                      const TArgs a) {
   using L = LayoutT;
   using T = __nv_bfloat16;
@@ -174,6 +180,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_x);
+    prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_s);
     prefetch_tmap(&tm_r);
   }
   if (warp == 1) {
@@ -187,17 +195,21 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
+    const uint64_t pol_w = policy_evict_last();  // weights are re-read by every row block
     long long it = 0;
     for (long long t = blockIdx.x; t < a.nTiles; t += gridDim.x) {
-      const int rb = (int)(t / a.nTilesN);
+      const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
       for (int ks = 0; ks < a.kTiles; ++ks, ++it) {
         const int s = (int)(it % NRX);
         if (!wait_bar_warp(BAR(TXEMPTY(s)), (uint32_t)(((it / NRX) & 1) ^ 1), abort_flag, a.status,
                            kTWProducer))
           goto pdone;
         if (lane == 0) {
-          mbar_arrive_expect_tx(BAR(TXFULL(s)), L::X_BYTES);
-          tma_load_2d(sbase + L::X_OFF + s * L::X_BYTES, &tm_x, ks * TK, rb * TM, BAR(TXFULL(s)));
+          const uint32_t st = sbase + L::X_OFF + s * L::STAGE;
+          mbar_arrive_expect_tx(BAR(TXFULL(s)), L::STAGE);
+          tma_load_2d(st, &tm_x, ks * TK, rb * TM, BAR(TXFULL(s)));
+          tma_load_2d_hint(st + L::X_BYTES, &tm_w, ks * (TK / 2), nt * TN, BAR(TXFULL(s)), pol_w);
+          tma_load_2d(st + L::X_BYTES + L::W_BYTES, &tm_s, nt * TN, (ks * TK) / a.group, BAR(TXFULL(s)));
         }
         __syncwarp();
       }
@@ -224,7 +236,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             goto mdone;
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t xaddr = sbase + L::X_OFF + s * L::X_BYTES;
+            const uint32_t xaddr = sbase + L::X_OFF + s * L::STAGE;
 #pragma unroll
             for (int kk = 0; kk < TK / 16; ++kk)
 #pragma unroll
@@ -250,57 +262,40 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     // ---------------------------------------------------------------- dequant
     const int h = (warp - kDq0) >> 2, q = warp & 3;
     const uint32_t lane_base = tmem_base + ((uint32_t)(32 * q) << 16) + kColA + (uint32_t)(h * 32);
-    const int kb = a.K / 2;  // bytes per weight row
+    const int r = h * 128 + 32 * q + lane;  // weight row of the tile
+    // this row's two 16-byte chunks in the 32-byte-swizzled weight block:
+    // chunk c of row r at r * 32 + 16 (c ^ ((r >> 2) & 1))
+    const uint32_t woff0 = (uint32_t)(r * 32 + 16 * ((r >> 2) & 1));
+    const uint32_t woff1 = (uint32_t)(r * 32 + 16 * (((r >> 2) & 1) ^ 1));
     long long it = 0;
-    // the 32 bytes (64 k) of weight row n at k-step ks; zero past N or K
-    auto load_w = [&](long long n, int ks, uint4 (&w)[2]) {
-      if (n < a.N && ks < a.kTiles) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(a.wt + n * kb + ks * 32);
-        w[0] = __ldg(src);
-        w[1] = __ldg(src + 1);
-      } else {
-        w[0] = w[1] = make_uint4(0u, 0u, 0u, 0u);
-      }
-    };
-    uint4 wcur[2], wnxt[2];
-    bool have = false;
-    long long n_next = 0;
-    int ks_next = 0;
     for (long long t = blockIdx.x; t < a.nTiles; t += gridDim.x) {
-      const int nt = (int)(t % a.nTilesN);
-      const long long n = (long long)nt * TN + h * 128 + 32 * q + lane;
       for (int ks = 0; ks < a.kTiles; ++ks, ++it) {
-        const int sa = (int)(it % NRA);
-        if (!have) load_w(n, ks, wcur);
-        // the next k-step's bytes (next tile's first when this tile ends) in flight
-        {
-          long long nn = n;
-          int kn = ks + 1;
-          if (kn == a.kTiles) {
-            kn = 0;
-            const long long tn = t + gridDim.x;
-            nn = tn < a.nTiles ? (long long)(tn % a.nTilesN) * TN + h * 128 + 32 * q + lane : a.N;
-          }
-          n_next = nn;
-          ks_next = kn;
-          load_w(n_next, ks_next, wnxt);
-        }
-        // scales of the two 32-deep halves of this k-step (the same word when
-        // the group is a multiple of 64)
-        uint32_t s_lo = 0u, s_hi = 0u;
-        if (n < a.N) {
-          const int k0 = ks * TK;
-          s_lo = __ldg(a.S16T + (long long)(k0 / a.group) * a.N + n);
-          s_hi = (k0 + 32 < a.K) ? __ldg(a.S16T + (long long)((k0 + 32) / a.group) * a.N + n) : 0u;
-        }
+        const int s = (int)(it % NRX), sa = (int)(it % NRA);
+        if (!wait_bar_warp(BAR(TXFULL(s)), (uint32_t)((it / NRX) & 1), abort_flag, a.status, kTWDequant))
+          goto ddone;
+        const uint32_t st = sbase + L::X_OFF + s * L::STAGE;
+        uint32_t w[8];
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "r"(st + L::X_BYTES + woff0));
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                     : "r"(st + L::X_BYTES + woff1));
+        // scale words of the two 32-deep halves: rows k0 / group and (k0 + 32) / group
+        // of the copied pair (the first is row 0)
+        const int k0 = ks * TK;
+        const uint32_t srow1 = (uint32_t)((k0 + 32) / a.group - k0 / a.group);
+        uint32_t s_lo, s_hi;
+        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(s_lo) : "r"(st + L::X_BYTES + L::W_BYTES + 4u * r));
+        asm volatile("ld.shared.b32 %0, [%1];"
+                     : "=r"(s_hi)
+                     : "r"(st + L::X_BYTES + L::W_BYTES + 4u * (srow1 * TN + r)));
         if (!wait_bar_warp(BAR(TAEMPTY(sa)), (uint32_t)(((it / NRA) & 1) ^ 1), abort_flag, a.status,
                            kTWDequant))
           goto ddone;
         tc_fence_after();
         {
           uint32_t out[32];
-          const uint32_t w[8] = {wcur[0].x, wcur[0].y, wcur[0].z, wcur[0].w,
-                                 wcur[1].x, wcur[1].y, wcur[1].z, wcur[1].w};
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const uint32_t sc = i < 4 ? s_lo : s_hi;
@@ -318,9 +313,6 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(TAFULL(sa)));
-        wcur[0] = wnxt[0];
-        wcur[1] = wnxt[1];
-        have = true;
       }
     }
   ddone:;
@@ -578,7 +570,7 @@ bool prefill_t_applicable(const Problem &p) {
   if (!p.transposed || p.wbits != 4 || p.dtype != WQ_BF16) return false;
   if (p.smode != kPerGroup || p.offset) return false;
   if (p.M < 1 || p.N < 1 || p.K % TK != 0 || p.N % 32 != 0) return false;
-  if (p.group % 32 != 0) return false;
+  if (p.group % 32 != 0 || p.G < 2) return false;  // a stage copies two scale rows
   const void *ptrs[] = {p.x1, p.x2, p.scale, p.bias, p.residual, p.gamma, p.y, p.normOut};
   for (const void *q : ptrs)
     if (!a16(q)) return false;
@@ -628,7 +620,6 @@ cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws, cudaS
   char *wsb = static_cast<char *>(ws);
 
   TArgs args = {};
-  args.wt = static_cast<const uint8_t *>(p.x2);
   args.bias = p.bias; args.gamma = p.gamma; args.y = p.y; args.normOut = p.normOut;
   args.status = reinterpret_cast<uint32_t *>(ws);
   args.counters = reinterpret_cast<uint32_t *>(wsb + plan.cnt_off);
@@ -652,9 +643,9 @@ cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws, cudaS
   if (e != cudaSuccess) return e;
   e = launch_so_prep_t(p, e_col, S16T, s);
   if (e != cudaSuccess) return e;
-  args.e_row = e_row; args.e_col = e_col; args.S16T = S16T;
+  args.e_row = e_row; args.e_col = e_col;
 
-  CUtensorMap tm_x, tm_r;
+  CUtensorMap tm_x, tm_w, tm_s, tm_r;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)p.K, (cuuint64_t)p.M};
     const cuuint64_t strides[1] = {(cuuint64_t)p.K * 2};
@@ -662,6 +653,28 @@ cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws, cudaS
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  {
+    // packed weight rows: (N, K/2) bytes, boxes of 32 bytes x 256 rows, 32-byte swizzle
+    const cuuint64_t dims[2] = {(cuuint64_t)p.K / 2, (cuuint64_t)p.N};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.K / 2};
+    const cuuint32_t box[2] = {TK / 2, TN};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(p.x2), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  {
+    // scale words: (G, N), boxes of 256 columns x 2 rows
+    const cuuint64_t dims[2] = {(cuuint64_t)p.N, (cuuint64_t)p.G};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.N * 4};
+    const cuuint32_t box[2] = {TN, 2};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, S16T, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
@@ -675,7 +688,7 @@ cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws, cudaS
                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  prefill_t_kernel<<<plan.grid, kThreadsT, L::SMEM, s>>>(tm_x, tm_r, args);
+  prefill_t_kernel<<<plan.grid, kThreadsT, L::SMEM, s>>>(tm_x, tm_w, tm_s, tm_r, args);
   return cudaGetLastError();
 }
 
