@@ -6,37 +6,41 @@
 // The product is computed transposed, D^T = W^T x1^T: the dequantized weight
 // is the MMA's A operand and lives in tensor memory, where the dequant warps
 // store it with tcgen05.st; only x1 (the B operand) passes through shared
-// memory. Per 64-deep k-step a CTA moves 16 KB of x1 into shared memory and
-// the MMAs read 32 KB of it -- against ~190 KB of shared-memory traffic when
-// the dequantized weight is the B operand in shared memory.
+// memory. Per 64-deep k-step a CTA moves 32 KB of x1 and 4 KB of packed
+// weights into shared memory and the MMAs read the x1 tile once -- against
+// ~190 KB of shared-memory traffic per k-step of the same work when the
+// dequantized weight is the B operand in shared memory.
 //
-// Output tile: 256 weight columns (two halves of 128 TMEM lanes, MMA M = 128)
-// x 128 rows of x1 (MMA N = 128), tiles in row-block-major order, one
-// persistent CTA per SM. Warp roles (16 warps):
-//   warp 0       TMA producer, per k-step: x1 tile (128 rows x 64, fp16 copy
+// Output tile: 128 weight columns (the 128 TMEM lanes, MMA M = 128) x 256
+// rows of x1 (MMA N = 256), tiles in row-block-major order, one persistent CTA
+// per SM; each dequantized weight element serves 256 rows. Warp roles (16):
+//   warp 0       TMA producer, per k-step: x1 tile (256 rows x 64, fp16 copy
 //                with a per-row power of two, 128-byte swizzle, K-major), the
-//                tile's 256 packed weight rows (32 bytes each, 32-byte swizzle)
+//                tile's 128 packed weight rows (32 bytes each, 32-byte swizzle)
 //                and two rows of scale words.
-//   warp 1       TMEM owner (512 columns: D halves at 0 and 128, four A stages
-//                of 64 columns at 256 + 64 s, half h at + 32 h) and MMA issuer
-//                (kind::f16, A from TMEM, B from shared memory, K = 16).
-//   warps 4-11   dequant: warp (half h, lane quarter q) owns weight rows
-//                n = 128 h + 32 q + lane of the tile; per k-step a thread
-//                reads its row's 32 bytes (64 k) from the stage, forms q * S16 in
-//                fp16 (exact) as 32 columns of (k even, k odd) pairs and stores
-//                them to its TMEM lane. The odd k's nibble is used in place at
-//                bits 7:4 (as 1152 + 16 q, with S16 / 16), the even k's at
-//                bits 3:0 (1032 + q, with S16).
+//   warp 1       TMEM owner (512 columns: D at 0, eight A stages of 32 columns
+//                at 256 + 32 s) and MMA issuer (kind::f16, A from TMEM, B from
+//                shared memory, M = 128, N = 256, K = 16).
+//   warps 4-11   dequant: warp (k half p, lane quarter q) owns weight row
+//                n = 32 q + lane of the tile and k 32 p .. 32 p + 31 of each
+//                k-step: it reads those 16 bytes from the stage, forms q * S16
+//                in fp16 (exact) as 16 columns of (k even, k odd) pairs and
+//                stores them to its TMEM lane. The odd k's nibble is used in
+//                place at bits 7:4 (as 1152 + 16 q, with S16 / 16), the even
+//                k's at bits 3:0 (1032 + q, with S16).
 //   warps 12-15  epilogue, lane quarter q: thread = weight column n, TMEM
 //                columns = rows m. y = acc * 2^(e_m + e_n) + bias + residual,
 //                the residual read as 32 x 32 TMA boxes ([m][n], two ahead), y
 //                written column-wise into a shared box and stored as coalesced
-//                box rows; each warp publishes per-row sums of y^2 over its 64
+//                box rows; each warp forms per-row sums of y^2 over its 32
 //                columns of the tile (a butterfly over the lanes leaves row j's
-//                sum in lane j), four partials per row and n-tile; the
-//                accumulator is handed back once read. Then the previous
-//                tile's rows are normalised a row per warp instruction once
-//                every partial of their row block is published.
+//                sum in lane j) in shared memory, and once all four warps have
+//                (an mbarrier, bounded wait) warp q adds the four in a fixed
+//                order for rows 64 q .. 64 q + 63 and publishes one partial per
+//                row and n-tile; the accumulator is handed back once read.
+//                Then the previous tile's rows (64 per warp) are normalised a
+//                row per warp instruction once every partial of their row
+//                block is published.
 // Every wait is bounded; on timeout the kernel records the place in the
 // status word, drains its copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -54,15 +58,15 @@ namespace {
 
 using namespace sm100;
 
-constexpr int TM = 128, TN = 256, TK = 64;
-constexpr int NRX = 6;  // x1 stages in shared memory
-constexpr int NRA = 4;  // weight stages in tensor memory
+constexpr int TM = 256, TN = 128, TK = 64;
+constexpr int NRX = 4;  // x1 + weight stages in shared memory
+constexpr int NRA = 8;  // weight stages in tensor memory (32 columns each)
 constexpr int kThreadsT = 512;
 constexpr int kDq0 = 4, kDqN = 8, kEpi0 = 12, kEpiN = 4;
 constexpr uint32_t kTmemColsT = 512, kColA = 256;
 constexpr int kNRes = 3;           // residual boxes per epilogue warp
 constexpr uint32_t kBox = 32 * 64; // 32 rows x 32 columns x 2 bytes
-constexpr int kPartsPerLaneT = 20; // row partials read by a normalising lane: 4 per n-tile, <= 160 n-tiles
+constexpr int kPartsPerLaneT = 10; // row partials read by a normalising lane: one per n-tile, <= 296 n-tiles
 
 enum WhereT : uint32_t {
   kTWProducer = 1, kTWMma = 2, kTWDequant = 3, kTWEpi = 4, kTWRowBlock = 5
@@ -82,17 +86,19 @@ struct TArgs {
   uint32_t extra;
 };
 
-// A stage: x1 tile (16 KB, 128-byte swizzle), the tile's packed weight rows
-// (256 rows x 32 bytes, 32-byte swizzle) and two rows of scale words (2 KB).
+// A stage: x1 tile (32 KB, 128-byte swizzle), the tile's packed weight rows
+// (128 rows x 32 bytes, 32-byte swizzle) and two rows of scale words (1 KB).
 struct LayoutT {
-  static constexpr uint32_t X_BYTES = TM * TK * 2;                  // 16 KB
-  static constexpr uint32_t W_BYTES = TN * TK / 2;                  // 8 KB
-  static constexpr uint32_t S_BYTES = 2 * TN * 4;                   // 2 KB
-  static constexpr uint32_t STAGE = X_BYTES + W_BYTES + S_BYTES;    // 26 KB, 1024-aligned
+  static constexpr uint32_t X_BYTES = TM * TK * 2;                  // 32 KB
+  static constexpr uint32_t W_BYTES = TN * TK / 2;                  // 4 KB
+  static constexpr uint32_t S_BYTES = 2 * TN * 4;                   // 1 KB
+  static constexpr uint32_t STAGE = X_BYTES + W_BYTES + S_BYTES;    // 37 KB, 1024-aligned
   static constexpr uint32_t X_OFF = 0;
   static constexpr uint32_t EPI_OFF = X_OFF + NRX * STAGE;          // 1024-aligned
-  static constexpr uint32_t BAR_OFF = EPI_OFF + kEpiN * (kNRes + 1) * kBox;
-  static constexpr int NBARS = 2 * NRX + 2 * NRA + 2 + 1 + kEpiN * kNRes;
+  // per-warp sums of y^2 of the tile's rows, two buffers: float [2][kEpiN][TM]
+  static constexpr uint32_t PART_OFF = EPI_OFF + kEpiN * (kNRes + 1) * kBox;
+  static constexpr uint32_t BAR_OFF = PART_OFF + 2 * kEpiN * TM * 4;
+  static constexpr int NBARS = 2 * NRX + 2 * NRA + 2 + 1 + kEpiN * kNRes + 2;
   static constexpr uint32_t SMEM = BAR_OFF + 8 * NBARS + 16 + 1024;
   static_assert(SMEM <= 232448, "shared memory per CTA");
 };
@@ -105,6 +111,7 @@ struct LayoutT {
 #define TACCEMPTY() (2 * NRX + 2 * NRA + 1)
 #define TDRAIN() (2 * NRX + 2 * NRA + 2)
 #define TRESFULL(q, b) (2 * NRX + 2 * NRA + 3 + kNRes * (q) + (b))
+#define TPARTFULL(b) (2 * NRX + 2 * NRA + 3 + kNRes * kEpiN + (b))
 
 // D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16, A read from tensor memory.
 __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
@@ -117,18 +124,14 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
-// 32 lanes x 32 columns of 32-bit TMEM words from registers: thread i of the
-// warp writes lane (base lane + i), columns col .. col+31.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+// 32 lanes x 16 columns of 32-bit TMEM words from registers.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      "r"(r[15])
       : "memory");
 }
 
@@ -177,6 +180,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     mbar_init(BAR(TDRAIN()), 1);
     for (int q = 0; q < kEpiN; ++q)
       for (int b = 0; b < kNRes; ++b) mbar_init(BAR(TRESFULL(q, b)), 1);
+    mbar_init(BAR(TPARTFULL(0)), kEpiN);
+    mbar_init(BAR(TPARTFULL(1)), kEpiN);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_x);
@@ -221,7 +226,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     {
-      const uint32_t idesc = idesc_f16(0u, 128, TM);  // fp16 x fp16, M = 128 (weight columns), N = 128
+      const uint32_t idesc = idesc_f16(0u, 128, TM);  // fp16 x fp16, M = 128 (weight columns), N = 256
       long long it = 0;
       int lt = 0;
       for (long long t = blockIdx.x; t < a.nTiles; t += gridDim.x, ++lt) {
@@ -239,11 +244,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             const uint32_t xaddr = sbase + L::X_OFF + s * L::STAGE;
 #pragma unroll
             for (int kk = 0; kk < TK / 16; ++kk)
-#pragma unroll
-              for (int h = 0; h < 2; ++h)
-                mma_f16_ts(tmem_base + (uint32_t)(h * TM),
-                           tmem_base + kColA + (uint32_t)(sa * 64 + h * 32 + kk * 8),
-                           desc_kmajor_sw128(xaddr + kk * 32), idesc, (ks | kk) != 0 ? 1u : 0u);
+              mma_f16_ts(tmem_base, tmem_base + kColA + (uint32_t)(sa * 32 + kk * 8),
+                         desc_kmajor_sw128(xaddr + kk * 32), idesc, (ks | kk) != 0 ? 1u : 0u);
             mma_commit(BAR(TXEMPTY(s)));
             mma_commit(BAR(TAEMPTY(sa)));
           }
@@ -260,13 +262,12 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     }
   } else if (warp >= kDq0 && warp < kDq0 + kDqN) {
     // ---------------------------------------------------------------- dequant
-    const int h = (warp - kDq0) >> 2, q = warp & 3;
-    const uint32_t lane_base = tmem_base + ((uint32_t)(32 * q) << 16) + kColA + (uint32_t)(h * 32);
-    const int r = h * 128 + 32 * q + lane;  // weight row of the tile
-    // this row's two 16-byte chunks in the 32-byte-swizzled weight block:
-    // chunk c of row r at r * 32 + 16 (c ^ ((r >> 2) & 1))
-    const uint32_t woff0 = (uint32_t)(r * 32 + 16 * ((r >> 2) & 1));
-    const uint32_t woff1 = (uint32_t)(r * 32 + 16 * (((r >> 2) & 1) ^ 1));
+    const int hp = (warp - kDq0) >> 2, q = warp & 3;  // k half, lane quarter
+    const uint32_t lane_base = tmem_base + ((uint32_t)(32 * q) << 16) + kColA + (uint32_t)(hp * 16);
+    const int r = 32 * q + lane;  // weight row of the tile
+    // this thread's 16-byte chunk hp of the row in the 32-byte-swizzled weight
+    // block: chunk c of row r at r * 32 + 16 (c ^ ((r >> 2) & 1))
+    const uint32_t woff = (uint32_t)(r * 32 + 16 * (hp ^ ((r >> 2) & 1)));
     long long it = 0;
     for (long long t = blockIdx.x; t < a.nTiles; t += gridDim.x) {
       for (int ks = 0; ks < a.kTiles; ++ks, ++it) {
@@ -274,40 +275,36 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         if (!wait_bar_warp(BAR(TXFULL(s)), (uint32_t)((it / NRX) & 1), abort_flag, a.status, kTWDequant))
           goto ddone;
         const uint32_t st = sbase + L::X_OFF + s * L::STAGE;
-        uint32_t w[8];
+        uint32_t w[4];
         asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                      : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                     : "r"(st + L::X_BYTES + woff0));
-        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
-                     : "r"(st + L::X_BYTES + woff1));
-        // scale words of the two 32-deep halves: rows k0 / group and (k0 + 32) / group
-        // of the copied pair (the first is row 0)
+                     : "r"(st + L::X_BYTES + woff));
+        // the scale word of this 32-deep half: row (k0 + 32 hp) / group of the
+        // copied pair, whose first row is k0 / group
         const int k0 = ks * TK;
-        const uint32_t srow1 = (uint32_t)((k0 + 32) / a.group - k0 / a.group);
-        uint32_t s_lo, s_hi;
-        asm volatile("ld.shared.b32 %0, [%1];" : "=r"(s_lo) : "r"(st + L::X_BYTES + L::W_BYTES + 4u * r));
+        const uint32_t srow = (uint32_t)((k0 + 32 * hp) / a.group - k0 / a.group);
+        uint32_t sc;
         asm volatile("ld.shared.b32 %0, [%1];"
-                     : "=r"(s_hi)
-                     : "r"(st + L::X_BYTES + L::W_BYTES + 4u * (srow1 * TN + r)));
+                     : "=r"(sc)
+                     : "r"(st + L::X_BYTES + L::W_BYTES + 4u * (srow * TN + r)));
         if (!wait_bar_warp(BAR(TAEMPTY(sa)), (uint32_t)(((it / NRA) & 1) ^ 1), abort_flag, a.status,
                            kTWDequant))
           goto ddone;
         tc_fence_after();
         {
-          uint32_t out[32];
+          uint32_t out[16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const uint32_t sc = i < 4 ? s_lo : s_hi;
+          for (int i = 0; i < 4; ++i) {
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
               // byte p of word i holds k = 8i + 2p (bits 3:0) and 8i + 2p + 1 (bits 7:4)
+              // of this half
               const uint32_t x = __byte_perm(w[i], 0u, (uint32_t)(p | (p << 8)));
               const uint32_t v = (x & 0x00F0000Fu) ^ 0x64806408u;
               out[4 * i + p] = sub_mul2_h(v, 0x64806408u, sc);
             }
           }
-          tmem_st32(lane_base + (uint32_t)(sa * 64), out);
+          tmem_st16(lane_base + (uint32_t)(sa * 32), out);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -327,6 +324,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     const uint32_t lane_addr = tmem_base + ((uint32_t)(32 * q) << 16);
     const uint32_t rbox = sbase + L::EPI_OFF + (uint32_t)q * (kNRes + 1) * kBox;
     const uint32_t ybox = rbox + (uint32_t)kNRes * kBox;
+    float *part = reinterpret_cast<float *>(smem + L::PART_OFF);
     uint32_t rc = 0, issued = 0;
     int lt = 0;
     long long prev_t = -1;
@@ -354,66 +352,65 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         __syncwarp();
         if (!done) return false;
       }
-      const int n = nt * TN + 8 * lane;
+      // lane l: columns 4 l .. 4 l + 3 of the 128-column tile (8 bytes)
+      const int n = nt * TN + 4 * lane;
       const bool col_ok = n < a.N;
-      uint4 g = make_uint4(0u, 0u, 0u, 0u);
-      if (col_ok) g = *reinterpret_cast<const uint4 *>(gam + n);
-      const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
-      const long long mbase = (long long)rb * TM + 32 * q;
-      const int nparts = 4 * a.nTilesN;
+      uint2 g = make_uint2(0u, 0u);
+      if (col_ok) g = *reinterpret_cast<const uint2 *>(gam + n);
+      const uint32_t gw[2] = {g.x, g.y};
+      const long long mbase = (long long)rb * TM + 64 * q;
 #pragma unroll 1
-      for (int r0 = 0; r0 < 32; r0 += 2) {
-        float pv[2][kPartsPerLaneT];
-        uint4 yv[2];
+      for (int r0 = 0; r0 < 64; r0 += 4) {
+        float pv[4][kPartsPerLaneT];
+        uint2 yv[4];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < 4; ++u) {
           const long long m = mbase + r0 + u;
-          yv[u] = make_uint4(0u, 0u, 0u, 0u);
           const bool live = m < a.M;
-          const float *rp = a.rowpart + m * nparts;
+          const float *rp = a.rowpart + m * a.nTilesN;
 #pragma unroll
           for (int i = 0; i < kPartsPerLaneT; ++i) {
             const int j = lane + 32 * i;
-            pv[u][i] = live && j < nparts ? __ldcg(rp + j) : 0.f;
+            pv[u][i] = live && j < a.nTilesN ? __ldcg(rp + j) : 0.f;
           }
-          if (live && col_ok) yv[u] = __ldcg(reinterpret_cast<const uint4 *>(yin + m * a.N + n));
+          yv[u] = make_uint2(0u, 0u);
+          if (live && col_ok) yv[u] = __ldcg(reinterpret_cast<const uint2 *>(yin + m * a.N + n));
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < 4; ++u) {
+          const long long m = mbase + r0 + u;
           float tot = 0.f;
 #pragma unroll
           for (int i = 0; i < kPartsPerLaneT; ++i) tot += pv[u][i];
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-          const long long m = mbase + r0 + u;
           if (m < a.M && col_ok) {
             const float rstd = rsqrtf(tot / (float)a.N + a.eps);
-            const uint32_t yw[4] = {yv[u].x, yv[u].y, yv[u].z, yv[u].w};
-            uint32_t o4[4];
+            const uint32_t yw[2] = {yv[u].x, yv[u].y};
+            uint32_t o2[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 2; ++i) {
               const float2 y2 = unpack2<WQ_BF16>(yw[i]), g2 = unpack2<WQ_BF16>(gw[i]);
-              o4[i] = pack2<WQ_BF16>(y2.x * rstd * g2.x, y2.y * rstd * g2.y);
+              o2[i] = pack2<WQ_BF16>(y2.x * rstd * g2.x, y2.y * rstd * g2.y);
             }
-            *reinterpret_cast<uint4 *>(nout + m * a.N + n) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+            *reinterpret_cast<uint2 *>(nout + m * a.N + n) = make_uint2(o2[0], o2[1]);
           }
         }
       }
       return true;
     };
 
-    // residual box k of a tile: half h = k / 4, rows 32 (k % 4) of the row
-    // block, this warp's 32 columns of the half
+    // residual box k of a tile: rows 32 (k % 8) of the row block, this warp's
+    // 32 columns of the tile (each tile takes exactly 8 boxes)
     auto load_res = [&](uint32_t k, long long t) {
       issued = k + 1;
       if (lane == 0) {
         const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
-        const int i = (int)(k % 8);  // boxes per tile: 2 halves x 4 row chunks
-        const int hh = i >> 2, c = i & 3;
+        const int c = (int)(k % 8);
         fence_proxy_async_smem();
         const uint32_t bar = BAR(TRESFULL(q, (int)(k % kNRes)));
         mbar_arrive_expect_tx(bar, kBox);
-        tma_load_2d(rbox + (k % kNRes) * kBox, &tm_r, nt * TN + hh * 128 + 32 * q, rb * TM + 32 * c, bar);
+        tma_load_2d(rbox + (k % kNRes) * kBox, &tm_r, nt * TN + 32 * q, rb * TM + 32 * c, bar);
       }
     };
 
@@ -423,95 +420,101 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       load_res(rc0, t);
       load_res(rc0 + 1, t);
       // per-row exponents of this row block: lane j of chunk c holds row 32 c + j
-      int erow[4];
+      int erow[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 8; ++c) {
         const long long m = (long long)rb * TM + 32 * c + lane;
         erow[c] = m < a.M ? (int)a.e_row[m] : 0;
       }
+      const long long n = (long long)nt * TN + 32 * q + lane;
+      const bool col_ok = n < a.N;
+      const int en = col_ok ? (int)a.e_col[n] : 0;
+      const float bv = (bias && col_ok) ? __bfloat162float(bias[n]) : 0.f;
       if (!wait_bar_warp(BAR(TACCFULL()), (uint32_t)(lt & 1), abort_flag, a.status, kTWEpi)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float rsum[4] = {0.f, 0.f, 0.f, 0.f};  // this warp's sums of y^2, row 32 c + lane
 #pragma unroll 1
-      for (int hh = 0; hh < 2 && ok; ++hh) {
-        const long long n = (long long)nt * TN + hh * 128 + 32 * q + lane;
-        const bool col_ok = n < a.N;
-        const int en = col_ok ? (int)a.e_col[n] : 0;
-        const float bv = (bias && col_ok) ? __bfloat162float(bias[n]) : 0.f;
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c, ++rc) {
-          const int i = hh * 4 + c;
-          if (i + 2 < 8) load_res(rc0 + (uint32_t)(i + 2), t);
-          uint32_t r[32];
-          tmem_ld32(lane_addr + (uint32_t)(hh * TM + 32 * c), r);
-          tmem_wait_ld();
-          if (!wait_bar_warp(BAR(TRESFULL(q, (int)(rc % kNRes))), (rc / kNRes) & 1u, abort_flag,
-                             a.status, kTWEpi)) {
-            ok = false;
-            break;
-          }
-          const uint32_t rbx = rbox + (rc % kNRes) * kBox;
-          const int erc = c == 0 ? erow[0] : (c == 1 ? erow[1] : (c == 2 ? erow[2] : erow[3]));
-          float sq[32];
-          __syncwarp();  // every lane has read the previous y box
+      for (int c = 0; c < 8; ++c, ++rc) {
+        if (c + 2 < 8) load_res(rc0 + (uint32_t)(c + 2), t);
+        uint32_t r[32];
+        tmem_ld32(lane_addr + (uint32_t)(32 * c), r);
+        tmem_wait_ld();
+        if (!wait_bar_warp(BAR(TRESFULL(q, (int)(rc % kNRes))), (rc / kNRes) & 1u, abort_flag,
+                           a.status, kTWEpi)) {
+          ok = false;
+          break;
+        }
+        const uint32_t rbx = rbox + (rc % kNRes) * kBox;
+        int erc = erow[0];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int em = __shfl_sync(0xffffffffu, erc, j);
-            uint16_t rr;
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(rr) : "r"(rbx + (uint32_t)(j * 64 + 2 * lane)));
-            const float yv = scale_pow2(__uint_as_float(r[j]), em + en) + bv +
-                             __bfloat162float(__ushort_as_bfloat16(rr));
-            const long long m = (long long)rb * TM + 32 * c + j;
-            sq[j] = (col_ok && m < a.M) ? yv * yv : 0.f;
-            const uint16_t yb = __bfloat16_as_ushort(__float2bfloat16_rn(yv));
-            asm volatile("st.shared.u16 [%0], %1;" ::"r"(ybox + (uint32_t)(j * 64 + 2 * lane)), "h"(yb)
-                         : "memory");
-          }
-          // sums over the warp's 32 columns: a butterfly leaves row j's sum in lane j
+        for (int i = 1; i < 8; ++i) erc = c == i ? erow[i] : erc;
+        float sq[32];
+        __syncwarp();  // every lane has read the previous y box
 #pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) {
+        for (int j = 0; j < 32; ++j) {
+          const int em = __shfl_sync(0xffffffffu, erc, j);
+          uint16_t rr;
+          asm volatile("ld.shared.u16 %0, [%1];" : "=h"(rr) : "r"(rbx + (uint32_t)(j * 64 + 2 * lane)));
+          const float yv = scale_pow2(__uint_as_float(r[j]), em + en) + bv +
+                           __bfloat162float(__ushort_as_bfloat16(rr));
+          const long long m = (long long)rb * TM + 32 * c + j;
+          sq[j] = (col_ok && m < a.M) ? yv * yv : 0.f;
+          const uint16_t yb = __bfloat16_as_ushort(__float2bfloat16_rn(yv));
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(ybox + (uint32_t)(j * 64 + 2 * lane)), "h"(yb)
+                       : "memory");
+        }
+        // sums over the warp's 32 columns: a butterfly leaves row j's sum in lane j
 #pragma unroll
-            for (int k = 0; k < o; ++k) {
-              const bool upper = (lane & o) != 0;
-              const float send = upper ? sq[k] : sq[k + o];
-              const float keep = upper ? sq[k + o] : sq[k];
-              sq[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-            }
-          }
-          if (c == 0) rsum[0] += sq[0];
-          else if (c == 1) rsum[1] += sq[0];
-          else if (c == 2) rsum[2] += sq[0];
-          else rsum[3] += sq[0];
-          __syncwarp();
-          // whole box rows: lanes 4i .. 4i+3 store row 8u + i
+        for (int o = 16; o >= 1; o >>= 1) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int rr = 8 * u + (lane >> 2), jj = lane & 3;
-            const long long my = (long long)rb * TM + 32 * c + rr;
-            const long long ny = (long long)nt * TN + hh * 128 + 32 * q + 8 * jj;
-            uint32_t q0, q1, q2, q3;
-            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(q0), "=r"(q1), "=r"(q2), "=r"(q3)
-                         : "r"(ybox + (uint32_t)(rr * 64 + jj * 16)));
-            if (my < a.M && ny < a.N)
-              *reinterpret_cast<uint4 *>(yout + my * a.N + ny) = make_uint4(q0, q1, q2, q3);
+          for (int k = 0; k < o; ++k) {
+            const bool upper = (lane & o) != 0;
+            const float send = upper ? sq[k] : sq[k + o];
+            const float keep = upper ? sq[k + o] : sq[k];
+            sq[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
           }
+        }
+        part[((lt & 1) * kEpiN + q) * TM + 32 * c + lane] = sq[0];
+        __syncwarp();
+        // whole box rows: lanes 4i .. 4i+3 store row 8u + i
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int rr = 8 * u + (lane >> 2), jj = lane & 3;
+          const long long my = (long long)rb * TM + 32 * c + rr;
+          const long long ny = (long long)nt * TN + 32 * q + 8 * jj;
+          uint32_t q0, q1, q2, q3;
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(q0), "=r"(q1), "=r"(q2), "=r"(q3)
+                       : "r"(ybox + (uint32_t)(rr * 64 + jj * 16)));
+          if (my < a.M && ny < a.N)
+            *reinterpret_cast<uint4 *>(yout + my * a.N + ny) = make_uint4(q0, q1, q2, q3);
         }
       }
       if (!ok) break;
-      // the accumulator has been read: hand it back to the MMA issuer
+      // the accumulator has been read: hand it back to the MMA issuer; this
+      // warp's partial of every row of the tile is published with the count
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(TACCEMPTY()));
-      // this warp's partial of every row of the tile; the row block is complete
-      // when all kEpiN warps of all its n-tiles have published
+      // the four warps' sums of each row, added in warp order; warp q takes
+      // rows 64 q .. 64 q + 63 and publishes them
+      if (lane == 0) mbar_arrive(BAR(TPARTFULL(lt & 1)));
+      if (!wait_bar_warp(BAR(TPARTFULL(lt & 1)), (uint32_t)((lt >> 1) & 1), abort_flag, a.status,
+                         kTWEpi)) {
+        ok = false;
+        break;
+      }
+      {
+        const float *pb = part + (lt & 1) * kEpiN * TM;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const long long m = (long long)rb * TM + 32 * c + lane;
-        if (m < a.M) a.rowpart[(m * a.nTilesN + nt) * 4 + q] = rsum[c];
+        for (int u = 0; u < 2; ++u) {
+          const int ml = 64 * q + 32 * u + lane;
+          const float tot = ((pb[ml] + pb[TM + ml]) + pb[2 * TM + ml]) + pb[3 * TM + ml];
+          const long long m = (long long)rb * TM + ml;
+          if (m < a.M) a.rowpart[m * a.nTilesN + nt] = tot;
+        }
       }
       __syncwarp();
       if (lane == 0) {
@@ -574,8 +577,10 @@ bool prefill_t_applicable(const Problem &p) {
   const void *ptrs[] = {p.x1, p.x2, p.scale, p.bias, p.residual, p.gamma, p.y, p.normOut};
   for (const void *q : ptrs)
     if (!a16(q)) return false;
+  // row-block waits: a CTA normalises tile t - 1 after publishing tile t, so every
+  // wait depends only on smaller tile indices while n-tiles per row <= 2 x grid
   const int64_t nt = (p.N + TN - 1) / TN;
-  if (nt > device_info().sms || nt > 32 * kPartsPerLaneT) return false;
+  if (nt > 2 * device_info().sms || nt > 32 * kPartsPerLaneT) return false;
   return true;
 }
 
@@ -593,7 +598,7 @@ bool plan_prefill_t(const Problem &p, Plan &plan) {
   plan.cnt_off = off;
   off += al256((uint64_t)plan.m_tiles * 4);
   plan.rowpart_off = off;
-  off += al256((uint64_t)p.M * (uint64_t)plan.n_tiles * 4 * sizeof(float));  // per epilogue warp
+  off += al256((uint64_t)p.M * (uint64_t)plan.n_tiles * sizeof(float));
   plan.erow_off = off;
   off += al256((uint64_t)p.M * sizeof(int16_t));
   plan.ecol_off = off;
