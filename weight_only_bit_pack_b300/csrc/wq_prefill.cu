@@ -369,9 +369,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long it = 0;
     const int kAll = a.kTiles + a.kTilesX;
     for (long long t = blockIdx.x; t < a.nTiles; t += gridDim.x) {
-      for (int ks = 0; ks < kAll; ++ks, ++it) {
+      // (ks * BK) % group, kept without a division; the stage's first group row
+      // is (ks * BK) / group, and this thread's k-octet lies in that row or the
+      // next ones: srow = (kmod + 8 ko) / group, at most 2 (group >= 32)
+      int kmod = 0;
+      for (int ks = 0; ks < kAll; ++ks, ++it, kmod += BK) {
+        while (kmod >= a.group && a.group > 0) kmod -= a.group;
         const int s = (int)(it % NR), sb = (int)(it % NB);
         const int k = ks * BK + 8 * ko;
+        const int kk8 = kmod + 8 * ko;
+        const int srow = kk8 < a.group ? 0 : (kk8 < 2 * a.group ? 1 : 2);
         if (ks >= a.kTiles) {
           // offset-term step: no weight to dequantize (the producer copied both
           // operands). The warps still arrive on the raw slot's and the B slot's
@@ -402,8 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (MODE == kF16Emu) {
             if (k < a.K) {
               // columns 8 lane .. 8 lane + 7, stored as words 4 lane .. and 128 + 4 lane ..
-              smem_s<8, 128>(sbase + L::S_OFF + s * L::SO_BYTES, (k / a.group - (ks * BK) / a.group),
-                             4 * lane, s2);
+              smem_s<8, 128>(sbase + L::S_OFF + s * L::SO_BYTES, srow, 4 * lane, s2);
             } else {
 #pragma unroll
               for (int j = 0; j < 8; ++j) s2[j] = 0u;
@@ -451,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             goto ddone;
           if constexpr (MODE == kF16Emu) {
             if (k < a.K) {
-              const int rr = k / a.group - (ks * BK) / a.group;
+              const int rr = srow;
               const uint32_t sa = sbase + L::S_OFF + s * L::SO_BYTES;
               smem_s<4, 4>(sa, rr, 4 * lane, s2a);
               smem_s<4, 4>(sa, rr, 4 * (lane + 32), s2b);
