@@ -92,6 +92,26 @@ CASES = [
                           group=256, offset=False)),
     ("max_n_65520", dict(M_shape=(1,), K=64, N=65520, dtype=torch.bfloat16, mode="group",
                          group=32)),
+    # group-structured loop (K % 128 == 0, group % 128 == 0 or one scale row,
+    # x1 staged in shared memory, >= 8 units of 128 k-rows per warp): groups
+    # of several units with a short last group, per-channel with an odd unit
+    # count, a per-tensor scale with offsets, one column group per CTA, eight
+    # rows with per-group offsets, two row blocks (12 rows)
+    ("m4_group256_short_last", dict(M_shape=(4,), K=16512, N=272, dtype=torch.bfloat16,
+                                    mode="group", group=256)),
+    ("m2_channel_odd_units", dict(M_shape=(2,), K=16256, N=4800, dtype=torch.float16,
+                                  mode="channel")),
+    ("m5_tensor_offset_k8192", dict(M_shape=(5,), K=8192, N=4096, dtype=torch.float16,
+                                    mode="tensor")),
+    ("m3_group384_one_group_per_cta", dict(M_shape=(3,), K=19200, N=96, dtype=torch.float16,
+                                           mode="group", group=384)),
+    ("m8_group128_offset_n8192", dict(M_shape=(8,), K=8192, N=8192, dtype=torch.bfloat16,
+                                      mode="group", group=128)),
+    ("m12_group128_two_row_blocks", dict(M_shape=(12,), K=4096, N=8192, dtype=torch.bfloat16,
+                                         mode="group", group=128, offset=False)),
+    # the general loop with 16 rows, offsets and x1 read from global memory
+    ("m16_group128_offset_k8192", dict(M_shape=(16,), K=8192, N=512, dtype=torch.bfloat16,
+                                       mode="group", group=128)),
 ]
 
 

@@ -46,6 +46,7 @@ using namespace sm100;
 constexpr int TW = 16;              // warps per CTA
 constexpr int TTHREADS = TW * 32;
 constexpr int TSL = 2;              // pairs a warp's run can touch
+constexpr int TSLG = 3;             // group-structured loop: column groups a run can touch
 constexpr uint32_t kTGbarOff = 128; // header: grid counters (arrive, depart)
 enum TWhere : uint32_t { kTWhereGrid = 15 };
 constexpr int kTParts = 5;          // per-CTA partial sums a lane reads: grid <= 160
@@ -58,6 +59,8 @@ struct DTArgs {
   uint32_t *status, *gbar;
   float *ss;          // G x 16 per-CTA sums of y^2
   int M, K, N, KS, NCG, group, Ns, G;
+  int gu, GV;         // group-structured loop: k-steps per group, groups along K
+  int G_rows;         // scale rows (ceil(K / group) per-group, else 1)
   float eps;
   long long budget;
   uint32_t extra;
@@ -83,8 +86,38 @@ __device__ __forceinline__ void word_to_a(uint32_t w, uint32_t (&a)[4]) {
   for (int i = 0; i < 4; ++i) a[i] = ((i ? w >> (4 * i) : w) & 0x000F000Fu) ^ MAGIC;
 }
 
-template <int DT, int MT, bool HAS_O, int TD, bool KFULL, bool XSMEM>
+// The same MMA without `volatile`, so the compiler may interleave it with the
+// conversions around it.
+template <bool BF>
+__device__ __forceinline__ void mma_16816_f(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                            uint32_t b1) {
+  if constexpr (BF)
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  else
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// The low (hi = false) or high 16-bit float of a pair, as fp32.
+template <int DT>
+__device__ __forceinline__ float half_to_f(uint32_t u, bool hi) {
+  if constexpr (DT == WQ_BF16)
+    return __uint_as_float(hi ? u & 0xFFFF0000u : u << 16);
+  else
+    return __half2float(__ushort_as_half((unsigned short)(hi ? u >> 16 : u & 0xFFFFu)));
+}
+
+// GRP: the group-structured main loop (K % 64 == 0 and scale groups of whole
+// 64-row k-steps, or one scale row cut into groups of two k-steps). Otherwise
+// the general loop: 32-row blocks, any group that is a multiple of 32, any K.
+template <int DT, int MT, bool HAS_O, int TD, bool KFULL, bool XSMEM, bool GRP>
 __global__ void __launch_bounds__(TTHREADS, 1) decode_tiled_kernel(const DTArgs a) {
+  static_assert(!GRP || KFULL, "the group-structured loop needs K % 64 == 0");
   constexpr int TRING = TD + 1;  // scale ring slots per warp
   using E = Elem<DT>;
   using T = typename E::T;
@@ -108,10 +141,17 @@ __global__ void __launch_bounds__(TTHREADS, 1) decode_tiled_kernel(const DTArgs 
   // XSMEM: the M rows of x1, row pitch 2K + 64 bytes (16-byte aligned, and the
   // 8 rows a warp reads at once fall in distinct bank groups)
   const uint32_t xpitch = 2u * (uint32_t)a.K + 64u;
-  uint8_t *xsm = reinterpret_cast<uint8_t *>(
+  // GRP: the x1 row sums of every group, [GV][MP], and the CTA's scale (then
+  // offset) rows, [G_rows][ncg_max * 16] each
+  float *dsm = reinterpret_cast<float *>(
       (reinterpret_cast<uintptr_t>(kblk + (a.K + 31) / 32) + 15) & ~static_cast<uintptr_t>(15));
+  T *ssm = reinterpret_cast<T *>(
+      (reinterpret_cast<uintptr_t>(dsm + (GRP ? a.GV * MP : 0)) + 15) & ~static_cast<uintptr_t>(15));
+  const size_t ssm_elems = GRP ? (size_t)(a.Ns == 1 ? 0 : a.G_rows) * ncg_max * 16 * (HAS_O ? 2 : 1) : 0;
+  uint8_t *xsm = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(ssm + ssm_elems) + 15) & ~static_cast<uintptr_t>(15));
   __shared__ __align__(8) uint64_t s_xbar;
-  __shared__ int s_tag[TW][TSL];
+  __shared__ int s_tag[TW][TSLG];
   __shared__ float s_rstd[16];
   __shared__ int s_abort;
 
@@ -127,7 +167,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) decode_tiled_kernel(const DTArgs 
   const T *x1 = static_cast<const T *>(a.x1);
   const size_t slab = (size_t)a.NCG * 512;  // bytes of one 64-row slab of tiles
 
-  if (threadIdx.x < TW * TSL) s_tag[threadIdx.x / TSL][threadIdx.x % TSL] = -1;
+  if (threadIdx.x < TW * TSLG) s_tag[threadIdx.x / TSLG][threadIdx.x % TSLG] = -1;
   if (threadIdx.x == 0) s_abort = 0;
   for (int j = threadIdx.x; j < (a.K + 31) / 32; j += TTHREADS) {
     const int k0 = 32 * j;
@@ -166,6 +206,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) decode_tiled_kernel(const DTArgs 
                     smem_u32(&s_xbar));
   }
 
+  if constexpr (!GRP) {
   // ---- unit (pair p, k-step s), fetched TD units ahead of its use: the lane's
   // 16 bytes of the pair's two tiles, an L1 prefetch of the activation lines
   // the unit will read (rows g and 8 + g, k-rows 64s..64s+63), and the scale
@@ -381,6 +422,224 @@ __global__ void __launch_bounds__(TTHREADS, 1) decode_tiled_kernel(const DTArgs 
   }
   if (pend_slot >= 0) flush(pend_slot, pend_h);
   if (cur_p >= 0) store_pair(cur_p, slot_i);
+  } else {
+  // ---- group-structured loop. A unit is one column group at two k-steps
+  // (two 512-byte tiles, 128 k-rows); a group of scales is a whole number of
+  // units (group % 128 == 0; per-channel and per-tensor scales are cut into
+  // groups of one unit). Items (column group, group) in column-group-major
+  // order are dealt to the warps in contiguous runs, at most three column
+  // groups long (ncg <= 32), so no group's sums are split between warps and a
+  // warp folds them at the group's last unit: tot += S (acc0 + acc1) +
+  // (O - 136 S) d, with d the group's x1 row sums (computed once per CTA
+  // below) and S, O from the CTA's scale block, staged in shared memory at the
+  // start. Per unit: two 16-byte weight loads (TD units ahead), four 16-byte
+  // activation loads from the staged x1, eight words into A registers and
+  // eight MMAs (one chain per k-step).
+  const int ncg = cg1 - cg0;
+  const int KS2 = a.KS >> 1;
+  const int ug = a.gu >> 1;  // units per group
+  const int UG = ncg * a.GV;
+  auto unit_of = [&](int item) {
+    const int c = item / a.GV, q = item - c * a.GV;
+    return c * KS2 + (q * ug < KS2 ? q * ug : KS2);
+  };
+  const int r0 = unit_of((int)((long long)UG * warp / TW));
+  const int r1 = unit_of((int)((long long)UG * (warp + 1) / TW));
+  // this lane's activation rows 8 mt + g at k-offset 8t (rows past M repeat
+  // row M - 1; their outputs are never stored)
+  const T *xrow[MT];
+  uint32_t xsrow[MT];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    const int m = 8 * mt + g < a.M ? 8 * mt + g : a.M - 1;
+    xrow[mt] = x1 + (size_t)m * a.K + 8 * t;
+    xsrow[mt] = smem_u32(xsm) + (uint32_t)m * xpitch + 16u * (uint32_t)t;
+  }
+  // the lane's 16 bytes of k-step ks, k-rows 32h.. of the step
+  auto load_x = [&](int ks, uint4 (&xb)[MT][2]) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if constexpr (XSMEM)
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(xb[mt][h].x), "=r"(xb[mt][h].y), "=r"(xb[mt][h].z), "=r"(xb[mt][h].w)
+                       : "r"(xsrow[mt] + (uint32_t)(128 * ks + 64 * h)));
+        else
+          xb[mt][h] = __ldg(reinterpret_cast<const uint4 *>(xrow[mt] + 64 * ks + 32 * h));
+      }
+  };
+
+  // the CTA's scale (offset) rows for its columns, [row][16 ncg] (rows: the
+  // groups, or one per-channel row; none for a per-tensor scale)
+  const int srows = a.Ns == 1 ? 0 : (a.group ? a.G_rows : 1);
+  {
+    const int cpr = 2 * ncg;  // 16-byte chunks per row
+    const T *sg = static_cast<const T *>(a.scale), *og = static_cast<const T *>(a.offset);
+    for (int i = threadIdx.x; i < srows * cpr; i += TTHREADS) {
+      const int r = i / cpr, q = i - r * cpr;
+      cp_async16(smem_u32(ssm + (size_t)r * ncols + 8 * q), sg + (size_t)r * a.N + 16 * cg0 + 8 * q);
+      if constexpr (HAS_O)
+        cp_async16(smem_u32(ssm + (size_t)(srows + r) * ncols + 8 * q),
+                   og + (size_t)r * a.N + 16 * cg0 + 8 * q);
+    }
+    cp_async_commit();
+  }
+
+  // weights: the fetch walk over units (fcl, fj)
+  int fcl = r0 / KS2, fj = r0 - fcl * KS2;
+  const uint8_t *fwp = a.w + (size_t)(2 * fj) * slab + (size_t)(cg0 + fcl) * 512 + lane * 16;
+  auto fetch = [&](uint4 (&wb)[2]) {
+    wb[0] = ld_stream_u4(fwp);
+    wb[1] = ld_stream_u4(fwp + slab);
+    if (!XSMEM && t < 2) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)  // first and last byte of the row's 256: two to four lines
+        asm volatile("prefetch.global.L1 [%0];" ::"l"(
+            reinterpret_cast<const char *>(xrow[mt] - 8 * t + 128 * fj) + 255 * t));
+    }
+    fwp += 2 * slab;
+    if (++fj == KS2) {
+      fj = 0;
+      ++fcl;
+      fwp = a.w + (size_t)(cg0 + fcl) * 512 + lane * 16;
+    }
+  };
+  uint4 wb[TD][2];
+#pragma unroll
+  for (int i = 0; i < TD; ++i)
+    if (r0 + i < r1) fetch(wb[i]);
+
+  if (XSMEM) {  // the staged x1 has landed (bounded wait; the copy always completes)
+    const long long t0 = clock64();
+    while (!mbar_try_wait(smem_u32(&s_xbar), 0u))
+      if (clock64() - t0 > kWaitBudget) break;
+  }
+  constexpr uint32_t ONES = BF ? 0x3F803F80u : 0x3C003C00u;
+  const uint32_t ONES4[4] = {ONES, ONES, ONES, ONES};
+  // d[gq][m] = sum of x1[m, k] over group gq's k-rows, by MMAs with A = ones
+  // (rows of D are equal; lanes 0..3 hold rows 2t and 2t + 1 of each block)
+  for (int gq = warp; gq < a.GV; gq += TW) {
+    float dd[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dd[mt][i] = 0.f;
+    const int ks1 = (gq + 1) * a.gu < a.KS ? (gq + 1) * a.gu : a.KS;
+    for (int ks = gq * a.gu; ks < ks1; ++ks) {
+      uint4 xb[MT][2];
+      load_x(ks, xb);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          mma_16816_f<BF>(dd[mt], ONES4, xb[mt][h].x, xb[mt][h].y);
+          mma_16816_f<BF>(dd[mt], ONES4, xb[mt][h].z, xb[mt][h].w);
+        }
+    }
+    if (g == 0) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+        *reinterpret_cast<float2 *>(dsm + gq * MP + 8 * mt + 2 * t) = make_float2(dd[mt][0], dd[mt][1]);
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();  // row sums and the scale block are in shared memory
+
+  float acc[2][MT][4], tot[MT][4];
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[q][mt][i] = tot[mt][i] = 0.f;
+  const float sscal = a.Ns == 1 ? E::to_f(static_cast<const T *>(a.scale)[0]) : 0.f;
+  const float oscal = (HAS_O && a.Ns == 1) ? E::to_f(static_cast<const T *>(a.offset)[0]) : 0.f;
+  constexpr float C136 = BF ? 136.f : 1032.f;  // A = C136 + q
+
+  // tot += S (acc0 + acc1) + (O - 136 S) d for group gq of column group cl
+  auto fold = [&](int gq, int cl) {
+    float2 dd[MT];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+      dd[mt] = *reinterpret_cast<const float2 *>(dsm + gq * MP + 8 * mt + 2 * t);
+    float sl = sscal, shi = sscal, ol = oscal, ohi = oscal;
+    if (srows) {
+      const T *sr = ssm + (size_t)(a.group ? gq : 0) * ncols + 16 * cl + g;
+      sl = E::to_f(sr[0]);
+      shi = E::to_f(sr[8]);
+      if constexpr (HAS_O) {
+        ol = E::to_f(sr[(size_t)srows * ncols]);
+        ohi = E::to_f(sr[(size_t)srows * ncols + 8]);
+      }
+    }
+    const float cl0 = fmaf(-C136, sl, ol), ch0 = fmaf(-C136, shi, ohi);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      tot[mt][0] = fmaf(cl0, dd[mt].x, fmaf(sl, acc[0][mt][0] + acc[1][mt][0], tot[mt][0]));
+      tot[mt][1] = fmaf(cl0, dd[mt].y, fmaf(sl, acc[0][mt][1] + acc[1][mt][1], tot[mt][1]));
+      tot[mt][2] = fmaf(ch0, dd[mt].x, fmaf(shi, acc[0][mt][2] + acc[1][mt][2], tot[mt][2]));
+      tot[mt][3] = fmaf(ch0, dd[mt].y, fmaf(shi, acc[0][mt][3] + acc[1][mt][3], tot[mt][3]));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[0][mt][i] = acc[1][mt][i] = 0.f;
+    }
+  };
+  // the run's sums of column group cl into slot sl of this warp, then cleared
+  auto store_cg = [&](int cl, int sl) {
+    float *dst = part + (size_t)(warp * TSLG + sl) * (MP * 16);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int m = 8 * mt + 2 * t + (i & 1), col = g + 8 * (i >> 1);
+        dst[m * 16 + col] = tot[mt][i];
+        tot[mt][i] = 0.f;
+      }
+    if (lane == 0) s_tag[warp][sl] = cl;
+  };
+
+  int cl = r0 / KS2, j = r0 - cl * KS2, slot_i = 0;
+  int gq = j / ug;                           // the open group (runs start at a group's first unit)
+  int ul = ug < KS2 - j ? ug : KS2 - j;      // its units left
+  for (int u0 = r0; u0 < r1; u0 += TD) {
+#pragma unroll
+    for (int i = 0; i < TD; ++i) {
+      const int u = u0 + i;
+      if (u >= r1) break;
+      const uint4 wq[2] = {wb[i][0], wb[i][1]};
+      uint4 xb[2][MT][2];
+      load_x(2 * j, xb[0]);
+      load_x(2 * j + 1, xb[1]);
+      if (u + TD < r1) fetch(wb[i]);
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int h = jj >> 1, jl = jj & 1;
+          uint32_t aa[4];
+          word_to_a<DT>(jj == 0 ? wq[q].x : jj == 1 ? wq[q].y : jj == 2 ? wq[q].z : wq[q].w, aa);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+            mma_16816_f<BF>(acc[q][mt], aa, jl ? xb[q][mt][h].z : xb[q][mt][h].x,
+                            jl ? xb[q][mt][h].w : xb[q][mt][h].y);
+        }
+      ++j;
+      if (--ul == 0) {  // the group ends with this unit
+        fold(gq, cl);
+        ++gq;
+        if (j == KS2) {  // and so does the column group
+          store_cg(cl, slot_i);
+          ++slot_i;
+          ++cl;
+          j = 0;
+          gq = 0;
+        }
+        ul = ug < KS2 - j ? ug : KS2 - j;
+      }
+    }
+  }
+  if (r0 < r1 && j != 0) store_cg(cl, slot_i);  // the run ended inside a column group
+  }
   cp_async_wait<0>();
   __syncthreads();
 
@@ -392,14 +651,25 @@ __global__ void __launch_bounds__(TTHREADS, 1) decode_tiled_kernel(const DTArgs 
     const int m = e / npair, col = 2 * (e - m * npair);
     const int cl = col >> 4, p = cl >> 1, c = cl & 1, cc = col & 15;
     float v0 = 0.f, v1 = 0.f;
-    for (int w = 0; w < TW; ++w)
+    if constexpr (GRP) {  // slots of one column group, [MP][16]
+      for (int w = 0; w < TW; ++w)
 #pragma unroll
-      for (int sl = 0; sl < TSL; ++sl)
-        if (s_tag[w][sl] == p) {
-          const float *src = part + (size_t)(w * TSL + sl) * SLOT_FLOATS + (c * MP + m) * 16 + cc;
-          v0 += src[0];
-          v1 += src[1];
-        }
+        for (int sl = 0; sl < TSLG; ++sl)
+          if (s_tag[w][sl] == cl) {
+            const float *src = part + (size_t)(w * TSLG + sl) * (MP * 16) + m * 16 + cc;
+            v0 += src[0];
+            v1 += src[1];
+          }
+    } else {  // slots of one pair, [2][MP][16]
+      for (int w = 0; w < TW; ++w)
+#pragma unroll
+        for (int sl = 0; sl < TSL; ++sl)
+          if (s_tag[w][sl] == p) {
+            const float *src = part + (size_t)(w * TSL + sl) * SLOT_FLOATS + (c * MP + m) * 16 + cc;
+            v0 += src[0];
+            v1 += src[1];
+          }
+    }
     const int n = 16 * cg0 + col;
     const float2 bb = a.bias ? unpack2<DT>(*reinterpret_cast<const uint32_t *>(ebias + col))
                              : make_float2(0.f, 0.f);
@@ -489,13 +759,29 @@ int tiled_grid_size(const Problem &p) {
 
 constexpr int kTD = 4;  // units in flight per warp
 
-// Shared memory of one CTA; with `xsmem` the staged x1 rows too.
-uint64_t tiled_smem(const Problem &p, int G, bool xsmem) {
+// The group-structured loop applies: whole 64-row k-steps, and scale groups of
+// whole k-steps (or one scale row, cut into groups of two k-steps).
+bool tiled_grp(const Problem &p) { return p.K % 128 == 0 && (p.group == 0 || p.group % 128 == 0); }
+int tiled_gu(const Problem &p) { return tiled_grp(p) ? (p.group ? (int)(p.group / 64) : 2) : 0; }
+int tiled_gv(const Problem &p) {
+  if (!tiled_grp(p)) return 0;
+  const int ks = (int)(p.K / 64), gu = tiled_gu(p);
+  return (ks + gu - 1) / gu;
+}
+
+// Shared memory of one CTA; with `xsmem` the staged x1 rows too, with `grp`
+// the group-structured loop's row sums and scale block.
+uint64_t tiled_smem(const Problem &p, int G, bool xsmem, bool grp) {
   const int MT = p.M <= 8 ? 1 : 2;
   const int64_t ncg_max = (p.N / 16 + G - 1) / G;
   uint64_t b = (uint64_t)TW * TSL * 2 * (8 * MT) * 16 * 4 + (uint64_t)TW * (kTD + 1) * 256 +
                (uint64_t)(8 * MT) * ncg_max * 16 * 4 + (uint64_t)(p.M + 2) * ncg_max * 16 * 2 +
                (uint64_t)(p.K + 31) / 32 * 2;
+  if (grp) {
+    const uint64_t srows = p.Ns == 1 ? 0 : (uint64_t)p.G;  // G = 1 unless per-group
+    b += 16 + (uint64_t)tiled_gv(p) * (8 * MT) * 4;
+    b += 16 + srows * (uint64_t)ncg_max * 16 * 2 * (p.offset ? 2 : 1);
+  }
   if (xsmem) b += 16 + (uint64_t)p.M * (2 * (uint64_t)p.K + 64);
   return b;
 }
@@ -515,7 +801,7 @@ bool decode_tiled_applicable(const Problem &p) {
   const int G = tiled_grid_size(p);
   const int64_t ncg_max = (p.N / 16 + G - 1) / G;
   if (ncg_max > 32) return false;
-  return tiled_smem(p, G, false) + 2048 <= (uint64_t)device_info().smem_optin;
+  return tiled_smem(p, G, false, false) + 2048 <= (uint64_t)device_info().smem_optin;
 }
 
 bool plan_decode_tiled(const Problem &p, Plan &plan) {
@@ -526,16 +812,14 @@ bool plan_decode_tiled(const Problem &p, Plan &plan) {
   return true;
 }
 
-template <int DT, int MT, bool HAS_O, bool KFULL, bool XSMEM>
+template <int DT, int MT, bool HAS_O, bool KFULL, bool XSMEM, bool GRP>
 static cudaError_t launch_decode_tiled_k(const Problem &p, const Plan &plan, void *ws,
                                          cudaStream_t s) {
   const int G = plan.grid;
-  const int64_t ncg_max = (p.N / 16 + G - 1) / G;
-  (void)ncg_max;
-  const uint32_t smem = (uint32_t)tiled_smem(p, G, XSMEM);
+  const uint32_t smem = (uint32_t)tiled_smem(p, G, XSMEM, GRP);
   // the cap leaves room for the kernel's few static shared variables
   static cudaError_t attr_err = cudaFuncSetAttribute(
-      decode_tiled_kernel<DT, MT, HAS_O, kTD, KFULL, XSMEM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      decode_tiled_kernel<DT, MT, HAS_O, kTD, KFULL, XSMEM, GRP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       (int)device_info().smem_optin - 2048);
   if (attr_err != cudaSuccess) return attr_err;
   char *wsb = static_cast<char *>(ws);
@@ -549,6 +833,8 @@ static cudaError_t launch_decode_tiled_k(const Problem &p, const Plan &plan, voi
   args.M = (int)p.M; args.K = (int)p.K; args.N = (int)p.N;
   args.KS = (int)((p.K + 63) / 64); args.NCG = (int)(p.N / 16);
   args.group = (int)p.group; args.Ns = (int)p.Ns; args.G = G;
+  args.gu = tiled_gu(p); args.GV = tiled_gv(p);
+  args.G_rows = (int)p.G;
   args.eps = p.eps;
   args.budget = wait_budget();
   args.extra = wait_extra_arrivals();
@@ -562,7 +848,7 @@ static cudaError_t launch_decode_tiled_k(const Problem &p, const Plan &plan, voi
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tiled_kernel<DT, MT, HAS_O, kTD, KFULL, XSMEM>, args);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tiled_kernel<DT, MT, HAS_O, kTD, KFULL, XSMEM, GRP>, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -572,12 +858,18 @@ static cudaError_t launch_decode_tiled_t(const Problem &p, const Plan &plan, voi
                                          cudaStream_t s) {
   // x1 staged in shared memory when it fits beside the rest (2 KB of static
   // shared variables are kept free)
-  const bool xs = tiled_smem(p, plan.grid, true) + 2048 <= (uint64_t)device_info().smem_optin;
+  const uint64_t cap = (uint64_t)device_info().smem_optin - 2048;
+  // the group-structured loop (x1 staged; at least 8 units per warp: with
+  // fewer, its per-CTA preparation outweighs the leaner loop)
+  const int64_t ncg_max = (p.N / 16 + plan.grid - 1) / plan.grid;
+  if (tiled_grp(p) && ncg_max * (p.K / 128) >= 8 * TW && tiled_smem(p, plan.grid, true, true) <= cap)
+    return launch_decode_tiled_k<DT, MT, HAS_O, true, true, true>(p, plan, ws, s);
+  const bool xs = tiled_smem(p, plan.grid, true, false) <= cap;
   if (p.K % 64 == 0)
-    return xs ? launch_decode_tiled_k<DT, MT, HAS_O, true, true>(p, plan, ws, s)
-              : launch_decode_tiled_k<DT, MT, HAS_O, true, false>(p, plan, ws, s);
-  return xs ? launch_decode_tiled_k<DT, MT, HAS_O, false, true>(p, plan, ws, s)
-            : launch_decode_tiled_k<DT, MT, HAS_O, false, false>(p, plan, ws, s);
+    return xs ? launch_decode_tiled_k<DT, MT, HAS_O, true, true, false>(p, plan, ws, s)
+              : launch_decode_tiled_k<DT, MT, HAS_O, true, false, false>(p, plan, ws, s);
+  return xs ? launch_decode_tiled_k<DT, MT, HAS_O, false, true, false>(p, plan, ws, s)
+            : launch_decode_tiled_k<DT, MT, HAS_O, false, false, false>(p, plan, ws, s);
 }
 
 cudaError_t launch_decode_tiled(const Problem &p, const Plan &plan, void *ws, cudaStream_t s) {
