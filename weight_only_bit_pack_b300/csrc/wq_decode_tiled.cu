@@ -103,19 +103,28 @@ __device__ __forceinline__ void mma_16816_f(float (&d)[4], const uint32_t (&a)[4
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// The low (hi = false) or high 16-bit float of a pair, as fp32.
-template <int DT>
-__device__ __forceinline__ float half_to_f(uint32_t u, bool hi) {
-  if constexpr (DT == WQ_BF16)
-    return __uint_as_float(hi ? u & 0xFFFF0000u : u << 16);
+// mma_16816_f with a zero accumulator input.
+template <bool BF>
+__device__ __forceinline__ void mma_16816_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                            uint32_t b1) {
+  const float z = 0.f;
+  if constexpr (BF)
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
   else
-    return __half2float(__ushort_as_half((unsigned short)(hi ? u >> 16 : u & 0xFFFFu)));
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
 }
 
-// GRP: the group-structured main loop (K % 64 == 0 and scale groups of whole
-// 64-row k-steps, or one scale row cut into groups of two k-steps). Otherwise
+// GRP: the group-structured main loop (K % 128 == 0 and scale groups of whole
+// 128-row units, or one scale row cut into groups of one unit); UG1: one unit
+// per group, so every unit starts its sums from zero and folds them. Otherwise
 // the general loop: 32-row blocks, any group that is a multiple of 32, any K.
-template <int DT, int MT, bool HAS_O, int TD, bool KFULL, bool XSMEM, bool GRP>
+template <int DT, int MT, bool HAS_O, int TD, bool KFULL, bool XSMEM, bool GRP, bool UG1 = false>
 __global__ void __launch_bounds__(TTHREADS, 1) decode_tiled_kernel(const DTArgs a) {
   static_assert(!GRP || KFULL, "the group-structured loop needs K % 64 == 0");
   constexpr int TRING = TD + 1;  // scale ring slots per warp
@@ -580,8 +589,10 @@ __global__ void __launch_bounds__(TTHREADS, 1) decode_tiled_kernel(const DTArgs 
       tot[mt][1] = fmaf(cl0, dd[mt].y, fmaf(sl, acc[0][mt][1] + acc[1][mt][1], tot[mt][1]));
       tot[mt][2] = fmaf(ch0, dd[mt].x, fmaf(shi, acc[0][mt][2] + acc[1][mt][2], tot[mt][2]));
       tot[mt][3] = fmaf(ch0, dd[mt].y, fmaf(shi, acc[0][mt][3] + acc[1][mt][3], tot[mt][3]));
+      if constexpr (!UG1) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[0][mt][i] = acc[1][mt][i] = 0.f;
+        for (int i = 0; i < 4; ++i) acc[0][mt][i] = acc[1][mt][i] = 0.f;
+      }
     }
   };
   // the run's sums of column group cl into slot sl of this warp, then cleared
@@ -601,42 +612,52 @@ __global__ void __launch_bounds__(TTHREADS, 1) decode_tiled_kernel(const DTArgs 
   int cl = r0 / KS2, j = r0 - cl * KS2, slot_i = 0;
   int gq = j / ug;                           // the open group (runs start at a group's first unit)
   int ul = ug < KS2 - j ? ug : KS2 - j;      // its units left
-  for (int u0 = r0; u0 < r1; u0 += TD) {
+  // one unit from wb[i]; its slot is refilled (TD units ahead) after use
+  auto unit = [&](uint4 (&wbi)[2], bool refill) {
+    uint4 xb[2][MT][2];
+    load_x(2 * j, xb[0]);
+    load_x(2 * j + 1, xb[1]);
 #pragma unroll
-    for (int i = 0; i < TD; ++i) {
-      const int u = u0 + i;
-      if (u >= r1) break;
-      const uint4 wq[2] = {wb[i][0], wb[i][1]};
-      uint4 xb[2][MT][2];
-      load_x(2 * j, xb[0]);
-      load_x(2 * j + 1, xb[1]);
-      if (u + TD < r1) fetch(wb[i]);
+    for (int q = 0; q < 2; ++q)
 #pragma unroll
-      for (int q = 0; q < 2; ++q)
+      for (int jj = 0; jj < 4; ++jj) {
+        const int h = jj >> 1, jl = jj & 1;
+        uint32_t aa[4];
+        word_to_a<DT>(jj == 0 ? wbi[q].x : jj == 1 ? wbi[q].y : jj == 2 ? wbi[q].z : wbi[q].w, aa);
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int h = jj >> 1, jl = jj & 1;
-          uint32_t aa[4];
-          word_to_a<DT>(jj == 0 ? wq[q].x : jj == 1 ? wq[q].y : jj == 2 ? wq[q].z : wq[q].w, aa);
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
-            mma_16816_f<BF>(acc[q][mt], aa, jl ? xb[q][mt][h].z : xb[q][mt][h].x,
-                            jl ? xb[q][mt][h].w : xb[q][mt][h].y);
+        for (int mt = 0; mt < MT; ++mt) {
+          const uint32_t b0 = jl ? xb[q][mt][h].z : xb[q][mt][h].x;
+          const uint32_t b1 = jl ? xb[q][mt][h].w : xb[q][mt][h].y;
+          if (UG1 && jj == 0)
+            mma_16816_z<BF>(acc[q][mt], aa, b0, b1);
+          else
+            mma_16816_f<BF>(acc[q][mt], aa, b0, b1);
         }
-      ++j;
-      if (--ul == 0) {  // the group ends with this unit
-        fold(gq, cl);
-        ++gq;
-        if (j == KS2) {  // and so does the column group
-          store_cg(cl, slot_i);
-          ++slot_i;
-          ++cl;
-          j = 0;
-          gq = 0;
-        }
-        ul = ug < KS2 - j ? ug : KS2 - j;
       }
+    if (refill) fetch(wbi);
+    ++j;
+    if (--ul == 0) {  // the group ends with this unit
+      fold(gq, cl);
+      ++gq;
+      if (j == KS2) {  // and so does the column group
+        store_cg(cl, slot_i);
+        ++slot_i;
+        ++cl;
+        j = 0;
+        gq = 0;
+      }
+      ul = ug < KS2 - j ? ug : KS2 - j;
     }
+  };
+  int u0 = r0;
+  for (; u0 + 2 * TD <= r1; u0 += TD) {  // every refill in range
+#pragma unroll
+    for (int i = 0; i < TD; ++i) unit(wb[i], true);
+  }
+  for (; u0 < r1; u0 += TD) {
+#pragma unroll
+    for (int i = 0; i < TD; ++i)
+      if (u0 + i < r1) unit(wb[i], u0 + i + TD < r1);
   }
   if (r0 < r1 && j != 0) store_cg(cl, slot_i);  // the run ended inside a column group
   }
@@ -812,14 +833,14 @@ bool plan_decode_tiled(const Problem &p, Plan &plan) {
   return true;
 }
 
-template <int DT, int MT, bool HAS_O, bool KFULL, bool XSMEM, bool GRP>
+template <int DT, int MT, bool HAS_O, bool KFULL, bool XSMEM, bool GRP, bool UG1 = false>
 static cudaError_t launch_decode_tiled_k(const Problem &p, const Plan &plan, void *ws,
                                          cudaStream_t s) {
   const int G = plan.grid;
   const uint32_t smem = (uint32_t)tiled_smem(p, G, XSMEM, GRP);
   // the cap leaves room for the kernel's few static shared variables
   static cudaError_t attr_err = cudaFuncSetAttribute(
-      decode_tiled_kernel<DT, MT, HAS_O, kTD, KFULL, XSMEM, GRP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      decode_tiled_kernel<DT, MT, HAS_O, kTD, KFULL, XSMEM, GRP, UG1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
       (int)device_info().smem_optin - 2048);
   if (attr_err != cudaSuccess) return attr_err;
   char *wsb = static_cast<char *>(ws);
@@ -848,7 +869,7 @@ static cudaError_t launch_decode_tiled_k(const Problem &p, const Plan &plan, voi
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tiled_kernel<DT, MT, HAS_O, kTD, KFULL, XSMEM, GRP>, args);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_tiled_kernel<DT, MT, HAS_O, kTD, KFULL, XSMEM, GRP, UG1>, args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -863,7 +884,8 @@ static cudaError_t launch_decode_tiled_t(const Problem &p, const Plan &plan, voi
   // fewer, its per-CTA preparation outweighs the leaner loop)
   const int64_t ncg_max = (p.N / 16 + plan.grid - 1) / plan.grid;
   if (tiled_grp(p) && ncg_max * (p.K / 128) >= 8 * TW && tiled_smem(p, plan.grid, true, true) <= cap)
-    return launch_decode_tiled_k<DT, MT, HAS_O, true, true, true>(p, plan, ws, s);
+    return tiled_gu(p) == 2 ? launch_decode_tiled_k<DT, MT, HAS_O, true, true, true, true>(p, plan, ws, s)
+                            : launch_decode_tiled_k<DT, MT, HAS_O, true, true, true, false>(p, plan, ws, s);
   const bool xs = tiled_smem(p, plan.grid, true, false) <= cap;
   if (p.K % 64 == 0)
     return xs ? launch_decode_tiled_k<DT, MT, HAS_O, true, true, false>(p, plan, ws, s)
