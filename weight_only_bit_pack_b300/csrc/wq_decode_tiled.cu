@@ -57,7 +57,7 @@ struct DTArgs {
   const void *scale, *offset, *bias, *residual, *gamma;
   void *y, *normOut;
   uint32_t *status, *gbar;
-  float *ss;          // G x 16 per-CTA sums of y^2
+  float *ss;          // 16 x G per-CTA sums of y^2, row-major by row (a row's CTAs contiguous)
   int M, K, N, KS, NCG, group, Ns, G;
   int gu, GV;         // group-structured loop: k-steps per group, groups along K
   int G_rows;         // scale rows (ceil(K / group) per-group, else 1)
@@ -708,7 +708,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) decode_tiled_kernel(const DTArgs 
     for (int col = lane; col < ncols; col += 32) sq = fmaf(ysm[m * ncols + col], ysm[m * ncols + col], sq);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-    if (lane == 0) __stcg(a.ss + cta * 16 + m, sq);
+    if (lane == 0) __stcg(a.ss + m * a.G + cta, sq);
   }
   __syncthreads();
 
@@ -747,7 +747,7 @@ __global__ void __launch_bounds__(TTHREADS, 1) decode_tiled_kernel(const DTArgs 
 #pragma unroll
     for (int i = 0; i < kTParts; ++i) {
       const int c = lane + 32 * i;
-      pv[i] = c < a.G ? __ldcg(a.ss + c * 16 + warp) : 0.f;
+      pv[i] = c < a.G ? __ldcg(a.ss + warp * a.G + c) : 0.f;
     }
     float tot2 = 0.f;
 #pragma unroll
