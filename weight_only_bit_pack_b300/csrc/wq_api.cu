@@ -284,15 +284,20 @@ int32_t make_plan(const Problem &p, int32_t kernel, Plan &plan) {
     chosen = WQ_KERNEL_GENERIC;
   }
   if (p.tiled) {
-    // the tiled layout: the tiled decode kernel for small M, else the generic kernel
+    // the tiled layout: the tiled decode kernels for small M (the k-major one
+    // for 9..32 rows), else the generic kernel
     if (chosen == WQ_KERNEL_AUTO)
-      chosen = (p.M <= 16 && decode_tiled_applicable(p)) ? WQ_KERNEL_DECODE : WQ_KERNEL_GENERIC;
+      chosen = ((p.M <= 16 && decode_tiled_applicable(p)) || decode_km_applicable(p))
+                   ? WQ_KERNEL_DECODE
+                   : WQ_KERNEL_GENERIC;
     if (chosen == WQ_KERNEL_DECODE) {
       if (!plan_decode_tiled(p, plan))
         return fail(WQ_ERR_UNSUPPORTED,
-                    "the tiled decode kernel needs 1 <= m <= 16, k %% 8 == 0, 16-byte aligned x1, "
+                    "the tiled decode kernels need 1 <= m <= 16, k %% 8 == 0, 16-byte aligned x1, "
                     "scale, offset, bias, residual and gamma, 4-byte aligned y and normOut, and at "
-                    "most 32 column groups of 16 per CTA");
+                    "most 32 column groups of 16 per CTA; or 9 <= m <= 32, k %% 128 == 0, group "
+                    "%% 128 == 0 (or per-channel / per-tensor scales) and at most 14 column "
+                    "groups of 16 per CTA");
       return WQ_OK;
     }
     if (chosen == WQ_KERNEL_PREFILL)

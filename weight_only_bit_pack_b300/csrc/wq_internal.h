@@ -86,6 +86,12 @@ cudaError_t launch_int4_tiled_to_nd(const uint8_t *in, uint8_t *out, int64_t K, 
 cudaError_t launch_int4_remap(const uint8_t *in, int in_layout, uint8_t *out, int out_layout,
                               int64_t K, int64_t N, cudaStream_t s);
 cudaError_t launch_decode_tiled(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
+// k-major decode for tiled INT4 weights with 9..32 rows (wq_decode_km.cu); its
+// plans carry mode kPlanModeKm, and launch_decode_tiled hands them on.
+constexpr int kPlanModeKm = 3;
+bool decode_km_applicable(const Problem &p);
+bool plan_decode_km(const Problem &p, Plan &plan);
+cudaError_t launch_decode_km(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
 // FP4 E2M1 pack and the mx block-scaled matmul (wq_fp4.cu).
 cudaError_t launch_pack_fp4(const float *in, uint8_t *out, int64_t K, int64_t N, cudaStream_t s);
 // x1t: x1 stored (K, M) packed along M and scale1 (ceil(K/32), M). The first
