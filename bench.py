@@ -537,8 +537,8 @@ def time_fp4(wq, dev, stream, steps, warmup, peaks):
 
 
 EXTRA = (("decode", 2000), ("decode@tiled", 2000), ("sweep:1", 1000), ("sweep:1@tiled", 1000),
-         ("sweep:16", 1000), ("sweep:16@tiled", 1000), ("w8a16", 50), ("prefill", 20),
-         ("sweep:4096@transposed", 10))
+         ("sweep:16", 1000), ("sweep:16@tiled", 1000), ("sweep:64", 500), ("sweep:64@tiled", 500),
+         ("w8a16", 50), ("prefill", 20), ("sweep:4096@transposed", 10))
 
 
 def traffic_record(kernel_name, workload):

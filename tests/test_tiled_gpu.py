@@ -112,7 +112,7 @@ CASES = [
     # the general loop with 16 rows, offsets and x1 read from global memory
     ("m16_group128_offset_k8192", dict(M_shape=(16,), K=8192, N=512, dtype=torch.bfloat16,
                                        mode="group", group=128)),
-    # the k-major kernel (9..32 rows, x1 staged per 128-row slice): 16 rows
+    # the k-major kernel (9..64 rows, x1 staged per 128-row slice): 16 rows
     # with >= 8 column groups per CTA, 24 rows (four row blocks, rows past M
     # zero-filled by the copy) with few column groups, 32 rows fp16 with
     # offsets and 256-row groups, per-channel, per-tensor with 9 rows
@@ -126,6 +126,11 @@ CASES = [
                             mode="channel")),
     ("km_m9_tensor_fp16", dict(M_shape=(9,), K=1280, N=20480, dtype=torch.float16,
                                mode="tensor")),
+    # eight row blocks (two passes per slice): 64 rows, and 40 rows fp16 with offsets
+    ("km_m64_group128", dict(M_shape=(64,), K=2048, N=4096, dtype=torch.bfloat16,
+                             mode="group", group=128, offset=False)),
+    ("km_m40_fp16_channel", dict(M_shape=(5, 8), K=1024, N=2048, dtype=torch.float16,
+                                 mode="channel")),
 ]
 
 

@@ -295,7 +295,7 @@ int32_t make_plan(const Problem &p, int32_t kernel, Plan &plan) {
         return fail(WQ_ERR_UNSUPPORTED,
                     "the tiled decode kernels need 1 <= m <= 16, k %% 8 == 0, 16-byte aligned x1, "
                     "scale, offset, bias, residual and gamma, 4-byte aligned y and normOut, and at "
-                    "most 32 column groups of 16 per CTA; or 9 <= m <= 32, k %% 128 == 0, group "
+                    "most 32 column groups of 16 per CTA; or 9 <= m <= 64, k %% 128 == 0, group "
                     "%% 128 == 0 (or per-channel / per-tensor scales) and at most 14 column "
                     "groups of 16 per CTA");
       return WQ_OK;

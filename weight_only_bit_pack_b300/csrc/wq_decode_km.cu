@@ -1,10 +1,10 @@
 // k-major decode kernel of the fused operator for weights in the kernel-native
-// tiled INT4 layout, 9..32 rows (aclnnWeightQuantMatmulAllReduceAddRmsNorm,
+// tiled INT4 layout, 9..64 rows (aclnnWeightQuantMatmulAllReduceAddRmsNorm,
 // "Function description": mm_out = x1 @ (x2*antiquantScale + antiquantOffset)
 // + bias; y = mm_out + residual; normOut = y / RMS(y) * gamma; the tiled
 // weight is the pack's matrix-unit output, aclnnConvertWeightToINT4Pack).
 //
-// With 9..32 rows x1 no longer fits in shared memory whole (8192 k-rows x 32
+// With 9..64 rows x1 no longer fits in shared memory whole (8192 k-rows x 32
 // rows is 512 KB), so every CTA walks K in slices of 128 k-rows and all its
 // warps work on the same slice: the slice of x1 (all rows, 128 k-rows) is
 // copied once per CTA by the TMA into a ring of shared-memory stages and read
@@ -20,7 +20,8 @@
 // Per slice a consumer warp has the two 512-byte tiles of its column group
 // (k-steps 2j, 2j+1), loaded TD slices ahead into registers: each word gives
 // four A registers (136 + q, or 1032 + q in fp16, exactly) of m16n8k16 MMAs
-// with B = x1^T from the staged slice. A scale group is a whole number of
+// with B = x1^T from the staged slice (eight row blocks: two passes of four
+// over the same weight words, converted again per pass). A scale group is a whole number of
 // slices (group % 128 == 0), or the scale is per-channel or per-tensor, so the
 // warp folds every slice's sums at once: tot += S acc + (O - 136 S) d, with the
 // scale (offset) values of its two columns loaded a slice ahead.
@@ -64,7 +65,7 @@ struct KmArgs {
   const void *scale, *offset, *bias, *residual, *gamma;
   void *y, *normOut;
   uint32_t *status, *gbar;
-  float *ss;            // 32 x G per-CTA sums of y^2, row-major by row
+  float *ss;            // 64 x G per-CTA sums of y^2, row-major by row
   int M, K, N, KS2, NCG, group, Ns, G;
   float eps;
   long long budget;
@@ -75,7 +76,7 @@ struct KmArgs {
 template <int MT>
 struct KmLayout {
   static constexpr int MP = 8 * MT;
-  static constexpr int ST = MT == 2 ? 12 : 8;           // x1 slice ring depth
+  static constexpr int ST = MT == 2 ? 12 : (MT == 4 ? 8 : 6);  // x1 slice ring depth
   static constexpr uint32_t XBOX = MP * 128;          // one 64-k box of MP rows
   static constexpr uint32_t XSLOT = 2 * XBOX;         // one 128-k slice
   static constexpr uint32_t RING = ST * XSLOT;
@@ -90,7 +91,7 @@ uint64_t km_smem_t(const Problem &p, int G) {
   return 1024 + KmLayout<MT>::E_OFF + (uint64_t)(p.M + 2) * ncg_max * 16 * 2;
 }
 uint64_t km_smem(const Problem &p, int G, int MT) {
-  return MT == 2 ? km_smem_t<2>(p, G) : km_smem_t<4>(p, G);
+  return MT == 2 ? km_smem_t<2>(p, G) : (MT == 4 ? km_smem_t<4>(p, G) : km_smem_t<8>(p, G));
 }
 
 template <int DT, int MT, bool HAS_O, int TD>
@@ -110,7 +111,7 @@ __global__ void __launch_bounds__(KTHREADS, 1)
   float *rowp = reinterpret_cast<float *>(sm + L::P_OFF);
   constexpr int ST_ = L::ST;
   __shared__ __align__(8) uint64_t s_bar[3 * ST_];  // full, row sums ready, empty
-  __shared__ float s_rstd[32];
+  __shared__ float s_rstd[64];
   __shared__ int s_abort;
   auto FULL = [&](int s) { return smem_u32(&s_bar[s]); };
   auto DRDY = [&](int s) { return smem_u32(&s_bar[ST_ + s]); };
@@ -165,18 +166,18 @@ __global__ void __launch_bounds__(KTHREADS, 1)
   const int xr = ((g & 1) << 2) | (g >> 1);
   // the lane's 16 bytes of x1 row 8 mt + xr, k-rows 32 h + 8 t .. of box q of a
   // stage (128-byte rows, 16-byte chunk c of row r at chunk c ^ (r & 7))
-  auto load_x = [&](uint32_t stage, int q, uint4 (&xb)[MT][2]) {
+  // (half h of the lane's 32 k-rows, row blocks mt0 .. mt0 + NR - 1)
+  auto load_xh = [&](uint32_t stage, int q, int h, int mt0, auto &xh) {
+    constexpr int NR = sizeof(xh) / sizeof(uint4);
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t r = (uint32_t)(8 * mt + xr);
-        const uint32_t addr = stage + (uint32_t)q * L::XBOX + r * 128u +
-                              ((uint32_t)((4 * h + t) ^ xr) << 4);
-        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(xb[mt][h].x), "=r"(xb[mt][h].y), "=r"(xb[mt][h].z), "=r"(xb[mt][h].w)
-                     : "r"(addr));
-      }
+    for (int r = 0; r < NR; ++r) {
+      const uint32_t row = (uint32_t)(8 * (mt0 + r) + xr);
+      const uint32_t addr = stage + (uint32_t)q * L::XBOX + row * 128u +
+                            ((uint32_t)((4 * h + t) ^ xr) << 4);
+      asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(xh[r].x), "=r"(xh[r].y), "=r"(xh[r].z), "=r"(xh[r].w)
+                   : "r"(addr));
+    }
   };
 
   // consumer warps: the folded sums of their 16 columns, then y (kept for normOut)
@@ -212,27 +213,32 @@ __global__ void __launch_bounds__(KTHREADS, 1)
       const int s = j % ST_;
       const uint32_t ph = (uint32_t)((j / ST_) & 1);
       if (!wait_bar_warp(FULL(s), ph, abort_flag, a.status, kKmWhereRowSums)) break;
-      float dd[MT][4];
+      constexpr int DB = MT < 4 ? MT : 4;  // row blocks per pass (registers)
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
+      for (int pp = 0; pp < MT / DB; ++pp) {
+        float dd[DB][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) dd[mt][i] = 0.f;
+        for (int r = 0; r < DB; ++r)
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint4 xb[MT][2];
-        load_x(sb + (uint32_t)s * L::XSLOT, q, xb);
+          for (int i = 0; i < 4; ++i) dd[r][i] = 0.f;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            mma_16816_f<BF>(dd[mt], ONES4, xb[mt][h].x, xb[mt][h].y);
-            mma_16816_f<BF>(dd[mt], ONES4, xb[mt][h].z, xb[mt][h].w);
-          }
-      }
-      if (g == 0) {
+            uint4 xh[DB];
+            load_xh(sb + (uint32_t)s * L::XSLOT, q, h, pp * DB, xh);
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-          *reinterpret_cast<float2 *>(dsl + s * MP + 8 * mt + 2 * t) = make_float2(dd[mt][0], dd[mt][1]);
+            for (int r = 0; r < DB; ++r) {
+              mma_16816_f<BF>(dd[r], ONES4, xh[r].x, xh[r].y);
+              mma_16816_f<BF>(dd[r], ONES4, xh[r].z, xh[r].w);
+            }
+          }
+        if (g == 0) {
+#pragma unroll
+          for (int r = 0; r < DB; ++r)
+            *reinterpret_cast<float2 *>(dsl + s * MP + 8 * (pp * DB + r) + 2 * t) =
+                make_float2(dd[r][0], dd[r][1]);
+        }
       }
       __syncwarp();
       if (lane == 0) {
@@ -287,44 +293,6 @@ __global__ void __launch_bounds__(KTHREADS, 1)
       if (!wait_bar_warp(DRDY(s), ph, abort_flag, a.status, kKmWhereConsumer)) return false;
       if (!wait_bar_warp(FULL(s), ph, abort_flag, a.status, kKmWhereConsumer)) return false;
       const uint32_t stage = sb + (uint32_t)s * L::XSLOT;
-      // one accumulator per k-step of the slice with two row blocks (two
-      // chains of four MMAs each instead of one of eight), one with four
-      // (registers)
-      constexpr int NA = MT == 2 ? 2 : 1;
-      float acc[NA][MT][4];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint4 xb[MT][2];
-        load_x(stage, q, xb);
-        const int qa = NA == 2 ? q : 0;
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int h = jj >> 1, jl = jj & 1;
-          uint32_t aa[4];
-          word_to_a<DT>(jj == 0 ? wbi[q].x : jj == 1 ? wbi[q].y : jj == 2 ? wbi[q].z : wbi[q].w, aa);
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const uint32_t b0 = jl ? xb[mt][h].z : xb[mt][h].x;
-            const uint32_t b1 = jl ? xb[mt][h].w : xb[mt][h].y;
-            if (jj == 0 && (q == 0 || NA == 2))
-              mma_16816_z<BF>(acc[qa][mt], aa, b0, b1);
-            else
-              mma_16816_f<BF>(acc[qa][mt], aa, b0, b1);
-          }
-        }
-      }
-      if constexpr (NA == 2) {
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[0][mt][e] += acc[1][mt][e];
-      }
-      float2 dd[MT];
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-        dd[mt] = *reinterpret_cast<const float2 *>(dsl + s * MP + 8 * mt + 2 * t);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(EMPTY(s));  // the slice and its row sums are read
       const float sl = so ? to_f(sri[0]) : sscal, shi = so ? to_f(sri[1]) : sscal;
       float ol = oscal, ohi = oscal;
       if constexpr (HAS_O) {
@@ -334,13 +302,53 @@ __global__ void __launch_bounds__(KTHREADS, 1)
         }
       }
       const float c0 = fmaf(-C136, sl, ol), c1 = fmaf(-C136, shi, ohi);
+      // passes of RB row blocks; with two row blocks one accumulator per k-step
+      // of the slice (two chains of four MMAs instead of one of eight)
+      constexpr int RB = MT < 4 ? MT : 4, NP = MT / RB;
+      constexpr int NA = MT == 2 ? 2 : 1;
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        tot[mt][0] = fmaf(c0, dd[mt].x, fmaf(sl, acc[0][mt][0], tot[mt][0]));
-        tot[mt][1] = fmaf(c0, dd[mt].y, fmaf(sl, acc[0][mt][1], tot[mt][1]));
-        tot[mt][2] = fmaf(c1, dd[mt].x, fmaf(shi, acc[0][mt][2], tot[mt][2]));
-        tot[mt][3] = fmaf(c1, dd[mt].y, fmaf(shi, acc[0][mt][3], tot[mt][3]));
+      for (int pp = 0; pp < NP; ++pp) {
+        float acc[NA][RB][4];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int qa = NA == 2 ? q : 0;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint4 xh[RB];
+            load_xh(stage, q, h, pp * RB, xh);
+#pragma unroll
+            for (int jl = 0; jl < 2; ++jl) {
+              const int jj = 2 * h + jl;
+              uint32_t aa[4];
+              word_to_a<DT>(jj == 0 ? wbi[q].x : jj == 1 ? wbi[q].y : jj == 2 ? wbi[q].z : wbi[q].w, aa);
+#pragma unroll
+              for (int r = 0; r < RB; ++r) {
+                const uint32_t b0 = jl ? xh[r].z : xh[r].x;
+                const uint32_t b1 = jl ? xh[r].w : xh[r].y;
+                if (jj == 0 && (q == 0 || NA == 2))
+                  mma_16816_z<BF>(acc[qa][r], aa, b0, b1);
+                else
+                  mma_16816_f<BF>(acc[qa][r], aa, b0, b1);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+          const int mt = pp * RB + r;
+          if constexpr (NA == 2) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[0][r][e] += acc[1][r][e];
+          }
+          const float2 dd = *reinterpret_cast<const float2 *>(dsl + s * MP + 8 * mt + 2 * t);
+          tot[mt][0] = fmaf(c0, dd.x, fmaf(sl, acc[0][r][0], tot[mt][0]));
+          tot[mt][1] = fmaf(c0, dd.y, fmaf(sl, acc[0][r][1], tot[mt][1]));
+          tot[mt][2] = fmaf(c1, dd.x, fmaf(shi, acc[0][r][2], tot[mt][2]));
+          tot[mt][3] = fmaf(c1, dd.y, fmaf(shi, acc[0][r][3], tot[mt][3]));
+        }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(EMPTY(s));  // the slice and its row sums are read
       if (j + TD < a.KS2) fetch(j + TD, wbi, sri, ori);
       return true;
     };
@@ -496,13 +504,13 @@ int km_grid(const Problem &p) {
   return ncg < sms ? ncg : sms;
 }
 
-int km_mt(const Problem &p) { return p.M <= 16 ? 2 : 4; }
+int km_mt(const Problem &p) { return p.M <= 16 ? 2 : (p.M <= 32 ? 4 : 8); }
 
 bool km_a16(const void *q) { return q == nullptr || reinterpret_cast<uintptr_t>(q) % 16 == 0; }
 
 template <int DT, int MT, bool HAS_O>
 cudaError_t launch_km_t(const Problem &p, const Plan &plan, void *ws, cudaStream_t s) {
-  constexpr int TD = MT == 2 ? 4 : 2;  // weight slices in flight per warp (registers)
+  constexpr int TD = MT == 2 ? 4 : (MT == 4 ? 2 : 1);  // weight slices in flight per warp (registers)
   const int G = plan.grid;
   const uint32_t smem = (uint32_t)km_smem(p, G, MT);
   static cudaError_t attr_err =
@@ -555,7 +563,7 @@ cudaError_t launch_km_t(const Problem &p, const Plan &plan, void *ws, cudaStream
 }  // namespace
 
 bool decode_km_applicable(const Problem &p) {
-  if (!p.tiled || p.wbits != 4 || p.M < 9 || p.M > 32) return false;
+  if (!p.tiled || p.wbits != 4 || p.M < 9 || p.M > 64) return false;
   if (p.N < 16 || p.N % 16 != 0 || p.K < 128 || p.K % 128 != 0) return false;
   if (p.group != 0 && p.group % 128 != 0) return false;
   const void *v16[] = {p.x1, p.x2, p.bias, p.residual, p.gamma};
@@ -579,7 +587,7 @@ bool plan_decode_km(const Problem &p, Plan &plan) {
   plan.kernel = WQ_KERNEL_DECODE;
   plan.mode = kPlanModeKm;
   plan.grid = km_grid(p);
-  plan.ws_bytes = kWsHeader + (uint64_t)plan.grid * 32 * 4;
+  plan.ws_bytes = kWsHeader + (uint64_t)plan.grid * 64 * 4;
   return true;
 }
 
@@ -589,11 +597,15 @@ cudaError_t launch_decode_km(const Problem &p, const Plan &plan, void *ws, cudaS
   if (p.dtype == WQ_BF16) {
     if (MT == 2) return o ? launch_km_t<WQ_BF16, 2, true>(p, plan, ws, s)
                           : launch_km_t<WQ_BF16, 2, false>(p, plan, ws, s);
-    return o ? launch_km_t<WQ_BF16, 4, true>(p, plan, ws, s) : launch_km_t<WQ_BF16, 4, false>(p, plan, ws, s);
+    if (MT == 4) return o ? launch_km_t<WQ_BF16, 4, true>(p, plan, ws, s)
+                          : launch_km_t<WQ_BF16, 4, false>(p, plan, ws, s);
+    return o ? launch_km_t<WQ_BF16, 8, true>(p, plan, ws, s) : launch_km_t<WQ_BF16, 8, false>(p, plan, ws, s);
   }
   if (MT == 2) return o ? launch_km_t<WQ_F16, 2, true>(p, plan, ws, s)
                         : launch_km_t<WQ_F16, 2, false>(p, plan, ws, s);
-  return o ? launch_km_t<WQ_F16, 4, true>(p, plan, ws, s) : launch_km_t<WQ_F16, 4, false>(p, plan, ws, s);
+  if (MT == 4) return o ? launch_km_t<WQ_F16, 4, true>(p, plan, ws, s)
+                        : launch_km_t<WQ_F16, 4, false>(p, plan, ws, s);
+  return o ? launch_km_t<WQ_F16, 8, true>(p, plan, ws, s) : launch_km_t<WQ_F16, 8, false>(p, plan, ws, s);
 }
 
 }  // namespace wq

@@ -86,7 +86,7 @@ cudaError_t launch_int4_tiled_to_nd(const uint8_t *in, uint8_t *out, int64_t K, 
 cudaError_t launch_int4_remap(const uint8_t *in, int in_layout, uint8_t *out, int out_layout,
                               int64_t K, int64_t N, cudaStream_t s);
 cudaError_t launch_decode_tiled(const Problem &p, const Plan &plan, void *ws, cudaStream_t s);
-// k-major decode for tiled INT4 weights with 9..32 rows (wq_decode_km.cu); its
+// k-major decode for tiled INT4 weights with 9..64 rows (wq_decode_km.cu); its
 // plans carry mode kPlanModeKm, and launch_decode_tiled hands them on.
 constexpr int kPlanModeKm = 3;
 bool decode_km_applicable(const Problem &p);
