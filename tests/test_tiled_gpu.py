@@ -165,9 +165,22 @@ def test_tiled_decode_deterministic_and_reusable_workspace(wq):
     assert int(ws[:2048].sum()) == 0  # grid counters back at zero
 
 
-def test_tiled_decode_timeout_path(wq):
-    prob = inputs.decode("cuda")
+def _timeout_problem(which):
+    if which == "decode":  # the general loop
+        return inputs.decode("cuda")
+    if which == "sweep1":  # the group-structured loop
+        return inputs.sweep(1, device="cuda")
+    # the k-major kernel
+    return inputs.make_problem(M_shape=(24,), K=2048, N=4096, dtype=torch.bfloat16, wbits=4,
+                               mode="group", group=128, seed=5, device="cuda", name="km_timeout")
+
+
+@pytest.mark.parametrize("which", ["decode", "sweep1", "kmajor"])
+def test_tiled_decode_timeout_path(wq, which):
+    prob = _timeout_problem(which)
     w = wq_tiled(prob)
+    assert wq.select_kernel(prob.x1, w, prob.scale, prob.offset, prob.bias, prob.residual,
+                            prob.gamma, prob.eps, prob.group) == wq.Kernel.DECODE
     ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
     wq.set_wait_limits_for_testing(2_000_000, 1)
     try:
