@@ -170,10 +170,15 @@ int32_t wq_convert_int4_layout(const wq_tensor *src, const wq_tensor *dst, void 
  *   x2        WQ_INT8 (K, N) or WQ_INT4 (K, N) packed as described above (N even),
  *             WQ_INT4_TILED (K, N) (N % 16 == 0, 16-byte aligned), or transposed:
  *             WQ_INT8_T / WQ_INT4_T given as (N, K) (K even for INT4_T);
- *             0 <= N <= 65535. A tiled weight runs on the tiled decode kernel for
- *             M <= 16 and on the generic kernel otherwise; a transposed weight
- *             runs on the generic kernel (wq_convert_int4_layout turns an INT4_T
- *             weight into the dense or tiled layout once, for the fast kernels).
+ *             0 <= N <= 65535. A tiled weight runs on the tiled decode kernels
+ *             for M <= 16, and for M <= 64 when K % 128 == 0 and the scales are
+ *             per-tensor, per-channel or in groups of a multiple of 128 rows,
+ *             else on the generic kernel. A transposed INT4 weight with bf16
+ *             per-group scales and no offset runs on the transposed-weight
+ *             prefill kernel for M > 16 (K % 64 == 0, N % 32 == 0); any other
+ *             transposed weight runs on the generic kernel
+ *             (wq_convert_int4_layout turns an INT4_T weight into the dense or
+ *             tiled layout once, for the other fast kernels).
  *   scale     antiquantScale, x1's dtype: (1) per-tensor, (N) or (1, N)
  *             per-channel, (ceil(K/group), N) per-group.
  *   offset    antiquantOffset or NULL; if given, the scale's shape and dtype.
