@@ -131,6 +131,9 @@ CASES = [
                              mode="group", group=128, offset=False)),
     ("km_m40_fp16_channel", dict(M_shape=(5, 8), K=1024, N=2048, dtype=torch.float16,
                                  mode="channel")),
+    # one 128-row slice (fewer slices than the weight ring holds)
+    ("km_m12_k128_channel", dict(M_shape=(12,), K=128, N=20480, dtype=torch.bfloat16,
+                                 mode="channel")),
 ]
 
 
