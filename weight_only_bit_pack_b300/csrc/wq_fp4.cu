@@ -174,28 +174,29 @@ __device__ __forceinline__ float scale_two_step(float acc, int e) {
   return acc * __int_as_float((a + 127) << 23) * __int_as_float((b + 127) << 23);
 }
 
-// One slice of a warp's 64 x 32 tile: two m16n8k16 MMAs deep from the fp16
-// tiles at a_base / b_base, then scaled by the slice's E8M0 bytes (e1s per tile
-// row, e2s per tile column) and added to tot.
-template <bool X1T>
+// One slice of a warp's (16 MTW) x 32 tile: two m16n8k16 MMAs deep from the
+// fp16 tiles at a_base / b_base, then scaled by the slice's E8M0 bytes (e1s per
+// tile row, e2s per tile column) and added to tot.
+template <bool X1T, int MTW = 4>
 __device__ __forceinline__ void mx_slice(uint32_t a_base, uint32_t b_base, const uint8_t *e1s,
-                                         const uint8_t *e2s, bool huge, float (&tot)[4][4][4],
+                                         const uint8_t *e2s, bool huge, float (&tot)[MTW][4][4],
                                          int lane, int wm, int wn) {
   const int g = lane >> 2, t = lane & 3;
-  float acc[4][4][4];
+  constexpr int WR = 16 * MTW;  // the warp's rows
+  float acc[MTW][4][4];
 #pragma unroll
-  for (int a = 0; a < 4; ++a)
+  for (int a = 0; a < MTW; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b)
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.f;
 #pragma unroll
   for (int kk = 0; kk < 2; ++kk) {
-    uint32_t af[4][4], bf[4][2];
+    uint32_t af[MTW][4], bf[4][2];
     const int sub = lane >> 3, r8 = lane & 7;
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      const int mb = wm * 64 + mt * 16;
+    for (int mt = 0; mt < MTW; ++mt) {
+      const int mb = wm * WR + mt * 16;
       if constexpr (X1T) {
         const int k = kk * 16 + r8 + 8 * (sub >> 1), m = mb + 8 * (sub & 1);
         ldmatrix_x4_trans(a_base + (uint32_t)(k * kRowH + m) * 2u, af[mt][0], af[mt][1],
@@ -213,7 +214,7 @@ __device__ __forceinline__ void mx_slice(uint32_t a_base, uint32_t b_base, const
                         bf[2 * np + 1][0], bf[2 * np + 1][1]);
     }
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
+    for (int mt = 0; mt < MTW; ++mt)
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
         mma_16816<false>(acc[mt][nt], af[mt][0], af[mt][1], af[mt][2], af[mt][3], bf[nt][0], bf[nt][1]);
@@ -229,9 +230,9 @@ __device__ __forceinline__ void mx_slice(uint32_t a_base, uint32_t b_base, const
       hc[nt][1] = e8m0_factor(e2s[cb + 1]);
     }
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      const float f0 = e8m0_factor(e1s[wm * 64 + mt * 16 + g]);
-      const float f1 = e8m0_factor(e1s[wm * 64 + mt * 16 + g + 8]);
+    for (int mt = 0; mt < MTW; ++mt) {
+      const float f0 = e8m0_factor(e1s[wm * WR + mt * 16 + g]);
+      const float f1 = e8m0_factor(e1s[wm * WR + mt * 16 + g + 8]);
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         const float h0 = hc[nt][0], h1 = hc[nt][1];
@@ -243,12 +244,12 @@ __device__ __forceinline__ void mx_slice(uint32_t a_base, uint32_t b_base, const
     }
   } else {
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
+    for (int mt = 0; mt < MTW; ++mt)
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const uint32_t e1 = e1s[wm * 64 + mt * 16 + g + 8 * (c >> 1)];
+          const uint32_t e1 = e1s[wm * WR + mt * 16 + g + 8 * (c >> 1)];
           const uint32_t e2 = e2s[wn * 32 + nt * 8 + 2 * t + (c & 1)];
           const float v = (e1 == 255u || e2 == 255u)
                               ? __int_as_float(0x7fc00000)
@@ -365,6 +366,9 @@ constexpr uint32_t kRawA = kGs * 64, kRawB = kGs * 64, kRawS = 2 * kTcT;
 constexpr uint32_t kRawStage = kRawA + kRawB + kRawS;
 constexpr uint32_t kF16Tile = kGs * kRowH * 2;
 constexpr uint32_t kRingSmem = kRing * kRawStage + 4 * kF16Tile;
+// 16 warps of 32 x 32 (the same 128 x 128 CTA tile): half the accumulator
+// registers of a 64 x 32 warp, so twice the warps are resident
+constexpr int kRingThreads = 512;
 
 __device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
@@ -379,7 +383,7 @@ __device__ __forceinline__ void cp_async_wait_group() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kRingThreads, 1)
     mx_mma_ring_kernel(const uint8_t *__restrict__ x1, const uint8_t *__restrict__ s1,
                        const uint8_t *__restrict__ x2, const uint8_t *__restrict__ s2,
                        float *__restrict__ y, int64_t M, int64_t K, int64_t N) {
@@ -389,15 +393,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t fa = raw + kRing * kRawStage;  // two A tiles, then two B tiles
   const uint32_t fb = fa + 2 * kF16Tile;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int wm = warp & 1, wn = warp >> 1;
+  const int wm = warp & 3, wn = warp >> 2;
   const int64_t m0 = (int64_t)blockIdx.y * kTcT, n0 = (int64_t)blockIdx.x * kTcT;
   const int64_t J = (K + kGs - 1) / kGs;
 
   // stage st of the ring: 32 rows x 64 bytes of x1 (threads 0..127) and of x2
   // (threads 128..255), 16 bytes a thread, and the slice's 128 + 128 scale bytes
-  // (threads 0..15); copies past K, M or N read nothing and fill zeros
+  // (threads 0..15); copies past K, M or N read nothing and fill zeros. Every
+  // thread commits one group per stage.
   auto issue = [&](int64_t st) {
-    if (st < J) {
+    if (st < J && tid < 256) {
       const uint32_t slot = raw + (uint32_t)(st % kRing) * kRawStage;
       const int64_t k0 = st * kGs;
       const int row = (tid & 127) >> 2, c = tid & 3;
@@ -422,12 +427,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     cp_async_commit_group();  // one group per stage on every thread, empty or not
   };
-  // raw stage st -> fp16 tiles b: 8 bytes of codes a thread for each operand
+  // raw stage st -> fp16 tiles b: 8 bytes of codes a thread, threads 0..255
+  // for x1 and 256..511 for x2
   auto decode = [&](int64_t st, int b) {
     const uint32_t slot = raw + (uint32_t)(st % kRing) * kRawStage;
-    const int row = tid >> 3, off = (tid & 7) * 8;
-#pragma unroll
-    for (int op = 0; op < 2; ++op) {
+    const int row = (tid & 255) >> 3, off = (tid & 7) * 8;
+    {
+      const int op = tid >> 8;
       uint32_t lo, hi;
       asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];"
                    : "=r"(lo), "=r"(hi)
@@ -446,13 +452,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                    "r"(w[6]), "r"(w[7])
                    : "memory");
     }
-    const uint32_t e = mx_smem[(st % kRing) * kRawStage + kRawA + kRawB + tid];
-    if (e >= 245u && e != 255u) huge[b] = 1;
+    if (tid < 256) {
+      const uint32_t e = mx_smem[(st % kRing) * kRawStage + kRawA + kRawB + tid];
+      if (e >= 245u && e != 255u) huge[b] = 1;
+    }
   };
 
-  float tot[4][4][4];
+  float tot[2][4][4];
 #pragma unroll
-  for (int a = 0; a < 4; ++a)
+  for (int a = 0; a < 2; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b)
 #pragma unroll
@@ -469,8 +477,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int buf = (int)(j & 1);
     issue(j + kRing - 1);
     const uint8_t *es = mx_smem + (j % kRing) * kRawStage + kRawA + kRawB;
-    mx_slice<true>(fa + (uint32_t)buf * kF16Tile, fb + (uint32_t)buf * kF16Tile, es, es + kTcT,
-                   huge[buf] != 0, tot, lane, wm, wn);
+    mx_slice<true, 2>(fa + (uint32_t)buf * kF16Tile, fb + (uint32_t)buf * kF16Tile, es, es + kTcT,
+                      huge[buf] != 0, tot, lane, wm, wn);
     if (j + 1 < J) {
       cp_async_wait_group<kRing - 2>();  // stage j + 1 has landed (this thread's copies)
       if (tid == 0) huge[buf ^ 1] = 0;   // last read a slice ago
@@ -481,12 +489,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   cp_async_wait_group<0>();  // no copy in flight at exit (only empty groups remain)
 #pragma unroll
-  for (int mt = 0; mt < 4; ++mt)
+  for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int64_t m = m0 + wm * 64 + mt * 16 + (lane >> 2) + 8 * (c >> 1);
+        const int64_t m = m0 + wm * 32 + mt * 16 + (lane >> 2) + 8 * (c >> 1);
         const int64_t n = n0 + wn * 32 + nt * 8 + 2 * (lane & 3) + (c & 1);
         if (m < M && n < N) y[m * N + n] += tot[mt][nt][c];
       }
@@ -516,7 +524,7 @@ cudaError_t launch_mx_matmul_add_tc(const uint8_t *x1, const uint8_t *s1, bool x
     static cudaError_t attr = cudaFuncSetAttribute(
         mx_mma_ring_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingSmem);
     if (attr != cudaSuccess) return attr;
-    mx_mma_ring_kernel<<<grid, kTcThreads, kRingSmem, s>>>(x1, s1, x2, s2, y, M, K, N);
+    mx_mma_ring_kernel<<<grid, kRingThreads, kRingSmem, s>>>(x1, s1, x2, s2, y, M, K, N);
   } else if (x1t)
     mx_mma_kernel<true><<<grid, kTcThreads, 0, s>>>(x1, s1, x2, s2, y, M, K, N);
   else
