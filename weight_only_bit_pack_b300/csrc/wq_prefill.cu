@@ -3,8 +3,8 @@
 // "Function description": mm_out = x1 @ (x2*antiquantScale + antiquantOffset)
 // + bias; y = mm_out + residual; normOut = y / RMS(y) * gamma).
 //
-// One persistent CTA per SM walks output tiles of (128 MH) x 256 in
-// row-block-major order, MH = 1 or (INT4 weights, M > 128) 2: with two 128-row
+// One persistent CTA per SM walks output tiles of (128 MH) x 256, row blocks
+// in pairs with their tiles interleaved (tile_coords), MH = 1 or (INT4 weights, M > 128) 2: with two 128-row
 // halves one dequantized INT4 weight tile feeds twice the MMAs (INT8 weights
 // are cheap to dequantize and gain nothing from it). Warp roles (16 warps):
 //   warp 0       TMA producer: x1 tile (128 MH x 64, 128-byte swizzle) and the
@@ -106,11 +106,34 @@ struct PrefillArgs {
   int K, N, group, Ns, nTilesN, kTiles;
   int kTilesX;               // F16EMU with offset: extra k-steps of the offset term (else 0)
   long long nTiles;
+  int mTiles;                // row blocks (TM rows each)
   float eps;
   uint32_t so_bytes;         // F16EMU: bytes of one scale/offset row box (rows x 256 x 4)
   long long budget;          // cycles a row-block wait lasts before it gives up
   uint32_t extra;            // arrivals a row-block wait needs beyond its own (0; > 0 only in tests)
 };
+
+// Tile t -> (row block rb, n-tile nt). Row blocks go in pairs: within a pair
+// the tiles alternate between its two row blocks at the same n-tile, so the
+// two CTAs that run tiles 2i and 2i+1 side by side read one weight tile and
+// the second read hits L2 (the whole INT4 weight nearly fills L2 by itself, so
+// a row-block-major order re-reads most of it from DRAM for every row block).
+// A last unpaired row block runs its n-tiles in order. The tiles of one row
+// block lie within 2 * nTilesN consecutive indices, so with nTilesN <= grid a
+// CTA that has published its current tile only ever waits for a row block
+// whose tiles precede its own next tile, which keeps the waits deadlock-free.
+__device__ __forceinline__ void tile_coords(const PrefillArgs &a, long long t, int &rb, int &nt) {
+  const long long span = 2LL * a.nTilesN;
+  const long long pair = t / span, r = t - pair * span;
+  const int rb0 = (int)(2 * pair);
+  if (rb0 + 1 < a.mTiles) {
+    rb = rb0 + (int)(r & 1);
+    nt = (int)(r >> 1);
+  } else {
+    rb = rb0;
+    nt = (int)r;
+  }
+}
 
 template <int WBITS, int MH, int MODE>
 struct Layout {
@@ -260,7 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     long long it = 0;
     const int kAll = a.kTiles + a.kTilesX;
     for (long long t = blockIdx.x; t < a.nTiles; t += gridDim.x) {
-      const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
+      int rb, nt;
+      tile_coords(a, t, rb, nt);
       for (int ks = 0; ks < kAll; ++ks, ++it) {
         const int s = (int)(it % NR);
         const uint32_t ph = (uint32_t)((it / NR) & 1);
@@ -538,7 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // cover a 256-column tile row with 16-byte accesses), rows of this warp's
     // lane quarter only, whose y this warp stored.
     auto normalize = [&](long long t) -> bool {
-      const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
+      int rb, nt;
+      tile_coords(a, t, rb, nt);
       // wait until every n-tile of this row block published its partial sums
       {
         const uint32_t target = (uint32_t)(kEpiWarps * a.nTilesN) + a.extra;
@@ -621,7 +646,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // main loop before the y pass's boxes read them.
     auto prefetch_residual = [&](long long t) {
       if (t >= a.nTiles) return;
-      const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
+      int rb, nt;
+      tile_coords(a, t, rb, nt);
       const int n0 = nt * BN;
       const T *res = static_cast<const T *>(a.residual);
 #pragma unroll
@@ -648,7 +674,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_residual(blockIdx.x);
     for (long long t = blockIdx.x; t < a.nTiles && ok; t += gridDim.x, ++lt) {
       const int buf = lt % NACC;
-      const int rb = (int)(t / a.nTilesN), nt = (int)(t % a.nTilesN);
+      int rb, nt;
+      tile_coords(a, t, rb, nt);
       const int n0 = nt * BN;
       // this tile's per-column parameters, 8 columns a lane (lane l holds
       // columns n0 + 8l ..), handed to the lanes that need them by shuffles
@@ -975,6 +1002,7 @@ static cudaError_t launch_prefill_t(const Problem &p, const Plan &plan, void *ws
   args.kTiles = (int)((p.K + BK - 1) / BK);
   args.kTilesX = MODE == kF16Emu && p.offset ? plan.ldx / BK : 0;
   args.nTiles = plan.n_tiles * plan.m_tiles;
+  args.mTiles = (int)plan.m_tiles;
   args.eps = p.eps;
   args.budget = wait_budget();
   args.extra = wait_extra_arrivals();
