@@ -112,6 +112,12 @@ PREFILL_EDGE = [
                                         wbits=4, mode="channel")),
     ("int8_bf16_tensor_79_ntiles", dict(M_shape=(200,), K=96, N=79 * 256, dtype=torch.bfloat16,
                                         wbits=8, mode="tensor", bias=False)),
+    # INT8 weights over 79 n-tiles: per-group scales (fp16-operand form with
+    # its offset k-steps) and per-channel scales with offsets, ragged last row block
+    ("int8_halves_bf16_g64_offset", dict(M_shape=(250,), K=192, N=79 * 256,
+                                         dtype=torch.bfloat16, wbits=8, mode="group", group=64)),
+    ("int8_halves_fp16_channel_offset", dict(M_shape=(2, 100), K=128, N=79 * 256,
+                                             dtype=torch.float16, wbits=8, mode="channel")),
 ]
 
 
