@@ -128,6 +128,76 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// The same fp16 copy and row exponent without the offset term's sums, one
+// 256-thread block per row holding the row in registers (R 16-byte vectors a
+// thread, K <= 2048 R): the row is read from memory once instead of twice.
+template <int DT, int R>
+__global__ void __launch_bounds__(256)
+    row_prep_reg_kernel(const typename Elem<DT>::T *__restrict__ x1, int64_t M, int K,
+                        int16_t *__restrict__ e_row, __half *__restrict__ x16) {
+  __shared__ float red[8];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
+    const typename Elem<DT>::T *row = x1 + m * K;
+    uint4 v[R];
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const int k = (j * 256 + tid) * 8;  // K % 8 == 0
+      v[j] = k < K ? *reinterpret_cast<const uint4 *>(row + k) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = unpack2<DT>(w[i]);
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) red[warp] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+    __syncthreads();  // red is rewritten for the next row only after every read
+    const int e = row_exponent(amax);
+    if (tid == 0) e_row[m] = (int16_t)e;
+    __half *out = x16 + m * K;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const int k = (j * 256 + tid) * 8;
+      if (k >= K) break;
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = unpack2<DT>(w[i]);
+        o[i] = pack2<WQ_F16>(scale_pow2(f.x, -e), scale_pow2(f.y, -e));
+      }
+      *reinterpret_cast<uint4 *>(out + k) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+template <int DT>
+cudaError_t launch_row_prep_reg(const Problem &p, int16_t *e_row, __half *x16, cudaStream_t s) {
+  using T = typename Elem<DT>::T;
+  const T *x1 = static_cast<const T *>(p.x1);
+  int64_t blocks = p.M < 1 ? 1 : p.M;
+  const int64_t cap = (int64_t)device_info().sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (p.K <= 2048)
+    row_prep_reg_kernel<DT, 1><<<(unsigned)blocks, 256, 0, s>>>(x1, p.M, (int)p.K, e_row, x16);
+  else if (p.K <= 4096)
+    row_prep_reg_kernel<DT, 2><<<(unsigned)blocks, 256, 0, s>>>(x1, p.M, (int)p.K, e_row, x16);
+  else
+    row_prep_reg_kernel<DT, 4><<<(unsigned)blocks, 256, 0, s>>>(x1, p.M, (int)p.K, e_row, x16);
+  return cudaGetLastError();
+}
+
 // One block covers 32 columns; its 8 warps split the group rows, so every warp
 // load reads 32 consecutive columns (coalesced) and the G loads of a column
 // are spread over 8 warps.
@@ -217,6 +287,9 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_row_prep(const Problem &p, float *rowsum, int16_t *e_row, __half *x16,
                             __nv_bfloat16 *dext, int ldx, cudaStream_t s) {
+  if (x16 && !rowsum && !dext && p.K <= 8192)
+    return p.dtype == WQ_BF16 ? launch_row_prep_reg<WQ_BF16>(p, e_row, x16, s)
+                              : launch_row_prep_reg<WQ_F16>(p, e_row, x16, s);
   const int64_t warps_needed = p.M;
   int64_t blocks = (warps_needed * 32 + 255) / 256;
   const int64_t cap = (int64_t)device_info().sms * 8;
