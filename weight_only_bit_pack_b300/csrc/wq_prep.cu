@@ -128,13 +128,14 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// The same fp16 copy and row exponent without the offset term's sums, one
-// 256-thread block per row holding the row in registers (R 16-byte vectors a
-// thread, K <= 2048 R): the row is read from memory once instead of twice.
+// The same fp16 copy, row exponent and (dext) group sums, one 256-thread block
+// per row holding the row in registers (R 16-byte vectors a thread, K <= 2048 R):
+// the row is read from memory once instead of twice.
 template <int DT, int R>
 __global__ void __launch_bounds__(256)
     row_prep_reg_kernel(const typename Elem<DT>::T *__restrict__ x1, int64_t M, int K,
-                        int16_t *__restrict__ e_row, __half *__restrict__ x16) {
+                        int16_t *__restrict__ e_row, __half *__restrict__ x16,
+                        __nv_bfloat16 *__restrict__ dext, int group, int G, int ldx) {
   __shared__ float red[8];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
@@ -179,22 +180,53 @@ __global__ void __launch_bounds__(256)
       }
       *reinterpret_cast<uint4 *>(out + k) = make_uint4(o[0], o[1], o[2], o[3]);
     }
+    if (dext) {
+      // per-group sums of the fp16 row just written, a thread per group, in
+      // ascending k (the block's own stores: __syncthreads orders them first)
+      __syncthreads();
+      __nv_bfloat16 *drow = dext + m * ldx;
+      for (int gi = tid; gi < G; gi += 256) {
+        const int k0 = gi * group, k1 = k0 + group < K ? k0 + group : K;
+        float d = 0.f;
+        for (int k = k0; k < k1; k += 8) {  // group % 32 == 0 and K % 8 == 0
+          const uint4 u = *reinterpret_cast<const uint4 *>(out + k);
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = unpack2<WQ_F16>(w[i]);
+            d += f.x;
+            d += f.y;
+          }
+        }
+        // d = hi + lo to 2^-18, each bf16 (the difference d - hi is exact in fp32)
+        const __nv_bfloat16 hi = __float2bfloat16_rn(d);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(d - __bfloat162float(hi));
+        drow[gi] = hi;
+        drow[G + gi] = lo;
+      }
+      for (int j = 2 * G + tid; j < ldx; j += 256) drow[j] = __float2bfloat16_rn(0.f);
+    }
   }
 }
 
 template <int DT>
-cudaError_t launch_row_prep_reg(const Problem &p, int16_t *e_row, __half *x16, cudaStream_t s) {
+cudaError_t launch_row_prep_reg(const Problem &p, int16_t *e_row, __half *x16,
+                                __nv_bfloat16 *dext, int ldx, cudaStream_t s) {
   using T = typename Elem<DT>::T;
   const T *x1 = static_cast<const T *>(p.x1);
   int64_t blocks = p.M < 1 ? 1 : p.M;
   const int64_t cap = (int64_t)device_info().sms * 8;
   if (blocks > cap) blocks = cap;
+  const int K = (int)p.K, group = (int)p.group, G = (int)p.G;
   if (p.K <= 2048)
-    row_prep_reg_kernel<DT, 1><<<(unsigned)blocks, 256, 0, s>>>(x1, p.M, (int)p.K, e_row, x16);
+    row_prep_reg_kernel<DT, 1><<<(unsigned)blocks, 256, 0, s>>>(x1, p.M, K, e_row, x16, dext,
+                                                                group, G, ldx);
   else if (p.K <= 4096)
-    row_prep_reg_kernel<DT, 2><<<(unsigned)blocks, 256, 0, s>>>(x1, p.M, (int)p.K, e_row, x16);
+    row_prep_reg_kernel<DT, 2><<<(unsigned)blocks, 256, 0, s>>>(x1, p.M, K, e_row, x16, dext,
+                                                                group, G, ldx);
   else
-    row_prep_reg_kernel<DT, 4><<<(unsigned)blocks, 256, 0, s>>>(x1, p.M, (int)p.K, e_row, x16);
+    row_prep_reg_kernel<DT, 4><<<(unsigned)blocks, 256, 0, s>>>(x1, p.M, K, e_row, x16, dext,
+                                                                group, G, ldx);
   return cudaGetLastError();
 }
 
@@ -287,9 +319,9 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_row_prep(const Problem &p, float *rowsum, int16_t *e_row, __half *x16,
                             __nv_bfloat16 *dext, int ldx, cudaStream_t s) {
-  if (x16 && !rowsum && !dext && p.K <= 8192)
-    return p.dtype == WQ_BF16 ? launch_row_prep_reg<WQ_BF16>(p, e_row, x16, s)
-                              : launch_row_prep_reg<WQ_F16>(p, e_row, x16, s);
+  if (x16 && !rowsum && p.K <= 8192)
+    return p.dtype == WQ_BF16 ? launch_row_prep_reg<WQ_BF16>(p, e_row, x16, dext, ldx, s)
+                              : launch_row_prep_reg<WQ_F16>(p, e_row, x16, dext, ldx, s);
   const int64_t warps_needed = p.M;
   int64_t blocks = (warps_needed * 32 + 255) / 256;
   const int64_t cap = (int64_t)device_info().sms * 8;
