@@ -47,3 +47,15 @@ def test_dynamic_quant_ties_zero_and_nonfinite_rows(wq):
         x = torch.tensor(rows, dtype=dt, device="cuda")
         for bits in (8, 4):
             _check(wq, x, None, bits)
+
+
+def test_dynamic_quant_tiny_and_huge_scales(wq):
+    """bf16 keeps fp32's exponent range: a row maximum near 1e-38 gives a
+    subnormal scale (codes from the IEEE quotient itself), near 1e-30 and 1e36
+    normal scales with their reciprocals far from 1."""
+    rows = [[1e-38, -5e-39, 3e-39, 0, 2.5e-39, -7.5e-39, 1e-40, 6e-39],
+            [1e-30, -3.3e-31, 5e-31, 0, 2e-31, -7.9e-31, 1e-32, 6.1e-31],
+            [1e36, -3.3e35, 5e35, 0, 2e35, -7.9e35, 1e34, 6.1e35]]
+    x = torch.tensor(rows, dtype=torch.bfloat16, device="cuda")
+    for bits in (8, 4):
+        _check(wq, x, None, bits)
